@@ -1,0 +1,71 @@
+"""torch-tensor helpers around the C ABI: allocate device buffers and the workspace, call.
+
+torch supplies device memory and the stream; every step of the computation runs in libmk.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import mk
+
+_TORCH_OUT = {mk.MK_BF16: torch.bfloat16, mk.MK_F32: torch.float32}
+
+
+def bf16_device(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """Upload a uint16 array of bf16 bit patterns as a contiguous bf16 device tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(bits)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def workspace(op: int, P: int, M: int, N: int, K_per_rank: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace of the size the op needs (torch allocations are 512-byte aligned)."""
+    n = mk.mk_workspace_size(op, P, M, N, K_per_rank)
+    if n == 0:
+        raise ValueError("invalid shape for mk_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def make_opts(split_mode=mk.MK_SPLIT_ADAPTIVE, comm_sms=0, timeout_ns=0, trace=None, num_ctas=0,
+              flags=0, skip_unit=-1) -> mk.mk_opts:
+    o = mk.mk_opts_default()
+    o.split_mode = split_mode
+    o.comm_sms = comm_sms
+    if timeout_ns:
+        o.wait_timeout_ns = timeout_ns
+    if trace is not None:
+        o.trace = trace.data_ptr()
+        o.trace_bytes = trace.numel() * trace.element_size()
+    o.num_ctas = num_ctas
+    o.flags = flags
+    o.debug_skip_unit = skip_unit
+    return o
+
+
+def gemm_allreduce(A, B, out_dtype=mk.MK_BF16, C=None, ws=None, opts=None, stream=None):
+    """C = sum_r A[r] @ B[r] via mk_gemm_allreduce.  Returns (C, status).  C may be one tensor
+    (every rank shares it) or a list of P tensors."""
+    P = len(A)
+    M, Kr = A[0].shape
+    N = B[0].shape[1]
+    if C is None:
+        C = torch.empty((M, N), dtype=_TORCH_OUT[out_dtype], device=A[0].device)
+    Cs = C if isinstance(C, (list, tuple)) else [C] * P
+    if ws is None:
+        ws = workspace(mk.MK_OP_ALLREDUCE, P, M, N, Kr, A[0].device)
+    st = mk.mk_gemm_allreduce(P, M, N, Kr, A, B, Cs, out_dtype, ws, opts=opts, stream=stream)
+    return C, st
+
+
+def gemm_reducescatter(A, B, out_dtype=mk.MK_BF16, shards=None, ws=None, opts=None, stream=None):
+    """Row shard s of sum_r A[r] @ B[r] into shards[s] via mk_gemm_reducescatter."""
+    P = len(A)
+    M, Kr = A[0].shape
+    N = B[0].shape[1]
+    if shards is None:
+        shards = [torch.empty((M // P, N), dtype=_TORCH_OUT[out_dtype], device=A[0].device)
+                  for _ in range(P)]
+    if ws is None:
+        ws = workspace(mk.MK_OP_REDUCESCATTER, P, M, N, Kr, A[0].device)
+    st = mk.mk_gemm_reducescatter(P, M, N, Kr, A, B, shards, out_dtype, ws, opts=opts, stream=stream)
+    return shards, st

@@ -1,0 +1,301 @@
+// mk_abi.cu -- host side of libmk.so: argument validation, workspace layout, TMA
+// tensor-map encoding and the launches behind the extern "C" entry points of mk.h.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "mk.h"
+#include "mk_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+mk_status fail(mk_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+mk_status fail_cuda(cudaError_t e, const char *what) {
+    return fail(MK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kRasterGroup = 8;
+constexpr int kCtrlPeriodNs = 1000;
+
+int choose_bn(int64_t N) { return N > 128 ? 256 : 128; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Geometry {
+    int bn;
+    int64_t tiles_m, tiles_n, num_tiles, num_units, num_kb;
+    size_t flags_off, partials_off, total;
+};
+
+bool make_geometry(int P, int64_t M, int64_t N, int64_t Kr, Geometry *g) {
+    if (P < 1 || P > MK_MAX_P || M < 0 || N < 0 || Kr < 0) return false;
+    g->bn = choose_bn(N);
+    g->tiles_m = (M + MK_BM - 1) / MK_BM;
+    g->tiles_n = (N + g->bn - 1) / g->bn;
+    g->num_tiles = g->tiles_m * g->tiles_n;
+    g->num_units = g->num_tiles * P;
+    g->num_kb = (Kr + MK_BK - 1) / MK_BK;
+    g->flags_off = MK_WS_HEADER_BYTES;
+    g->partials_off = align_up(g->flags_off + static_cast<size_t>(g->num_units) * sizeof(uint32_t), MK_WS_ALIGN);
+    g->total = g->partials_off + static_cast<size_t>(g->num_units) * MK_BM * g->bn * sizeof(float);
+    return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// bf16 row-major matrix rows x cols, TMA box {box_cols (inner), box_rows}, 128-byte swizzle,
+// out-of-bounds elements filled with zero.
+mk_status encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return MK_OK;
+}
+
+// Shape of a reduce-role cost relative to a compute unit, used for the first target before
+// the controller has measurements: per-SM tensor rate ~11 TFLOP/s, per-SM streaming rate
+// ~120 GB/s.  Only the ratio matters.
+int initial_reduce_ctas(int S, int P, int bn, int64_t Kr) {
+    const double t_unit = 2.0 * MK_BM * bn * static_cast<double>(Kr) / 11e12;
+    const double t_tile = static_cast<double>(P) * MK_BM * bn * 4.0 / 120e9;
+    int nr = static_cast<int>(S * t_tile / (P * t_unit + t_tile) + 0.5);
+    if (nr < 1) nr = 1;
+    if (nr > S - 1) nr = S - 1;
+    return nr;
+}
+
+mk_status check_opts(const mk_opts *o) {
+    if (o->split_mode < MK_SPLIT_ADAPTIVE || o->split_mode > MK_SPLIT_UNFUSED)
+        return fail(MK_ERR_INVALID_ARG, "split_mode %d out of range", o->split_mode);
+    if (o->split_mode == MK_SPLIT_STATIC && o->comm_sms < 1)
+        return fail(MK_ERR_INVALID_ARG, "static split needs comm_sms >= 1");
+    if (o->comm_sms < 0) return fail(MK_ERR_INVALID_ARG, "comm_sms < 0");
+    if (o->num_ctas < 0) return fail(MK_ERR_INVALID_ARG, "num_ctas < 0");
+    if (o->trace_bytes && !o->trace) return fail(MK_ERR_INVALID_ARG, "trace_bytes without trace buffer");
+    if (o->trace && !aligned16(o->trace)) return fail(MK_ERR_ALIGNMENT, "trace buffer not 16-byte aligned");
+    return MK_OK;
+}
+
+// Shared front half of the two row-parallel ops.
+mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const void *const *A,
+                          const void *const *B, void *const *C, mk_dtype out_dtype, void *ws, size_t ws_bytes,
+                          const mk_opts *opts_in, void *stream) {
+    g_last_error[0] = '\0';
+    if (P < 1 || P > MK_MAX_P) return fail(MK_ERR_INVALID_ARG, "P=%d outside [1, %d]", P, MK_MAX_P);
+    if (M < 0 || N < 0 || Kr < 0) return fail(MK_ERR_INVALID_ARG, "negative dimension");
+    if (out_dtype != MK_BF16 && out_dtype != MK_F32) return fail(MK_ERR_INVALID_ARG, "unknown out_dtype");
+    if (!A || !B || !C || !ws) return fail(MK_ERR_INVALID_ARG, "null pointer array or workspace");
+    mk_opts o;
+    mk_opts_default(&o);
+    if (opts_in) o = *opts_in;
+    mk_status st = check_opts(&o);
+    if (st != MK_OK) return st;
+    if (N % 8 || Kr % 8) return fail(MK_ERR_UNSUPPORTED_SHAPE, "N=%lld and K_per_rank=%lld must be multiples of 8",
+                                     (long long)N, (long long)Kr);
+    if (M > INT32_MAX || N > INT32_MAX || Kr > INT32_MAX)
+        return fail(MK_ERR_UNSUPPORTED_SHAPE, "dimension above 2^31-1");
+    if (op == MK_IOP_RS && M % P) return fail(MK_ERR_UNSUPPORTED_SHAPE, "M=%lld not divisible by P=%d", (long long)M, P);
+    Geometry g;
+    make_geometry(P, M, N, Kr, &g);
+    if (g.num_units > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "too many tiles");
+    if (M == 0 || N == 0) return MK_OK;   // nothing to read or write
+    for (int r = 0; r < P; ++r) {
+        if (!C[r]) return fail(MK_ERR_INVALID_ARG, "C[%d] is null", r);
+        if (!aligned16(C[r])) return fail(MK_ERR_ALIGNMENT, "C[%d] not 16-byte aligned", r);
+        if (Kr > 0) {
+            if (!A[r] || !B[r]) return fail(MK_ERR_INVALID_ARG, "A[%d] or B[%d] is null", r, r);
+            if (!aligned16(A[r]) || !aligned16(B[r])) return fail(MK_ERR_ALIGNMENT, "A[%d]/B[%d] not 16-byte aligned", r, r);
+        }
+    }
+    if (reinterpret_cast<uintptr_t>(ws) % MK_WS_ALIGN) return fail(MK_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    if (ws_bytes < g.total)
+        return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, g.total);
+
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+    e = mk_max_persistent_ctas(g.bn, &per_sm);
+    if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
+    const int resident = sms * per_sm;
+    const int S = o.num_ctas > 0 ? o.num_ctas : resident;
+    if (S > resident || S < 2)
+        return fail(MK_ERR_NOT_RESIDENT, "persistent grid of %d blocks cannot be co-resident (%d fit)", S, resident);
+    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > S - 1)
+        return fail(MK_ERR_INVALID_ARG, "comm_sms=%d must be below the grid size %d", o.comm_sms, S);
+
+    MkParams p;
+    memset(&p, 0, sizeof p);
+    for (int r = 0; r < P && Kr > 0; ++r) {
+        st = encode_2d(&p.tmA[r], A[r], M, Kr, MK_BK, MK_BM);
+        if (st != MK_OK) return st;
+        st = encode_2d(&p.tmB[r], B[r], Kr, N, 64, MK_BK);
+        if (st != MK_OK) return st;
+    }
+    if (op == MK_IOP_RS) {
+        for (int r = 0; r < P; ++r) p.out[r] = C[r];
+        p.num_out = P;
+    } else {
+        int n = 0;
+        for (int r = 0; r < P; ++r) {
+            bool seen = false;
+            for (int q = 0; q < n; ++q) seen = seen || (p.out[q] == C[r]);
+            if (!seen) p.out[n++] = C[r];
+        }
+        p.num_out = n;
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    p.hdr = reinterpret_cast<MkWsHeader *>(wsb);
+    p.flags = reinterpret_cast<uint32_t *>(wsb + g.flags_off);
+    p.partials = reinterpret_cast<float *>(wsb + g.partials_off);
+    p.trace = o.trace;
+    p.trace_cap = static_cast<uint32_t>(o.trace_bytes / sizeof(mk_trace_record));
+    p.skip_unit = o.debug_skip_unit;
+    p.timeout_ns = o.wait_timeout_ns ? o.wait_timeout_ns : kDefaultTimeoutNs;
+    p.P = P;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.Kr = static_cast<int32_t>(Kr);
+    p.tiles_m = static_cast<int32_t>(g.tiles_m);
+    p.tiles_n = static_cast<int32_t>(g.tiles_n);
+    p.num_tiles = static_cast<int32_t>(g.num_tiles);
+    p.num_units = static_cast<int32_t>(g.num_units);
+    p.num_kb = static_cast<int32_t>(g.num_kb);
+    p.op = op;
+    p.out_bf16 = out_dtype == MK_BF16;
+    p.rows_per_shard = static_cast<int32_t>(M / P);
+    p.static_nr = o.comm_sms;
+    p.init_nr = o.comm_sms > 0 ? (o.comm_sms < S ? o.comm_sms : S - 1) : initial_reduce_ctas(S, P, g.bn, Kr);
+    p.raster_group = kRasterGroup;
+    p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
+    p.ctrl_period_ns = kCtrlPeriodNs;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (o.split_mode == MK_SPLIT_UNFUSED) {
+        p.mode = MK_MODE_COMPUTE_ONLY;
+        e = mk_launch_persistent(p, g.bn, S, s);
+        if (e != cudaSuccess) return fail_cuda(e, "launch of the per-rank GEMM kernel");
+        e = mk_launch_reduce(p, g.bn, S, s);
+        if (e != cudaSuccess) return fail_cuda(e, "launch of the reduce kernel");
+        return MK_OK;
+    }
+    p.mode = o.split_mode == MK_SPLIT_STATIC ? MK_MODE_STATIC : MK_MODE_ADAPTIVE;
+    e = mk_launch_persistent(p, g.bn, S, s);
+    if (e != cudaSuccess) return fail_cuda(e, "launch of the fused kernel");
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mk_opts_default(mk_opts *o) {
+    if (!o) return;
+    memset(o, 0, sizeof *o);
+    o->split_mode = MK_SPLIT_ADAPTIVE;
+    o->comm_sms = 0;
+    o->wait_timeout_ns = kDefaultTimeoutNs;
+    o->trace = nullptr;
+    o->trace_bytes = 0;
+    o->num_ctas = 0;
+    o->flags = 0;
+    o->debug_skip_unit = -1;
+}
+
+size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank) {
+    Geometry g;
+    if (op == MK_OP_ALLREDUCE || op == MK_OP_REDUCESCATTER) {
+        if (!make_geometry(P, M, N, K_per_rank, &g)) return 0;
+        return g.total;
+    }
+    return 0;
+}
+
+mk_status mk_gemm_allreduce(int P, int64_t M, int64_t N, int64_t K_per_rank, const void *const *A,
+                            const void *const *B, void *const *C, mk_dtype out_dtype, void *ws, size_t ws_bytes,
+                            const mk_opts *opts, void *cuda_stream) {
+    return run_rowparallel(MK_IOP_AR, P, M, N, K_per_rank, A, B, C, out_dtype, ws, ws_bytes, opts, cuda_stream);
+}
+
+mk_status mk_gemm_reducescatter(int P, int64_t M, int64_t N, int64_t K_per_rank, const void *const *A,
+                                const void *const *B, void *const *C_shard, mk_dtype out_dtype, void *ws,
+                                size_t ws_bytes, const mk_opts *opts, void *cuda_stream) {
+    return run_rowparallel(MK_IOP_RS, P, M, N, K_per_rank, A, B, C_shard, out_dtype, ws, ws_bytes, opts,
+                           cuda_stream);
+}
+
+mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *const *A_shard,
+                            const void *const *B, void *const *A_gathered, void *const *C, mk_dtype out_dtype,
+                            void *ws, size_t ws_bytes, const mk_opts *opts, void *cuda_stream) {
+    (void)P; (void)M; (void)N; (void)K; (void)A_shard; (void)B; (void)A_gathered; (void)C; (void)out_dtype;
+    (void)ws; (void)ws_bytes; (void)opts; (void)cuda_stream;
+    return fail(MK_ERR_UNSUPPORTED_SHAPE, "mk_allgather_gemm: not available in this build");
+}
+
+mk_status mk_status_check(void *ws, void *cuda_stream) {
+    g_last_error[0] = '\0';
+    if (!ws) return fail(MK_ERR_INVALID_ARG, "null workspace");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    MkWsHeader h;
+    e = cudaMemcpy(&h, ws, 64, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "reading the workspace status");
+    if (h.status == MK_OK) return MK_OK;
+    const uint32_t zero = 0;
+    e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e, "clearing the workspace status");
+    return fail(static_cast<mk_status>(h.status), "device reported %s (wait site %u, index %u)",
+                mk_status_string(static_cast<mk_status>(h.status)), h.err_site, h.err_index);
+}
+
+const char *mk_status_string(mk_status s) {
+    switch (s) {
+        case MK_OK: return "ok";
+        case MK_ERR_INVALID_ARG: return "invalid argument";
+        case MK_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MK_ERR_ALIGNMENT: return "misaligned pointer";
+        case MK_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MK_ERR_CUDA: return "CUDA error";
+        case MK_ERR_TIMEOUT: return "device wait timed out";
+        case MK_ERR_INTERNAL: return "internal error";
+        case MK_ERR_NOT_RESIDENT: return "persistent grid not co-resident";
+    }
+    return "unknown status";
+}
+
+const char *mk_last_error(void) { return g_last_error; }
+
+}  // extern "C"

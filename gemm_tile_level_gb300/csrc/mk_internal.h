@@ -1,0 +1,80 @@
+// mk_internal.h -- layout shared by the host ABI (mk_abi.cu) and the kernels
+// (mk_kernels.cu): launch parameters and the workspace header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define MK_MAX_P 16
+
+// Output tile of one compute unit is BM x BN; K is consumed in BK slices.
+#define MK_BM 128
+#define MK_BK 64
+
+// Persistent kernel block: warp 0 schedules and issues TMA loads, warp 1 issues
+// tcgen05.mma (and owns the TMEM allocation), warps 2..9 drain accumulators and
+// run the reduce role, warp 10 hosts the split controller (block 0 only).
+#define MK_THREADS 352
+#define MK_EPI_THREADS 256
+#define MK_EPI_WARP0 2
+#define MK_CTRL_WARP 10
+
+// Workspace layout: [header 256 B][flags][partials]
+#define MK_WS_HEADER_BYTES 256
+#define MK_WS_ALIGN 256
+
+enum MkMode {
+    MK_MODE_ADAPTIVE = 0,   // fused, controller publishes the split
+    MK_MODE_STATIC = 1,     // fused, fixed split
+    MK_MODE_COMPUTE_ONLY = 2 // unfused baseline, first kernel
+};
+
+enum MkOpInternal { MK_IOP_AR = 0, MK_IOP_RS = 1 };
+
+// Lives at the start of the workspace; zero-initialised once by the caller.
+struct MkWsHeader {
+    uint32_t status;        // first device-side error (mk_status), sticky until checked
+    uint32_t epoch;         // value the last completed call wrote into the readiness flags
+    uint32_t abort;         // set with status; every block stops claiming work
+    uint32_t done_ctas;     // blocks finished in the current call
+    uint32_t compute_next;  // next compute unit to claim
+    uint32_t reduce_next;   // next output tile to claim for reduction
+    uint32_t target_nr;     // published number of reduce-role blocks (0 = not yet published)
+    uint32_t units_done;    // compute units whose partial tile is released
+    uint32_t tiles_done;    // output tiles reduced and written
+    uint32_t trace_count;   // controller records written
+    uint64_t compute_busy;  // SM cycles spent issuing compute units (sum over blocks)
+    uint64_t reduce_busy;   // SM cycles spent reducing ready tiles (sum over blocks)
+    uint32_t err_site;      // which wait gave up (diagnostic)
+    uint32_t err_index;     // the unit / tile it was waiting for (diagnostic)
+    uint32_t pad[(MK_WS_HEADER_BYTES - 64) / 4];
+};
+static_assert(sizeof(MkWsHeader) == MK_WS_HEADER_BYTES, "workspace header size");
+
+// Launch parameters, passed as one __grid_constant__ kernel argument.
+struct MkParams {
+    CUtensorMap tmA[MK_MAX_P];   // A_r: dims {K_r, M}, box {64, 128}, 128-byte swizzle
+    CUtensorMap tmB[MK_MAX_P];   // B_r: dims {N, K_r}, box {64, 64}, 128-byte swizzle
+    void *out[MK_MAX_P];         // AR: distinct result buffers; RS: the P shards
+    MkWsHeader *hdr;
+    uint32_t *flags;             // [num_tiles][P] readiness flags (epoch-valued)
+    float *partials;             // [P][num_tiles][BM*BN] fp32 partial tiles
+    void *trace;                 // controller records or null
+    int64_t skip_unit;           // fault injection (-1 = off)
+    uint64_t timeout_ns;
+    uint32_t trace_cap;          // records that fit in trace
+    int32_t P, M, N, Kr;
+    int32_t tiles_m, tiles_n, num_tiles, num_units, num_kb;
+    int32_t op, out_bf16, num_out, rows_per_shard;
+    int32_t mode, static_nr, init_nr, raster_group;
+    int32_t discard;
+    int32_t ctrl_period_ns;
+};
+
+// Implemented in mk_kernels.cu
+size_t mk_persistent_smem_bytes(int bn);
+cudaError_t mk_prepare_kernels(int bn);
+cudaError_t mk_max_persistent_ctas(int bn, int *ctas_per_sm);
+cudaError_t mk_launch_persistent(const MkParams &p, int bn, int num_ctas, cudaStream_t s);
+cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s);

@@ -1,0 +1,190 @@
+/*
+ * mk.h -- C ABI of libmk.so: tile-granular fused GEMM + collective kernels of
+ * row- and column-parallel tensor parallelism, run on one GB300 (sm_103a)
+ * with the P logical ranks held in separate HBM partitions of that GPU.
+ *
+ * The operations are the three tensor-parallel kernels of
+ * "mKernel: Fast Multi-GPU, Multi-Node Fused Kernels", Table 3:
+ *   GEMM + AllReduce      (compute -> communication; every rank gets C)
+ *   GEMM + ReduceScatter  (compute -> communication; rank s gets row shard s)
+ *   AllGather + GEMM      (communication -> compute; row shards of A gathered)
+ * and the persistent-kernel design of its Figure 2: thread blocks take a
+ * compute role (write finished tiles to GPU memory and set readiness flags) or
+ * a communication role (observe the flags and reduce / move the tiles), and an
+ * optional on-GPU controller reads progress counters and publishes the target
+ * number of communication blocks (abstract; Figure 2, dashed arrow; Figure 7).
+ *
+ * Conventions shared by every entry point
+ *   - All matrices are row-major with no padding (leading dimension = number
+ *     of columns).  bf16 operands; fp32 accumulation; bf16 or fp32 output.
+ *   - Pointer-array arguments (A, B, C, ...) are HOST arrays of P DEVICE
+ *     pointers, one per logical rank.  Every device pointer must be 16-byte
+ *     aligned (TMA requirement) and belong to the current CUDA device.
+ *   - The caller owns every device buffer (operands, outputs, workspace).  The
+ *     library allocates no device memory and keeps no per-call host state; it
+ *     caches only the driver's tensor-map encoder entry point.
+ *   - Calls are asynchronous and stream-ordered on `cuda_stream` (a
+ *     cudaStream_t, NULL = legacy default stream).  Calls that share one
+ *     workspace must be ordered on the GPU (same stream or explicit events).
+ *   - Synchronous argument errors return a non-zero mk_status and launch
+ *     nothing.  Errors found by the kernel (a bounded wait that ran out, an
+ *     internal inconsistency) are written to the workspace status word; the
+ *     kernel then exits cleanly.  mk_status_check() reports (and clears) it.
+ *   - Supported sizes: 1 <= P <= 16; M, N, K >= 0; N and K (per rank) must be
+ *     multiples of 8 (16-byte row pitch for TMA).  M == 0 or N == 0 is a
+ *     no-op.  K == 0 yields C = 0.  Ragged tails of M and N (not multiples of
+ *     the 128 x 256 output tile) and of K (not a multiple of 64) are handled.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = 1,        /* null pointer, P out of range, bad option value */
+    MK_ERR_UNSUPPORTED_SHAPE = 2,  /* N or K not a multiple of 8, M not divisible by P (RS/AG), too large */
+    MK_ERR_ALIGNMENT = 3,          /* a device pointer not 16-byte aligned, workspace not 256-byte aligned */
+    MK_ERR_WORKSPACE_TOO_SMALL = 4,/* ws_bytes < mk_workspace_size(...) */
+    MK_ERR_CUDA = 5,               /* a CUDA runtime/driver call or the launch failed (see mk_last_error) */
+    MK_ERR_TIMEOUT = 6,            /* device side: a bounded wait ran out (wait_timeout_ns) */
+    MK_ERR_INTERNAL = 7,           /* device side: inconsistent state detected */
+    MK_ERR_NOT_RESIDENT = 8        /* the persistent grid cannot be co-resident on this device */
+} mk_status;
+
+typedef enum { MK_BF16 = 0, MK_F32 = 1 } mk_dtype;
+
+typedef enum { MK_OP_ALLREDUCE = 0, MK_OP_REDUCESCATTER = 1, MK_OP_ALLGATHER_GEMM = 2 } mk_op;
+
+typedef enum {
+    MK_SPLIT_ADAPTIVE = 0, /* on-GPU controller publishes the reduce-role block count at run time */
+    MK_SPLIT_STATIC = 1,   /* comm_sms blocks hold the communication role for the whole call */
+    MK_SPLIT_UNFUSED = 2   /* baseline: one kernel computes every per-rank tile, a second kernel reduces */
+} mk_split_mode;
+
+/* Bits of mk_opts.flags */
+#define MK_FLAG_KEEP_PARTIALS 1u /* do not discard consumed partial tiles from L2 (default: discard) */
+
+/*
+ * Options.  Start from mk_opts_default() and change fields; a NULL mk_opts*
+ * means the defaults.
+ *   split_mode      : mk_split_mode.
+ *   comm_sms        : MK_SPLIT_STATIC: number of communication-role blocks,
+ *                     1 <= comm_sms < persistent grid size.  MK_SPLIT_ADAPTIVE:
+ *                     initial target (0 = derived from the shape).  Ignored
+ *                     for MK_SPLIT_UNFUSED.
+ *   wait_timeout_ns : limit of every device-side wait (readiness flags,
+ *                     pipeline barriers, the controller's progress watchdog);
+ *                     0 = 2 s.  A wait that runs out sets MK_ERR_TIMEOUT.
+ *   trace, trace_bytes : optional device buffer receiving controller records
+ *                     (mk_trace_record, see below); NULL/0 = off.
+ *   num_ctas        : persistent grid size, 0 = one block per SM.
+ *   flags           : MK_FLAG_* bits.
+ *   debug_skip_unit : fault injection for tests: the compute unit with this
+ *                     index (tile * P + rank) is never produced, so the
+ *                     consumer's bounded wait must run out.  -1 = off.
+ */
+typedef struct {
+    int32_t split_mode;
+    int32_t comm_sms;
+    uint64_t wait_timeout_ns;
+    void *trace;
+    uint64_t trace_bytes;
+    int32_t num_ctas;
+    uint32_t flags;
+    int64_t debug_skip_unit;
+} mk_opts;
+
+/* One controller record written to mk_opts.trace (32 bytes). */
+typedef struct {
+    uint64_t t_ns;          /* time since the controller started */
+    uint32_t target;        /* published number of communication-role blocks */
+    uint32_t units_done;    /* compute units (tile, rank) finished so far */
+    uint32_t tiles_done;    /* output tiles reduced so far */
+    uint32_t num_blocks;    /* persistent grid size */
+    uint64_t reserved;
+} mk_trace_record;
+
+/* Fill *o with the defaults (adaptive split, 2 s waits, no trace, one block per SM). */
+void mk_opts_default(mk_opts *o);
+
+/*
+ * Bytes of workspace an op needs for this shape (op = mk_op; for
+ * MK_OP_ALLGATHER_GEMM, K_per_rank is the full K).  The workspace holds the
+ * per-rank fp32 partial tiles (rank r's partition), the readiness flags, the
+ * progress counters, the call epoch and the status word.  It must be
+ * 256-byte aligned and ZEROED ONCE before its first use; after that it is
+ * reused as is (flags are epoch-valued, counters are reset by the kernel).
+ * Returns 0 for invalid arguments.
+ */
+size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank);
+
+/*
+ * GEMM + AllReduce (row-parallel TP): C = sum_{r=0}^{P-1} A_r B_r, delivered
+ * to every rank.  (mKernel, Table 3, row "GEMM + AllReduce (TP)": compute ->
+ * communication; reduction of the ranks' partial tiles, then broadcast of the
+ * result.)
+ *   A[r] : M x K_per_rank bf16   (rank r's slice of the activations' K)
+ *   B[r] : K_per_rank x N bf16   (rank r's slice of the weight rows)
+ *   C[r] : M x N, out_dtype      (rank r's copy of the result; entries may
+ *                                 alias: each distinct pointer is written once)
+ * The sum over ranks is taken in fixed order r = 0, 1, ..., P-1 on fp32
+ * partial tiles, so results do not depend on the split mode or timing.
+ */
+mk_status mk_gemm_allreduce(int P, int64_t M, int64_t N, int64_t K_per_rank,
+                            const void *const *A, const void *const *B, void *const *C,
+                            mk_dtype out_dtype, void *ws, size_t ws_bytes, const mk_opts *opts,
+                            void *cuda_stream);
+
+/*
+ * GEMM + ReduceScatter (row-parallel TP): rank s receives rows
+ * [s*M/P, (s+1)*M/P) of sum_r A_r B_r.  (mKernel, Table 3, row
+ * "GEMM + ReduceScatter (TP)".)  Arguments as for mk_gemm_allreduce except
+ *   C_shard[s] : (M/P) x N, out_dtype; M must be divisible by P.
+ */
+mk_status mk_gemm_reducescatter(int P, int64_t M, int64_t N, int64_t K_per_rank,
+                                const void *const *A, const void *const *B, void *const *C_shard,
+                                mk_dtype out_dtype, void *ws, size_t ws_bytes, const mk_opts *opts,
+                                void *cuda_stream);
+
+/*
+ * AllGather + GEMM (column-parallel TP): C_r = [A_0; A_1; ...; A_{P-1}] B_r.
+ * (mKernel, Table 3, row "AllGather + GEMM (TP)": communication -> compute,
+ * row shards of the activations gathered in 128-row chunks.)
+ *   A_shard[s]    : (M/P) x K bf16, rank s's row shard; M divisible by P
+ *   B[r]          : K x N bf16, rank r's column shard of the weights
+ *   A_gathered[r] : M x K bf16 buffer receiving the gathered activations on
+ *                   rank r, or NULL entries (then the compute role reads the
+ *                   shards in place and only waits on nothing)
+ *   C[r]          : M x N, out_dtype
+ * Communication-role blocks copy 128-row chunks and release a readiness flag
+ * per chunk; compute-role blocks acquire the flags of the rows they need.
+ */
+mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *const *A_shard,
+                            const void *const *B, void *const *A_gathered, void *const *C,
+                            mk_dtype out_dtype, void *ws, size_t ws_bytes, const mk_opts *opts,
+                            void *cuda_stream);
+
+/*
+ * Synchronize `cuda_stream`, then read and clear the workspace status word.
+ * Returns MK_ERR_CUDA if the synchronization itself fails, otherwise the
+ * status the kernels recorded since the last check (MK_OK if none).
+ */
+mk_status mk_status_check(void *ws, void *cuda_stream);
+
+/* Static English description of a status code. */
+const char *mk_status_string(mk_status s);
+
+/* Human-readable detail of the last error returned on this host thread ("" if none). */
+const char *mk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H */

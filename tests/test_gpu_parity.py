@@ -1,0 +1,215 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small and ragged shapes are compared element by element; the full-size workloads are compared
+on sampled elements the oracle computes one by one, plus properties that hold at any size
+(fused == unfused bitwise, result independent of the SM split, bf16 output == RNE(fp32
+output), ReduceScatter shards == AllReduce rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputgen as ig
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gemm_tile_level_gb300 import api, mk
+    import gpu_util as gu
+
+MODES = ("adaptive", "static", "unfused")
+
+
+def opts_for(mode, comm_sms=4, **kw):
+    if mode == "adaptive":
+        return api.make_opts(mk.MK_SPLIT_ADAPTIVE, **kw)
+    if mode == "static":
+        return api.make_opts(mk.MK_SPLIT_STATIC, comm_sms=comm_sms, **kw)
+    return api.make_opts(mk.MK_SPLIT_UNFUSED, **kw)
+
+
+def dtype_code(s):
+    return mk.MK_BF16 if s == "bf16" else mk.MK_F32
+
+
+# ------------------------------------------------------------------ the small workload
+SMALL = ig.WORKLOADS["ar_p2_m128_n128_k256"]
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_small_integer_bit_exact(mode):
+    A, B, Ad, Bd = gu.upload(SMALL, integer=True)
+    ref = oracle.allreduce(A, B)
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=1))
+    gu.assert_bit_exact(gu.host_values(C), ref)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_small_random_within_tolerance(mode):
+    A, B, Ad, Bd = gu.upload(SMALL)
+    ref = oracle.allreduce(A, B)
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=1))
+    gu.check_tolerance(gu.host_values(C), ref, out_bf16=False)
+
+
+# ------------------------------------------------------------------ ragged and edge shapes
+EDGE_SHAPES = [
+    # P, M, N, K_r
+    (1, 1, 8, 8),
+    (2, 128, 256, 64),
+    (3, 130, 136, 72),      # ragged M, ragged N (BN=256 tile with 136 columns), K below one slice
+    (2, 129, 264, 200),     # ragged everything, K not a multiple of 64
+    (5, 300, 520, 24),
+    (16, 64, 256, 64),      # the most ranks
+    (4, 256, 128, 1024),
+    (7, 384, 768, 136),
+]
+
+
+@pytest.mark.parametrize("P,M,N,Kr", EDGE_SHAPES)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_edge_shapes_integer_bit_exact(P, M, N, Kr, out):
+    wl = ig.Workload("edge", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, out, seed=P + M)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = gu.rounded_reference(oracle.allreduce(A, B), out == "bf16")
+    for mode in MODES:
+        C = gu.call_ar(Ad, Bd, dtype_code(out), opts=opts_for(mode, comm_sms=2))
+        gu.assert_bit_exact(gu.host_values(C), ref)
+
+
+@pytest.mark.parametrize("P,M,N,Kr", EDGE_SHAPES)
+def test_edge_shapes_random_within_tolerance(P, M, N, Kr):
+    wl = ig.Workload("edge", "allreduce", P, M, N, Kr, ig.normal(1.0), ig.normal(1.0 / (P * Kr)),
+                     "bf16", seed=3)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = oracle.allreduce(A, B)
+    for out in ("f32", "bf16"):
+        C = gu.call_ar(Ad, Bd, dtype_code(out))
+        gu.check_tolerance(gu.host_values(C), ref, out_bf16=(out == "bf16"))
+
+
+def test_zero_k_gives_zeros_and_empty_is_noop():
+    P, M, N = 3, 200, 136
+    Ad = [torch.empty((M, 0), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Bd = [torch.empty((0, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    C = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    gu.call_ar(Ad, Bd, mk.MK_F32, C=C)
+    assert not C.any()
+    Ad = [torch.empty((0, 64), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Bd = [torch.zeros((64, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    C = gu.call_ar(Ad, Bd, mk.MK_F32)
+    assert C.shape == (0, N)
+
+
+def test_distinct_output_buffers_all_receive_the_result():
+    wl = ig.Workload("bcast", "allreduce", 4, 256, 512, 128, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16")
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = gu.rounded_reference(oracle.allreduce(A, B), True)
+    Cs = [torch.empty((256, 512), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    gu.call_ar(Ad, Bd, mk.MK_BF16, C=Cs)
+    for c in Cs:
+        gu.assert_bit_exact(gu.host_values(c), ref)
+
+
+def test_reducescatter_small_and_ragged_shards():
+    for P, M, N, Kr in [(2, 256, 256, 64), (3, 192, 136, 40), (8, 1024, 512, 64)]:
+        wl = ig.Workload("rs", "reducescatter", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16")
+        A, B, Ad, Bd = gu.upload(wl)
+        want = [gu.rounded_reference(s, True) for s in oracle.reducescatter(A, B)]
+        for mode in MODES:
+            shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=opts_for(mode, comm_sms=2))
+            for s in range(P):
+                gu.assert_bit_exact(gu.host_values(shards[s]), want[s])
+
+
+def test_workspace_reuse_across_calls_and_shapes():
+    ws = api.workspace(mk.MK_OP_ALLREDUCE, 8, 512, 1024, 256)
+    for i, (P, M, N, Kr) in enumerate([(8, 512, 1024, 256), (4, 256, 512, 128), (8, 512, 1024, 256),
+                                       (2, 128, 256, 64)]):
+        wl = ig.Workload("reuse", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32",
+                         seed=i)
+        A, B, Ad, Bd = gu.upload(wl)
+        for mode in MODES:
+            C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode), ws=ws)
+            gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
+
+
+# ------------------------------------------------------------------ the 2048 x 4096 workload
+MID = ig.WORKLOADS["ar_p8_m2048_n4096_k512"]
+
+
+def test_mid_workload_full_oracle_comparison():
+    A, B, Ad, Bd = gu.upload(MID)
+    ref = oracle.allreduce(A, B)
+    outs = {}
+    for mode in MODES:
+        outs[mode] = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for(mode, comm_sms=16))
+        gu.check_tolerance(gu.host_values(outs[mode]), ref, out_bf16=True)
+    c32 = gu.call_ar(Ad, Bd, mk.MK_F32)
+    gu.check_tolerance(gu.host_values(c32), ref, out_bf16=False)
+    # one fixed-order sum regardless of the schedule, and bf16 = RNE(fp32) of that sum
+    assert torch.equal(outs["adaptive"], outs["unfused"]) and torch.equal(outs["static"], outs["unfused"])
+    assert torch.equal(outs["adaptive"], c32.to(torch.bfloat16))
+
+
+def test_mid_workload_integer_bit_exact():
+    A, B, Ad, Bd = gu.upload(MID, integer=True)
+    ref = gu.rounded_reference(oracle.allreduce(A, B), True)
+    C = gu.call_ar(Ad, Bd, mk.MK_BF16)
+    gu.assert_bit_exact(gu.host_values(C), ref)
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled)
+def sampled_check(wl, out_tensor_fn, integer=False, n=4096):
+    A, B, Ad, Bd = gu.upload(wl, integer=integer)
+    rows, cols = gu.sample_indices(wl.M, wl.N, n)
+    ref = oracle.allreduce_at(A, B, rows, cols)
+    out = out_tensor_fn(Ad, Bd)
+    got = gu.host_values(out)[rows, cols]
+    if integer:
+        gu.assert_bit_exact(got, gu.rounded_reference(ref, True))
+    else:
+        # rms of the full C from a row sample of the oracle (the sampled elements are random)
+        rms_rows = oracle.allreduce_rows(A, B, 0, 2)
+        gu.check_tolerance(got, ref, out_bf16=True, rms_ref=float(np.sqrt(np.mean(rms_rows ** 2))))
+    return Ad, Bd, out
+
+
+MLP = ig.WORKLOADS["ar_mlp_down_p8_m8192_n8192_k3584"]
+
+
+def test_mlp_down_projection_sampled_and_schedule_invariant():
+    Ad, Bd, C = sampled_check(MLP, lambda Ad, Bd: gu.call_ar(Ad, Bd, mk.MK_BF16))
+    for mode, nr in (("unfused", 0), ("static", 1), ("static", 16), ("static", gu.num_sms() // 2)):
+        other = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for(mode, comm_sms=nr))
+        assert torch.equal(C, other), (mode, nr)
+
+
+def test_mlp_down_projection_integer_sampled_bit_exact():
+    sampled_check(MLP, lambda Ad, Bd: gu.call_ar(Ad, Bd, mk.MK_BF16), integer=True)
+
+
+RS = ig.WORKLOADS["rs_p8_m16384_n8192_k1024"]
+
+
+def test_reducescatter_full_size_sampled_and_equal_to_allreduce_rows():
+    shards_box = {}
+
+    def run(Ad, Bd):
+        shards_box["s"] = gu.call_rs(Ad, Bd, mk.MK_BF16)
+        return torch.cat(shards_box["s"], dim=0)
+
+    Ad, Bd, cat = sampled_check(RS, run)
+    ar = gu.call_ar(Ad, Bd, mk.MK_BF16)
+    assert torch.equal(cat, ar)
+    assert all(s.shape == (RS.M // RS.P, RS.N) for s in shards_box["s"])
+
+
+@pytest.mark.parametrize("M", ig.SWEEP_M)
+def test_sweep_shapes_sampled_and_split_invariant(M):
+    wl = ig.sweep_workload(M)
+    Ad, Bd, C = sampled_check(wl, lambda Ad, Bd: gu.call_ar(Ad, Bd, mk.MK_BF16), n=1024)
+    for nr in (1, gu.num_sms() - 1):
+        assert torch.equal(C, gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for("static", comm_sms=nr)))
+    assert torch.equal(C, gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for("unfused")))
