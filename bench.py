@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GEMM + AllReduce hot path on one GB300 (or N independent replicas).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mk|reference]
+                  [--workload NAME] [--split adaptive|static|unfused] [--comm-sms n]
+  python bench.py --sweep        # SM-split sweep: adaptive vs every static split, per M
+
+A step is one mk_gemm_allreduce (or mk_gemm_reducescatter) call over one batch of seeded
+synthetic inputs already resident in HBM.  Prints ONE JSON line (rank 0).
+
+Default workload: the row-parallel MLP down-projection GEMM + AllReduce, P=8 logical ranks,
+M=N=8192, K_per_rank=3584 (the large AllReduce shape the tensor-peak target refers to).  Its
+operands (940 MB) exceed the 129 MB L2, so no flush is needed between steps.
+
+--impl reference times the fp64 CPU oracle (the only reference this method has) on a bounded
+row sample of the same workload, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import inputgen as ig  # noqa: E402
+
+DEFAULT_WORKLOAD = "ar_mlp_down_p8_m8192_n8192_k3584"
+METRIC = "fused GEMM+AllReduce TFLOP/s on 1 GB300 and % of bf16 tensor/HBM roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "gemm_tile_level_gb300", "csrc", f)
+                  for f in ("mk_kernels.cu", "mk_ptx.cuh", "mk_internal.h")]
+
+
+def workload_by_name(name: str) -> ig.Workload:
+    if name in ig.WORKLOADS:
+        return ig.WORKLOADS[name]
+    for M in ig.SWEEP_M:
+        if ig.sweep_workload(M).name == name:
+            return ig.sweep_workload(M)
+    raise SystemExit(f"unknown workload {name}; choose from {list(ig.WORKLOADS)}")
+
+
+def algorithmic_bytes(wl: ig.Workload) -> int:
+    """A and B once, every rank's fp32 partial tile written and read once, the output once."""
+    a = wl.P * wl.M * wl.Kr * 2
+    b = wl.P * wl.Kr * wl.N * 2
+    partial = wl.P * wl.M * wl.N * 4
+    out = wl.M * wl.N * (2 if wl.out_dtype == "bf16" else 4)
+    return a + b + 2 * partial + out
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel sources (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_FILE):
+        line = line.strip()
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_src_sha") != kernel_source_hash() or kv.get("workload") != workload:
+        return None
+    try:
+        return int(kv["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting",
+            0x10: "sync_boost", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Reads SM clock, max clock and clock-event reasons through NVML (read-only queries) every
+    few milliseconds in a background thread; falls back to `nvidia-smi -lms`."""
+
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) == 0:
+                    self._nvml, self._h = nv, h
+                    m = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                        self.max_mhz = m.value
+        except OSError:
+            self._nvml = None
+
+    def _loop(self):
+        nv, h = self._nvml, self._h
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if get_r(h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append(int(float(parts[0])))
+                    self.max_mhz = int(float(parts[1]))
+                    self.reasons |= int(parts[2], 16)
+                except (ValueError, IndexError):
+                    pass
+
+    def summary(self):
+        names = sorted(n for bit, n in _REASONS.items() if self.reasons & bit)
+        med = statistics.median(self.samples) if self.samples else None
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def time_oracle(wl: ig.Workload, A, B, target_s: float = 12.0):
+    """The fp64 oracle as it stands on a bounded row sample: returns (TFLOP/s, rows, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.allreduce_rows(A, B, 0, 8)
+    t_cal = max(time.perf_counter() - t0, 1e-3)
+    rows = int(max(8, min(wl.M, 8 * target_s / t_cal)))
+    t0 = time.perf_counter()
+    oracle.allreduce_rows(A, B, 0, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * wl.N * wl.Kr * wl.P
+    return flops / dt / 1e12, rows, dt
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ distributed plumbing (replicas)
+class Ranks:
+    def __init__(self, gpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.dist = dist
+        if gpus != self.world:
+            print(f"warning: --gpus {gpus} but WORLD_SIZE={self.world}", file=sys.stderr)
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+def reference_arm(args, wl, ranks):
+    """--impl reference: the fp64 oracle on host cores, rank 0 only."""
+    if ranks.rank != 0:
+        return
+    A, B = ig.make_operands(wl)
+    vals = []
+    rows = secs = None
+    # each step is a bounded row sample, sized so the whole run stays within a few minutes
+    per_step = min(args.reference_step_s, 150.0 / (args.warmup + args.steps))
+    for i in range(args.warmup + args.steps):
+        v, rows, secs = time_oracle(wl, A, B, target_s=per_step)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    sample = f"rows 0..{rows - 1} of {wl.M} (all N={wl.N}, all P={wl.P} ranks, K_r={wl.Kr}), fp64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
+                       "K_per_rank": wl.Kr, "implementation": "fp64 CPU oracle"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def split_opts(api, mk, split: str, comm_sms: int):
+    if split == "adaptive":
+        return api.make_opts(mk.MK_SPLIT_ADAPTIVE, comm_sms=comm_sms)
+    if split == "static":
+        return api.make_opts(mk.MK_SPLIT_STATIC, comm_sms=comm_sms)
+    return api.make_opts(mk.MK_SPLIT_UNFUSED)
+
+
+class Problem:
+    """Device-resident operands, outputs and workspace of one workload."""
+
+    def __init__(self, wl, torch, api, mk, host=None):
+        self.wl = wl
+        A, B = host if host is not None else ig.make_operands(wl)
+        self.A_host, self.B_host = A, B
+        self.Ad = [api.bf16_device(a) for a in A]
+        self.Bd = [api.bf16_device(b) for b in B]
+        out_t = torch.bfloat16 if wl.out_dtype == "bf16" else torch.float32
+        self.out_code = mk.MK_BF16 if wl.out_dtype == "bf16" else mk.MK_F32
+        self.rs = wl.op == "reducescatter"
+        if self.rs:
+            self.C = [torch.empty((wl.M // wl.P, wl.N), dtype=out_t, device="cuda") for _ in range(wl.P)]
+            self.op = mk.MK_OP_REDUCESCATTER
+        else:
+            self.C = torch.empty((wl.M, wl.N), dtype=out_t, device="cuda")
+            self.op = mk.MK_OP_ALLREDUCE
+        self.ws = api.workspace(self.op, wl.P, wl.M, wl.N, wl.Kr)
+        self.mk = mk
+
+    def call(self, opts, stream):
+        mk, wl = self.mk, self.wl
+        if self.rs:
+            return mk.mk_gemm_reducescatter(wl.P, wl.M, wl.N, wl.Kr, self.Ad, self.Bd, self.C,
+                                            self.out_code, self.ws, opts=opts, stream=stream)
+        return mk.mk_gemm_allreduce(wl.P, wl.M, wl.N, wl.Kr, self.Ad, self.Bd, [self.C] * wl.P,
+                                    self.out_code, self.ws, opts=opts, stream=stream)
+
+
+def time_launches(torch, prob, opts, steps, warmup, stream):
+    """Returns (total ms over `steps`, per-launch ms list)."""
+    for _ in range(warmup):
+        prob.mk.check(prob.call(opts, stream))
+    prob.mk.check(prob.mk.mk_status_check(prob.ws, stream))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        st = prob.call(opts, stream)
+        ev[i + 1].record(stream)
+        if st != 0:
+            prob.mk.check(st)
+    torch.cuda.synchronize()
+    prob.mk.check(prob.mk.mk_status_check(prob.ws, stream))
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[steps]), per
+
+
+def gpu_arm(args, wl, ranks):
+    import torch
+    from gemm_tile_level_gb300 import api, mk
+
+    dev = ranks.local if ranks.world > 1 else 0
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        prob = Problem(wl, torch, api, mk)
+        opts = split_opts(api, mk, args.split, args.comm_sms)
+        for _ in range(args.warmup):
+            mk.check(prob.call(opts, stream))
+        mk.check(mk.mk_status_check(prob.ws, stream))
+
+        # ---------------- timed region: K steps, inputs resident in HBM
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        clocks = ClockSampler(dev)
+        ranks.barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        ev[0].record(stream)
+        for i in range(args.steps):
+            st = prob.call(opts, stream)
+            ev[i + 1].record(stream)
+            if st != 0:
+                mk.check(st)
+        torch.cuda.synchronize()
+        clocks.stop()
+        ranks.barrier()
+        mk.check(mk.mk_status_check(prob.ws, stream))
+        total_ms = ev[0].elapsed_time(ev[args.steps])
+        per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+        ms_per_step = ranks.max(total_ms / args.steps)
+        value = ranks.world * wl.flops / (ms_per_step * 1e-3) / 1e12
+
+        # ---------------- end to end through the C ABI with host buffers
+        e2e = None
+        if not args.no_e2e:
+            e2e = e2e_leg(torch, prob, opts, stream, max(2, min(args.steps, 10)), ranks)
+
+        # ---------------- unfused two-kernel baseline on the same inputs (context, not `value`)
+        unfused = None
+        if args.split != "unfused" and not args.no_baseline:
+            tot, _ = time_launches(torch, prob, split_opts(api, mk, "unfused", 0),
+                                   max(3, min(args.steps, 20)), 2, stream)
+            n = max(3, min(args.steps, 20))
+            unfused = {"value": wl.flops / (tot / n * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "ms_per_step": tot / n, "launches_per_step": 2}
+
+    peaks, peak_src = load_peaks()
+    kernel_ms = statistics.mean(per_launch)
+    achieved = wl.flops / (kernel_ms * 1e-3) / 1e12
+    bytes_alg = algorithmic_bytes(wl)
+    t_tensor = wl.flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    else:
+        gbs = bytes_alg / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"]}
+    roof["traffic"] = committed_traffic(wl.name)
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json, burst)" if peak_src == "measured" else "fallback"
+    roof["roofline_frac"] = max(t_tensor, t_hbm) / (kernel_ms * 1e-3)
+    roof["algorithmic_bytes"] = bytes_alg
+    roof["kernel"] = "mk_persistent_kernel<256>" if wl.N > 128 else "mk_persistent_kernel<128>"
+
+    if ranks.rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ranks.world == 1:
+        v, rows, secs = time_oracle(wl, prob.A_host, prob.B_host, target_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of {wl.M}, all N={wl.N}, all P={wl.P} ranks, "
+                         f"K_r={wl.Kr}; {secs:.1f} s fp64"}
+    clk = clocks.summary()
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ranks.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
+                       "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype, "split": args.split,
+                       "accumulate": "fp32", "seed": wl.seed,
+                       "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
+                       "parallelism": f"{wl.P} logical ranks on one GPU" + (
+                           f"; {ranks.world} replicas" if ranks.world > 1 else "")},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "unfused_baseline": unfused}
+    print(json.dumps(line), flush=True)
+
+
+def e2e_leg(torch, prob, opts, stream, steps, ranks):
+    """Same metric through the C ABI with host buffers: every step copies this step's inputs
+    from pinned host memory, runs the call, and copies the result back."""
+    wl = prob.wl
+    A_pin = [torch.from_numpy(a).view(torch.bfloat16).pin_memory() for a in prob.A_host]
+    B_pin = [torch.from_numpy(b).view(torch.bfloat16).pin_memory() for b in prob.B_host]
+    outs = prob.C if isinstance(prob.C, list) else [prob.C]
+    C_pin = [torch.empty(c.shape, dtype=c.dtype, pin_memory=True) for c in outs]
+    h2d = sum(t.numel() * 2 for t in A_pin + B_pin)
+    d2h = sum(t.numel() * t.element_size() for t in C_pin)
+
+    def step():
+        for d, h in zip(prob.Ad + prob.Bd, A_pin + B_pin):
+            d.copy_(h, non_blocking=True)
+        prob.mk.check(prob.call(opts, stream))
+        for h, d in zip(C_pin, outs):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ranks.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    prob.mk.check(prob.mk.mk_status_check(prob.ws, stream))
+    ms = ranks.max(e0.elapsed_time(e1) / steps)
+    return {"value": ranks.world * wl.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+# ------------------------------------------------------------------ SM-split sweep
+def sweep(args):
+    import torch
+    from gemm_tile_level_gb300 import api, mk
+
+    torch.cuda.set_device(0)
+    S = torch.cuda.get_device_properties(0).multi_processor_count
+    stream = torch.cuda.Stream()
+    results = []
+    with torch.cuda.stream(stream):
+        for M in (args.sweep_m or ig.SWEEP_M):
+            wl = ig.sweep_workload(M)
+            prob = Problem(wl, torch, api, mk)
+            steps, warm = args.sweep_steps, 2
+
+            def ms(opts):
+                tot, _ = time_launches(torch, prob, opts, steps, warm, stream)
+                return tot / steps
+
+            adaptive = ms(split_opts(api, mk, "adaptive", 0))
+            static = {nr: ms(split_opts(api, mk, "static", nr)) for nr in range(1, S, args.sweep_stride)}
+            unf = ms(split_opts(api, mk, "unfused", 0))
+            best_nr = min(static, key=static.get)
+            rec = {"M": M, "adaptive_ms": adaptive, "best_static_ms": static[best_nr],
+                   "best_static_comm_sms": best_nr, "adaptive_over_best_static": adaptive / static[best_nr],
+                   "unfused_ms": unf, "fused_over_unfused": adaptive / unf,
+                   "adaptive_tflops": wl.flops / (adaptive * 1e-3) / 1e12,
+                   "static_ms": {str(k): v for k, v in static.items()}}
+            results.append(rec)
+            print(json.dumps({k: v for k, v in rec.items() if k != "static_ms"}), flush=True)
+            del prob
+            torch.cuda.empty_cache()
+    if args.sweep_out:
+        with open(args.sweep_out, "w") as f:
+            json.dump(results, f)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mk", "reference"], default="mk")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--split", choices=["adaptive", "static", "unfused"], default="adaptive")
+    ap.add_argument("--comm-sms", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-step-s", type=float, default=8.0)
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-m", type=int, nargs="*")
+    ap.add_argument("--sweep-steps", type=int, default=10)
+    ap.add_argument("--sweep-stride", type=int, default=1)
+    ap.add_argument("--sweep-out", default="")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    if args.sweep:
+        sweep(args)
+        return
+    wl = workload_by_name(args.workload)
+    ranks = Ranks(args.gpus)
+    try:
+        if args.impl == "reference":
+            reference_arm(args, wl, ranks)
+        else:
+            gpu_arm(args, wl, ranks)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    main()
