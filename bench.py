@@ -493,6 +493,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--split", choices=["adaptive", "static", "unfused"], default="adaptive")
     ap.add_argument("--comm-sms", type=int, default=0)
+    ap.add_argument("--shape", default="", help="P,M,N,K_per_rank override (same distributions); "
+                    "for small profiling cases")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-baseline", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -509,6 +511,9 @@ def main():
         sweep(args)
         return
     wl = workload_by_name(args.workload)
+    if args.shape:
+        P, M, N, Kr = (int(x) for x in args.shape.split(","))
+        wl = wl.with_shape(name=f"{wl.name}@P{P}_M{M}_N{N}_K{Kr}", P=P, M=M, N=N, Kr=Kr)
     ranks = Ranks(args.gpus)
     try:
         if args.impl == "reference":
