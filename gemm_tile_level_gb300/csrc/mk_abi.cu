@@ -36,6 +36,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Geometry {
     int bn;
     int64_t tiles_m, tiles_n, num_tiles, num_units, num_kb;
+    int64_t pair_tiles_m, num_pair_tiles, num_pair_units;
     size_t flags_off, partials_off, total;
 };
 
@@ -47,6 +48,9 @@ bool make_geometry(int P, int64_t M, int64_t N, int64_t Kr, Geometry *g) {
     g->num_tiles = g->tiles_m * g->tiles_n;
     g->num_units = g->num_tiles * P;
     g->num_kb = (Kr + MK_BK - 1) / MK_BK;
+    g->pair_tiles_m = (g->tiles_m + 1) / 2;
+    g->num_pair_tiles = g->pair_tiles_m * g->tiles_n;
+    g->num_pair_units = g->num_pair_tiles * P;
     g->flags_off = MK_WS_HEADER_BYTES;
     g->partials_off = align_up(g->flags_off + static_cast<size_t>(g->num_units) * sizeof(uint32_t), MK_WS_ALIGN);
     g->total = g->partials_off + static_cast<size_t>(g->num_units) * MK_BM * g->bn * sizeof(float);
@@ -143,19 +147,20 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     if (ws_bytes < g.total)
         return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, g.total);
 
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
-    e = mk_max_persistent_ctas(g.bn, &per_sm);
+    const bool pair = (o.flags & MK_FLAG_SINGLE_SM_TILES) == 0;
+    int resident = 0;
+    cudaError_t e = mk_max_persistent_ctas(g.bn, pair, &resident);
     if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
-    const int resident = sms * per_sm;
     const int S = o.num_ctas > 0 ? o.num_ctas : resident;
-    if (S > resident || S < 2)
+    if (S > resident)
         return fail(MK_ERR_NOT_RESIDENT, "persistent grid of %d blocks cannot be co-resident (%d fit)", S, resident);
-    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > S - 1)
-        return fail(MK_ERR_INVALID_ARG, "comm_sms=%d must be below the grid size %d", o.comm_sms, S);
+    if (pair && (S & 1)) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d must be even with SM-pair tiles", S);
+    if (S < (pair ? 4 : 2)) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d too small for two roles", S);
+    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > S - (pair ? 2 : 1))
+        return fail(MK_ERR_INVALID_ARG, "comm_sms=%d leaves no compute SMs in a grid of %d", o.comm_sms, S);
+    // role units: blocks, or SM pairs (communication SMs are then counted in whole pairs)
+    const int role_units = pair ? S / 2 : S;
+    const int per_role = pair ? 2 : 1;
 
     MkParams p;
     memset(&p, 0, sizeof p);
@@ -194,11 +199,21 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.num_tiles = static_cast<int32_t>(g.num_tiles);
     p.num_units = static_cast<int32_t>(g.num_units);
     p.num_kb = static_cast<int32_t>(g.num_kb);
+    p.pair_tiles_m = static_cast<int32_t>(g.pair_tiles_m);
+    p.num_pair_tiles = static_cast<int32_t>(g.num_pair_tiles);
+    p.num_pair_units = static_cast<int32_t>(g.num_pair_units);
     p.op = op;
     p.out_bf16 = out_dtype == MK_BF16;
     p.rows_per_shard = static_cast<int32_t>(M / P);
-    p.static_nr = o.comm_sms;
-    p.init_nr = o.comm_sms > 0 ? (o.comm_sms < S ? o.comm_sms : S - 1) : initial_reduce_ctas(S, P, g.bn, Kr);
+    {
+        int nr = (o.comm_sms + per_role - 1) / per_role;
+        if (nr > role_units - 1) nr = role_units - 1;
+        p.static_nr = nr < 1 ? 1 : nr;
+        int init = o.comm_sms > 0 ? p.static_nr
+                                  : (initial_reduce_ctas(S, P, g.bn, Kr) + per_role - 1) / per_role;
+        if (init > role_units - 1) init = role_units - 1;
+        p.init_nr = init < 1 ? 1 : init;
+    }
     p.raster_group = kRasterGroup;
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
     p.ctrl_period_ns = kCtrlPeriodNs;
@@ -206,14 +221,14 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
 
     if (o.split_mode == MK_SPLIT_UNFUSED) {
         p.mode = MK_MODE_COMPUTE_ONLY;
-        e = mk_launch_persistent(p, g.bn, S, s);
+        e = mk_launch_persistent(p, g.bn, pair, S, s);
         if (e != cudaSuccess) return fail_cuda(e, "launch of the per-rank GEMM kernel");
         e = mk_launch_reduce(p, g.bn, S, s);
         if (e != cudaSuccess) return fail_cuda(e, "launch of the reduce kernel");
         return MK_OK;
     }
     p.mode = o.split_mode == MK_SPLIT_STATIC ? MK_MODE_STATIC : MK_MODE_ADAPTIVE;
-    e = mk_launch_persistent(p, g.bn, S, s);
+    e = mk_launch_persistent(p, g.bn, pair, S, s);
     if (e != cudaSuccess) return fail_cuda(e, "launch of the fused kernel");
     return MK_OK;
 }

@@ -66,15 +66,16 @@ struct MkParams {
     uint32_t trace_cap;          // records that fit in trace
     int32_t P, M, N, Kr;
     int32_t tiles_m, tiles_n, num_tiles, num_units, num_kb;
+    int32_t pair_tiles_m, num_pair_tiles, num_pair_units;   // SM-pair kernel: 256-row tiles
     int32_t op, out_bf16, num_out, rows_per_shard;
     int32_t mode, static_nr, init_nr, raster_group;
     int32_t discard;
     int32_t ctrl_period_ns;
 };
 
-// Implemented in mk_kernels.cu
-size_t mk_persistent_smem_bytes(int bn);
-cudaError_t mk_prepare_kernels(int bn);
-cudaError_t mk_max_persistent_ctas(int bn, int *ctas_per_sm);
-cudaError_t mk_launch_persistent(const MkParams &p, int bn, int num_ctas, cudaStream_t s);
+// Implemented in mk_kernels.cu.  `pair` selects the SM-pair (cta_group::2, 256 x BN) kernel,
+// otherwise the one-SM (128 x BN) kernel.
+size_t mk_persistent_smem_bytes(int bn, bool pair);
+cudaError_t mk_max_persistent_ctas(int bn, bool pair, int *ctas);
+cudaError_t mk_launch_persistent(const MkParams &p, int bn, bool pair, int num_ctas, cudaStream_t s);
 cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s);

@@ -1,5 +1,5 @@
-// mk_kernels.cu -- the persistent, role-specialised GEMM + reduction kernel for sm_103a
-// and the standalone reduction kernel of the unfused baseline.
+// mk_kernels.cu -- the persistent, role-specialised GEMM + reduction kernels for sm_103a and
+// the standalone reduction kernel of the unfused baseline.
 //
 // Method (mKernel: Fast Multi-GPU, Multi-Node Fused Kernels; abstract, Figure 2, Table 3):
 // one persistent kernel whose thread blocks take a compute role or a communication role.
@@ -10,16 +10,25 @@
 // shard).  An on-GPU controller reads progress counters and publishes the target number of
 // communication blocks (Figure 2, dashed arrow; Figure 7).
 //
-// GB300 mapping of one compute unit (output tile t of rank r, 128 x BN, K_r deep):
-//   warp 0  : claims work, TMA-loads 64-wide K slices of A_r and B_r into a 4..6-stage
-//             shared-memory ring (128-byte swizzle), completion on mbarriers
-//   warp 1  : one thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32) into one of two
-//             TMEM accumulators and commits to mbarriers
-//   warps 2-9: tcgen05.ld the accumulator, store the fp32 partial tile into rank r's
-//             workspace partition (coalesced 512-byte warp stores), release flag[t][r]
-//   warp 10 : the split controller (block 0, adaptive mode)
-// Reduce unit (tile t): warps 2-9 acquire flag[t][0..P-1], stream the P partial tiles with
-// 16-byte L2-only loads, sum them in rank order 0..P-1, round and write C (or the shard).
+// Two compute-tile shapes share everything but the MMA issue:
+//   mk_pair_kernel<BN>  (default): a cluster of two CTAs on two SMs computes one 256 x BN tile
+//       with tcgen05.mma.cta_group::2 (M=256); each CTA stages only its 128 rows of A and its
+//       BN/2 columns of B, so a 6-stage TMA ring fits and L2->SM bytes per FLOP drop by a third.
+//   mk_persistent_kernel<BN>: one CTA computes a 128 x BN tile with cta_group::1.
+// Warp roles in a block (352 threads):
+//   warp 0   : work scheduler (pair: the even CTA claims for both) and TMA producer
+//   warp 1   : one thread issues tcgen05.mma into one of two TMEM accumulators (pair: even CTA)
+//   warps 2-9: tcgen05.ld the accumulator, store the fp32 partial tile of rank r into rank r's
+//              workspace partition with coalesced 512-byte warp stores, release flag[tile][r];
+//              or, for a reduce item, acquire flag[tile][0..P-1], stream the P partials with
+//              16-byte L2-only loads, sum them in rank order 0..P-1 and write C or the shard
+//   warp 10  : the split controller (block 0, adaptive mode)
+//
+// Failure handling: every wait is bounded.  A wait for another block's progress (readiness
+// flags, the work gate, the controller watchdog) gives up after timeout_ns and raises
+// MK_ERR_TIMEOUT plus a grid-wide abort; then every block stops claiming work, skips pending
+// reductions, and drains its queued compute items so that no TMA load or MMA is in flight at
+// exit.  Waits inside one block's (or pair's) pipeline only give up after 4 x timeout_ns.
 #include "mk_internal.h"
 #include "mk_ptx.cuh"
 #include "mk.h"
@@ -32,45 +41,61 @@ enum { ITEM_END = 0, ITEM_COMPUTE = 1, ITEM_REDUCE = 2 };
 enum {
     SITE_WORK_EMPTY = 1, SITE_WORK_FULL = 2, SITE_STAGE_EMPTY = 3, SITE_STAGE_FULL = 4,
     SITE_ACC_EMPTY = 5, SITE_ACC_FULL = 6, SITE_FLAG = 7, SITE_DRAIN = 8, SITE_GATE = 9,
-    SITE_WATCHDOG = 10
+    SITE_WATCHDOG = 10, SITE_CLAIMED = 11
 };
 
+constexpr int WQ = 4;          // depth of the per-block work queue
+constexpr int ACC = 2;         // TMEM accumulators per block
+
+// One-SM tiles: 128 x BN per CTA, A 16 KiB + B BN/64 boxes of 8 KiB per 64-deep K slice.
 template <int BN>
-struct TileCfg {
-    static constexpr int A_BYTES = MK_BM * MK_BK * 2;     // 16 KiB: 128 rows x 128 B
-    static constexpr int B_BOX_BYTES = 64 * MK_BK * 2;    // 8 KiB: 64 K rows x 64 N columns
+struct Cfg1 {
+    static constexpr int A_BYTES = MK_BM * MK_BK * 2;
+    static constexpr int B_BOX_BYTES = 64 * MK_BK * 2;
     static constexpr int B_BOXES = BN / 64;
-    static constexpr int B_BYTES = B_BOX_BYTES * B_BOXES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BOXES * B_BOX_BYTES;
     static constexpr int STAGES = (BN == 256) ? 4 : 6;
-    static constexpr int ACC = 2;
     static constexpr int TMEM_COLS = ACC * BN;
-    static constexpr int WQ = 4;
     static constexpr int TILE_FLOATS = MK_BM * BN;
     static constexpr uint32_t IDESC = idesc_bf16_f32(MK_BM, BN);
 };
 
+// SM-pair tiles: 256 x BN per cluster; per CTA A 16 KiB + its BN/2 columns of B.
 template <int BN>
+struct Cfg2 {
+    static constexpr int A_BYTES = MK_BM * MK_BK * 2;
+    static constexpr int B_BOX_BYTES = 64 * MK_BK * 2;
+    static constexpr int B_BOXES = BN / 128;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BOXES * B_BOX_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 6 : 8;
+    static constexpr int TMEM_COLS = ACC * BN;
+    static constexpr int TILE_FLOATS = MK_BM * BN;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(2 * MK_BM, BN);
+};
+
+template <int STAGES>
 struct SmemCtl {
-    using T = TileCfg<BN>;
-    uint64_t full[T::STAGES];
-    uint64_t empty[T::STAGES];
-    uint64_t tfull[T::ACC];
-    uint64_t tempty[T::ACC];
-    uint64_t wfull[T::WQ];
-    uint64_t wempty[T::WQ];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[ACC];
+    uint64_t tempty[ACC];
+    uint64_t wfull[WQ];
+    uint64_t wempty[WQ];
     uint64_t drain;
-    int2 items[T::WQ];
+    int2 items[WQ];
     uint32_t tmem_base;
     uint32_t epoch;
     int abort;
+    uint32_t peer_issued;   // pair kernel: number of K-slice loads the odd CTA's producer issued
+    uint32_t issued;        // number of K-slice loads this CTA's producer issued
     int pad;
 };
 
 struct Ctx {
     MkWsHeader *hdr;
     volatile int *s_abort;
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;     // cross-block waits
+    uint64_t pipe_timeout_ns; // waits inside one block's / pair's pipeline
 };
 
 __device__ __forceinline__ void raise_error(const Ctx &c, uint32_t code, uint32_t site, uint32_t index) {
@@ -91,32 +116,18 @@ __device__ __forceinline__ bool global_abort(const Ctx &c) {
     return false;
 }
 
-// Bounded mbarrier wait: false if the block is aborting or the limit ran out (which raises
-// MK_ERR_TIMEOUT).  At most 2^32 polls and at most timeout_ns.
+// Bounded pipeline wait on a local mbarrier (cluster-scope acquire when `CLUSTER`): false only
+// when 4 x timeout has passed or 2^32 polls were made; that raises MK_ERR_TIMEOUT.
+template <bool CLUSTER>
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctx &c, uint32_t site, uint32_t index) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1; i != 0u; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*c.s_abort) return false;
-        if ((i & 63u) == 0u) {
-            if (global_abort(c)) return false;
-            if (globaltimer() - t0 > c.timeout_ns) break;
-        }
+        if (poll()) return true;
+        if ((i & 63u) == 0u && globaltimer() - t0 > c.pipe_timeout_ns) break;
     }
     raise_error(c, MK_ERR_TIMEOUT, site, index);
-    return false;
-}
-
-// Wait used while shutting down: ignores the abort flag (the asynchronous work it waits for
-// must finish before the block exits) but keeps the time limit.
-__device__ bool wait_bar_final(uint32_t bar, uint32_t parity, const Ctx &c, uint32_t site) {
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 0; i != 0xFFFFFFFFu; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && globaltimer() - t0 > c.timeout_ns) break;
-    }
-    raise_error(c, MK_ERR_TIMEOUT, site, 0);
     return false;
 }
 
@@ -133,32 +144,43 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool v) {
     return r != 0u;
 }
 
-// Grouped raster: groups of `raster_group` tile rows, walked column by column, so that
-// concurrently computed tiles share A rows and B columns in L2.
-__device__ __forceinline__ void tile_coords(const MkParams &p, int t, int &tm, int &tn) {
-    const int G = p.raster_group;
-    const int per_group = G * p.tiles_n;
+// Grouped raster over a tiles_m x tiles_n grid: groups of G rows walked column by column, so
+// that concurrently computed tiles share A rows and B columns in L2.
+__device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, int &tm, int &tn) {
+    const int per_group = G * tiles_n;
     const int g = t / per_group;
     const int first_m = g * G;
-    const int gsize = min(G, p.tiles_m - first_m);
+    const int gsize = min(G, tiles_m - first_m);
     const int local = t - g * per_group;
     tm = first_m + local % gsize;
     tn = local / gsize;
 }
 
 // ------------------------------------------------------------------ work claiming
-// Role of this block for its next claim: reduce if blockIdx >= S - target (the target is
-// published by the controller or fixed by the caller); once the compute queue is empty
-// every block reduces.  Block 0 always computes while compute work remains.
+// Role of a role unit (a block, or an SM pair) for its next claim: reduce if its index is
+// >= R - target (the target is published by the controller or fixed by the caller); once the
+// compute queue is empty every role unit reduces.  Role unit 0 always computes while compute
+// work remains.
 //
-// Deadlock freedom: a reduction of tile t is queued only after every compute unit of t has
-// been claimed (by any block).  Each block works through its queue in claim order, so a
+// Deadlock freedom: a reduction of item i is queued only after every compute unit it consumes
+// has been claimed (by anyone).  Each block works through its queue in claim order, so a
 // reduction waits only on units claimed before it, which in turn wait only on items claimed
 // earlier still: the wait-for relation follows claim order and has no cycle.
 //
-// A reduce-role block claims the next tile only when the units finished so far reach it
-// (one tile of slack), so that reducers do not park on tiles far ahead of the compute front.
-__device__ bool wait_claimed(const MkParams &p, const Ctx &c, uint32_t need) {
+// A reduce-role unit claims the next item only when the units finished so far reach it (one
+// item of slack), so reducers do not park on items far ahead of the compute front.
+//
+// units_done counts `done_per_unit` increments per compute unit (1 for one-SM tiles, 2 for an
+// SM pair whose two CTAs each count their half).
+struct ClaimGeom {
+    uint32_t num_units;   // compute units (tile, rank)
+    uint32_t num_items;   // reduce items (tiles, or tile pairs)
+    uint32_t role_index;  // this role unit
+    uint32_t role_units;  // role units in the grid
+    uint32_t done_per_unit;
+};
+
+__device__ bool wait_claimed(const Ctx &c, uint32_t need) {
     uint64_t t0 = 0;
     for (uint32_t spin = 0; spin != 0xFFFFFFFFu; ++spin) {
         if (ld_relaxed_gpu(&c.hdr->compute_next) >= need) return true;
@@ -167,14 +189,12 @@ __device__ bool wait_claimed(const MkParams &p, const Ctx &c, uint32_t need) {
         else if (globaltimer() - t0 > c.timeout_ns) break;
         __nanosleep(100);
     }
-    raise_error(c, MK_ERR_TIMEOUT, SITE_GATE, need);
+    raise_error(c, MK_ERR_TIMEOUT, SITE_CLAIMED, need);
     return false;
 }
 
-__device__ int2 claim_work(const MkParams &p, const Ctx &c, bool &exhausted) {
+__device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, bool &exhausted) {
     MkWsHeader *h = c.hdr;
-    const int S = static_cast<int>(gridDim.x);
-    const uint32_t num_units = static_cast<uint32_t>(p.num_units);
     const uint32_t P = static_cast<uint32_t>(p.P);
     uint64_t gate_t0 = 0;
     uint32_t gate_seen = 0xFFFFFFFFu;
@@ -182,7 +202,7 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, bool &exhausted) {
         if (global_abort(c)) return make_int2(ITEM_END, 0);
         if (p.mode == MK_MODE_COMPUTE_ONLY) {
             const uint32_t u = atomicAdd(&h->compute_next, 1u);
-            if (u >= num_units) return make_int2(ITEM_END, 0);
+            if (u >= g.num_units) return make_int2(ITEM_END, 0);
             if (static_cast<int64_t>(u) == p.skip_unit) continue;
             return make_int2(ITEM_COMPUTE, static_cast<int>(u));
         }
@@ -192,20 +212,20 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, bool &exhausted) {
                 const uint32_t pub = ld_relaxed_gpu(&h->target_nr);
                 nr = pub ? static_cast<int>(pub) : p.init_nr;
             }
-            if (static_cast<int>(blockIdx.x) < S - nr) {
+            if (static_cast<int>(g.role_index) < static_cast<int>(g.role_units) - nr) {
                 const uint32_t u = atomicAdd(&h->compute_next, 1u);
-                if (u < num_units) {
+                if (u < g.num_units) {
                     if (static_cast<int64_t>(u) == p.skip_unit) continue;
                     return make_int2(ITEM_COMPUTE, static_cast<int>(u));
                 }
                 exhausted = true;
             } else {
                 const uint32_t next = ld_relaxed_gpu(&h->reduce_next);
-                if (next >= static_cast<uint32_t>(p.num_tiles)) return make_int2(ITEM_END, 0);
+                if (next >= g.num_items) return make_int2(ITEM_END, 0);
                 const uint32_t done = ld_relaxed_gpu(&h->units_done);
                 const uint32_t issued = ld_relaxed_gpu(&h->compute_next);
-                if (issued < num_units &&
-                    (static_cast<uint64_t>(next) + 1) * P > static_cast<uint64_t>(done) + P) {
+                const uint64_t per_item = static_cast<uint64_t>(P) * g.done_per_unit;
+                if (issued < g.num_units && (static_cast<uint64_t>(next) + 1) * per_item > done + per_item) {
                     // nothing ready yet: wait for compute progress (bounded), then re-read the role
                     if (done != gate_seen) {
                         gate_seen = done;
@@ -219,137 +239,18 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, bool &exhausted) {
                 }
             }
         }
-        const uint32_t t = atomicAdd(&h->reduce_next, 1u);
-        if (t >= static_cast<uint32_t>(p.num_tiles)) return make_int2(ITEM_END, 0);
-        const uint64_t need64 = (static_cast<uint64_t>(t) + 1) * P;
-        const uint32_t need = need64 < num_units ? static_cast<uint32_t>(need64) : num_units;
-        if (!wait_claimed(p, c, need)) return make_int2(ITEM_END, 0);
-        return make_int2(ITEM_REDUCE, static_cast<int>(t));
+        const uint32_t i = atomicAdd(&h->reduce_next, 1u);
+        if (i >= g.num_items) return make_int2(ITEM_END, 0);
+        const uint64_t need64 = (static_cast<uint64_t>(i) + 1) * P;
+        const uint32_t need = need64 < g.num_units ? static_cast<uint32_t>(need64) : g.num_units;
+        if (!wait_claimed(c, need)) return make_int2(ITEM_END, 0);
+        return make_int2(ITEM_REDUCE, static_cast<int>(i));
     }
     raise_error(c, MK_ERR_TIMEOUT, SITE_GATE, 0);
     return make_int2(ITEM_END, 0);
 }
 
-// ------------------------------------------------------------------ warp 0: scheduler + TMA
-template <int BN>
-__device__ void run_producer(const MkParams &p, SmemCtl<BN> &s, uint8_t *stages, const Ctx &c) {
-    using T = TileCfg<BN>;
-    int stage = 0;
-    uint32_t phase = 0;
-    int wq = 0;
-    uint32_t wphase = 0;
-    bool exhausted = false;
-    uint32_t armed = 0;                 // bit i: stage i has a load issued
-    uint32_t armed_phase = 0;           // bit i: phase of that load
-    bool stop = false;
-    while (!stop) {
-        const int2 it = claim_work(p, c, exhausted);
-        if (!wait_bar(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
-        s.items[wq] = it;
-        mbar_arrive(smem_u32(&s.wfull[wq]));
-        if (++wq == T::WQ) {
-            wq = 0;
-            wphase ^= 1u;
-        }
-        if (it.x == ITEM_END) break;
-        if (it.x != ITEM_COMPUTE) continue;
-        const int u = it.y;
-        const int t = u / p.P;
-        const int r = u - t * p.P;
-        int tm, tn;
-        tile_coords(p, t, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
-                stop = true;
-                break;
-            }
-            const uint32_t fb = smem_u32(&s.full[stage]);
-            uint8_t *sa = stages + stage * T::STAGE_BYTES;
-            uint8_t *sb = sa + T::A_BYTES;
-            mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
-            tma_load_2d(smem_u32(sa), &p.tmA[r], fb, kb * MK_BK, tm * MK_BM);
-#pragma unroll
-            for (int j = 0; j < T::B_BOXES; ++j)
-                tma_load_2d(smem_u32(sb + j * T::B_BOX_BYTES), &p.tmB[r], fb, tn * BN + j * 64,
-                            kb * MK_BK);
-            armed |= 1u << stage;
-            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == T::STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-    }
-    // Every TMA load issued by this thread must land before the block can exit.
-    for (int i = 0; i < T::STAGES; ++i)
-        if (armed & (1u << i)) wait_bar_final(smem_u32(&s.full[i]), (armed_phase >> i) & 1u, c, SITE_DRAIN);
-}
-
-// ------------------------------------------------------------------ warp 1: tcgen05.mma issue
-template <int BN>
-__device__ void run_mma(const MkParams &p, SmemCtl<BN> &s, uint8_t *stages, const Ctx &c,
-                        uint32_t tmem_base) {
-    using T = TileCfg<BN>;
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t aphase = 0;
-    int wq = 0;
-    uint32_t wphase = 0;
-    for (;;) {
-        if (!wait_bar(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0)) break;
-        const int2 it = s.items[wq];
-        mbar_arrive(smem_u32(&s.wempty[wq]));
-        if (++wq == T::WQ) {
-            wq = 0;
-            wphase ^= 1u;
-        }
-        if (it.x == ITEM_END) break;
-        if (it.x != ITEM_COMPUTE) continue;
-        if (!wait_bar(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
-        tc_fence_after();
-        const long long t0 = clock64();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bar(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
-            const uint32_t sb = sa + T::A_BYTES;
-            // A: K-major, rows 128 B apart, 8-row groups 1024 B apart; K step of 16 = +32 B.
-            // B: MN-major, 64-column boxes 8 KiB apart (LBO), 8-row K groups 1024 B apart
-            //    (SBO); K step of 16 rows = +2048 B.
-            const uint64_t ad = sw128_desc(sa, 16, 1024);
-            const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
-#pragma unroll
-            for (int kk = 0; kk < MK_BK / 16; ++kk)
-                umma_bf16(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
-                          T::IDESC, static_cast<uint32_t>((kb | kk) != 0));
-            umma_commit(smem_u32(&s.empty[stage]));
-            if (++stage == T::STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-        if (!ok) break;
-        umma_commit(smem_u32(&s.tfull[acc]));
-        if (++acc == T::ACC) {
-            acc = 0;
-            aphase ^= 1u;
-        }
-        atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
-                  static_cast<unsigned long long>(clock64() - t0));
-    }
-    // Every MMA issued by this thread must complete before TMEM is released.
-    umma_commit(smem_u32(&s.drain));
-    wait_bar_final(smem_u32(&s.drain), 0, c, SITE_DRAIN);
-}
-
 // ------------------------------------------------------------------ reduction of one tile
-template <int BN>
 __device__ __forceinline__ void store_out4(const MkParams &p, int grow, int gcol, float4 v) {
     if (p.op == MK_IOP_RS) {
         const int sh = grow / p.rows_per_shard;
@@ -370,22 +271,25 @@ __device__ __forceinline__ void store_out4(const MkParams &p, int grow, int gcol
     }
 }
 
-// Sum the P partial tiles of output tile t in rank order and write the result.  The tile
-// layout in a partition is [BN/4 column groups][128 rows][4 floats]; thread `tid` (0..255)
-// owns row tid % 128 and one half of the column groups, so each warp load instruction reads
-// 512 contiguous bytes.  No waits and no barriers inside.
+// Partial tile (rank r, tile (tm, tn)) lives at ((r * num_tiles) + tm * tiles_n + tn) tiles into
+// the partial region; inside a tile the layout is [BN/4 column groups][128 rows][4 floats].
 template <int BN>
-__device__ __forceinline__ void reduce_tile_body(const MkParams &p, int t, int tid) {
-    using T = TileCfg<BN>;
-    int tm, tn;
-    tile_coords(p, t, tm, tn);
+__device__ __forceinline__ float *partial_tile(const MkParams &p, int r, int lt) {
+    return p.partials + (static_cast<size_t>(r) * p.num_tiles + lt) * (MK_BM * BN);
+}
+
+// Sum the P partial tiles of output tile (tm, tn) in rank order and write the result.  Thread
+// `tid` (0..255) owns row tid % 128 and one half of the column groups, so each warp load
+// instruction reads 512 contiguous bytes.  No waits and no barriers inside.
+template <int BN>
+__device__ __forceinline__ void reduce_tile_body(const MkParams &p, int tm, int tn, int tid) {
     const int row = tid & (MK_BM - 1);
     const int grow = tm * MK_BM + row;
     if (grow >= p.M) return;
+    const int lt = tm * p.tiles_n + tn;
     const int g_begin = (tid >> 7) * (BN / 8);
-    const size_t rank_stride4 = static_cast<size_t>(p.num_tiles) * (T::TILE_FLOATS / 4);
-    const float4 *tile4 = reinterpret_cast<const float4 *>(p.partials) +
-                          static_cast<size_t>(t) * (T::TILE_FLOATS / 4);
+    const size_t rank_stride4 = static_cast<size_t>(p.num_tiles) * (MK_BM * BN / 4);
+    const float4 *tile4 = reinterpret_cast<const float4 *>(partial_tile<BN>(p, 0, lt));
 #pragma unroll 1
     for (int g = g_begin; g < g_begin + BN / 8; g += 4) {
         const int gcol = tn * BN + g * 4;
@@ -410,25 +314,24 @@ __device__ __forceinline__ void reduce_tile_body(const MkParams &p, int t, int t
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (gcol + 4 * j < p.N) store_out4<BN>(p, grow, gcol + 4 * j, a[j]);
+            if (gcol + 4 * j < p.N) store_out4(p, grow, gcol + 4 * j, a[j]);
     }
 }
 
-// Drop the consumed partial tiles of tile t from L2 without write-back (scratch data).
+// Drop the consumed partial tiles of tile lt from L2 without write-back (scratch data).
 template <int BN>
-__device__ __forceinline__ void discard_tile(const MkParams &p, int t, int tid, int nthreads) {
-    using T = TileCfg<BN>;
-    constexpr int LINES = T::TILE_FLOATS * 4 / 128;
+__device__ __forceinline__ void discard_tile(const MkParams &p, int lt, int tid, int nthreads) {
+    constexpr int LINES = MK_BM * BN * 4 / 128;
     for (int r = 0; r < p.P; ++r) {
-        const char *base = reinterpret_cast<const char *>(
-            p.partials + (static_cast<size_t>(r) * p.num_tiles + t) * T::TILE_FLOATS);
+        const char *base = reinterpret_cast<const char *>(partial_tile<BN>(p, r, lt));
         for (int l = tid; l < LINES; l += nthreads) discard_l2_line(base + static_cast<size_t>(l) * 128);
     }
 }
 
-// Thread 0 of the reduce group: acquire flag[t][r] == epoch for every rank (bounded).
-__device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int t, uint32_t epoch) {
-    const uint32_t *f = p.flags + static_cast<size_t>(t) * p.P;
+// Thread 0 of the reduce group: acquire flag[lt][r] == epoch for every rank.  False if the
+// grid is aborting or the limit ran out (which raises MK_ERR_TIMEOUT).
+__device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int lt, uint32_t epoch) {
+    const uint32_t *f = p.flags + static_cast<size_t>(lt) * p.P;
     uint64_t t0 = 0;
     for (int r = 0; r < p.P; ++r) {
         for (uint32_t polls = 0; ld_acquire_gpu(f + r) != epoch; ++polls) {
@@ -437,7 +340,7 @@ __device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int t, uint32_t
             if ((polls & 15u) == 15u) {
                 if (global_abort(c)) return false;
                 if (globaltimer() - t0 > c.timeout_ns || polls > (1u << 30)) {
-                    raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, static_cast<uint32_t>(t * p.P + r));
+                    raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, static_cast<uint32_t>(lt * p.P + r));
                     return false;
                 }
             }
@@ -447,105 +350,67 @@ __device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int t, uint32_t
     return true;
 }
 
-// ------------------------------------------------------------------ warps 2-9: epilogue / reduce
+// The reduce group (warps 2-9) handles one reduce item for tile (tm, tn).
 template <int BN>
-__device__ void run_epilogue(const MkParams &p, SmemCtl<BN> &s, const Ctx &c, uint32_t tmem_base,
-                             uint32_t epoch) {
-    using T = TileCfg<BN>;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int e = warp - MK_EPI_WARP0;
-    const int lq = warp & 3;       // the TMEM lane quarter this warp can access
-    const int half = e >> 2;       // which half of the tile's columns
-    const int etid = threadIdx.x - MK_EPI_WARP0 * 32;
+__device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int etid, uint32_t epoch) {
+    bool ok = true;
+    const bool exists = tm < p.tiles_m;
+    const int lt = tm * p.tiles_n + tn;
+    if (exists && etid == 0) ok = wait_tile_ready(p, c, lt, epoch);
+    ok = bar_and(1, MK_EPI_THREADS, ok);
+    if (exists && ok) {
+        const long long t0 = clock64();
+        reduce_tile_body<BN>(p, tm, tn, etid);
+        bar_sync(1, MK_EPI_THREADS);   // every read of the partials is done
+        if (p.discard) discard_tile<BN>(p, lt, etid, MK_EPI_THREADS);
+        if (etid == 0)
+            atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->reduce_busy),
+                      static_cast<unsigned long long>(clock64() - t0));
+    }
+    if (etid == 0 && (ok || !exists)) atomicAdd(&c.hdr->tiles_done, 1u);
+}
+
+// The epilogue group drains TMEM accumulator `acc` (128 lanes x BN columns of fp32) into the
+// partial tile (r, lt) with 512-byte coalesced warp stores.
+template <int BN>
+__device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_acc, int r, int lt, int warp,
+                                              int lane) {
+    const int lq = warp & 3;                          // the TMEM lane quarter this warp can access
+    const int half = (warp - MK_EPI_WARP0) >> 2;      // which half of the tile's columns
     const int row = lq * 32 + lane;
-    int acc = 0;
-    uint32_t aphase = 0;
-    int wq = 0;
-    uint32_t wphase = 0;
-    for (;;) {
-        bool ok = true;
-        if (lane == 0) ok = wait_bar(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0);
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-        if (!bar_and(1, MK_EPI_THREADS, ok)) break;
-        const int2 it = s.items[wq];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s.wempty[wq]));
-        if (++wq == T::WQ) {
-            wq = 0;
-            wphase ^= 1u;
-        }
-        if (it.x == ITEM_END) break;
-        if (it.x == ITEM_COMPUTE) {
-            const int u = it.y;
-            const int t = u / p.P;
-            const int r = u - t * p.P;
-            ok = true;
-            if (lane == 0) ok = wait_bar(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
-            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-            if (!bar_and(1, MK_EPI_THREADS, ok)) break;
-            tc_fence_after();
-            float *tile = p.partials + (static_cast<size_t>(r) * p.num_tiles + t) * T::TILE_FLOATS;
+    float *tile = partial_tile<BN>(p, r, lt);
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 64; ++cc) {
-                const int col0 = half * (BN / 2) + cc * 32;
-                uint32_t v[32];
-                if (p.num_kb > 0) {
-                    tmem_ld32(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) +
-                                  static_cast<uint32_t>(acc * BN + col0),
-                              v);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = 0u;
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float *dst = tile + (static_cast<size_t>((col0 >> 2) + q) * MK_BM + row) * 4;
-                    st_f4(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[acc]));
-            if (++acc == T::ACC) {
-                acc = 0;
-                aphase ^= 1u;
-            }
-            bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
-            if (etid == 0) {
-                st_release_gpu(p.flags + static_cast<size_t>(t) * p.P + r, epoch);
-                atomicAdd(&c.hdr->units_done, 1u);
-            }
+    for (int cc = 0; cc < BN / 64; ++cc) {
+        const int col0 = half * (BN / 2) + cc * 32;
+        uint32_t v[32];
+        if (p.num_kb > 0) {
+            tmem_ld32(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0), v);
         } else {
-            const int t = it.y;
-            ok = true;
-            if (etid == 0) ok = wait_tile_ready(p, c, t, epoch);
-            if (!bar_and(1, MK_EPI_THREADS, ok)) break;
-            const long long t0 = clock64();
-            reduce_tile_body<BN>(p, t, etid);
-            bar_sync(1, MK_EPI_THREADS);   // every read of the partials is done
-            if (p.discard) discard_tile<BN>(p, t, etid, MK_EPI_THREADS);
-            if (etid == 0) {
-                atomicAdd(&c.hdr->tiles_done, 1u);
-                atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->reduce_busy),
-                          static_cast<unsigned long long>(clock64() - t0));
-            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float *dst = tile + (static_cast<size_t>((col0 >> 2) + q) * MK_BM + row) * 4;
+            st_f4(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                  __uint_as_float(v[4 * q + 3]));
         }
     }
 }
 
-// ------------------------------------------------------------------ warp 10: split controller
-// Every ctrl_period_ns: with W_c compute units and W_r tiles left, and measured SM-cycle
-// costs tau_c per unit and tau_r per tile, publish
-//     n_r = clamp(round(S * W_r tau_r / (W_c tau_c + W_r tau_r)), 1, S - 1),
-// i.e. give each role SMs in proportion to the work it still has, so both finish together.
-// As compute nears completion W_c -> 0 and the target moves toward communication.  This
-// formula is a reading of the controller's stated intent; the pages do not give it.
-// The loop doubles as a watchdog: no progress for timeout_ns raises MK_ERR_TIMEOUT.
-__device__ void run_controller(const MkParams &p, const Ctx &c) {
+// ------------------------------------------------------------------ split controller
+// Every ctrl_period_ns: with W_c compute units and W_r tiles left, and measured SM-cycle costs
+// tau_c per unit and tau_r per tile, publish
+//     n_r = clamp(round(S * W_r tau_r / (W_c tau_c + W_r tau_r)), 1, S - 1)
+// SMs of communication role (converted to role units), i.e. give each role SMs in proportion
+// to the work it still has, so both finish together.  As compute nears completion W_c -> 0 and
+// the target moves toward communication.  This formula is a reading of the controller's
+// stated intent; the pages do not give it.  The loop doubles as a watchdog: no progress for
+// timeout_ns raises MK_ERR_TIMEOUT.
+__device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_units, uint32_t num_tiles_total,
+                               uint32_t done_per_unit, int role_units, int sms_per_role) {
     MkWsHeader *h = c.hdr;
-    const int S = static_cast<int>(gridDim.x);
+    const int S = role_units * sms_per_role;
     int cur = p.init_nr;
     st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
     const uint64_t start = globaltimer();
@@ -560,14 +425,14 @@ __device__ void run_controller(const MkParams &p, const Ctx &c) {
         if (trace && nrec < p.trace_cap) {
             mk_trace_record rec;
             rec.t_ns = now - start;
-            rec.target = static_cast<uint32_t>(cur);
-            rec.units_done = u;
+            rec.target = static_cast<uint32_t>(cur * sms_per_role);
+            rec.units_done = u / done_per_unit;
             rec.tiles_done = d;
             rec.num_blocks = static_cast<uint32_t>(S);
             rec.reserved = 0;
             trace[nrec++] = rec;
         }
-        if (d >= static_cast<uint32_t>(p.num_tiles) || global_abort(c)) break;
+        if (d >= num_tiles_total || global_abort(c)) break;
         if (u != last_u || d != last_d) {
             last_u = u;
             last_d = d;
@@ -576,16 +441,19 @@ __device__ void run_controller(const MkParams &p, const Ctx &c) {
             raise_error(c, MK_ERR_TIMEOUT, SITE_WATCHDOG, d);
             break;
         }
-        if (u > 0 && d > 0) {
-            const double tau_c = static_cast<double>(ld_relaxed_gpu64(&h->compute_busy)) / u;
+        const uint32_t units = u / done_per_unit;
+        if (units > 0 && d > 0) {
+            const double tau_c = sms_per_role * static_cast<double>(ld_relaxed_gpu64(&h->compute_busy)) / units;
             const double tau_r = static_cast<double>(ld_relaxed_gpu64(&h->reduce_busy)) / d;
-            const double wc = static_cast<double>(p.num_units - static_cast<int>(min(u, (uint32_t)p.num_units))) * tau_c;
-            const double wr = static_cast<double>(p.num_tiles - static_cast<int>(d)) * tau_r;
-            int nr = (wc + wr > 0.0) ? static_cast<int>(S * wr / (wc + wr) + 0.5) : cur;
-            nr = max(1, min(S - 1, nr));
-            if (nr != cur) {
-                cur = nr;
-                st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
+            const double wc = static_cast<double>(num_units - min(units, num_units)) * tau_c;
+            const double wr = static_cast<double>(num_tiles_total - d) * tau_r;
+            if (wc + wr > 0.0) {
+                int nr = static_cast<int>(S * wr / (wc + wr) / sms_per_role + 0.5);
+                nr = max(1, min(role_units - 1, nr));
+                if (nr != cur) {
+                    cur = nr;
+                    st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
+                }
             }
         }
         __nanosleep(static_cast<unsigned>(p.ctrl_period_ns));
@@ -614,42 +482,205 @@ __device__ void finish_call(const MkParams &p, uint32_t epoch) {
     }
 }
 
+template <int STAGES>
+__device__ void init_barriers(SmemCtl<STAGES> &s, const MkParams &p, uint32_t full_count, uint32_t tempty_count,
+                              uint32_t wempty_count) {
+    for (int i = 0; i < STAGES; ++i) {
+        mbar_init(smem_u32(&s.full[i]), full_count);
+        mbar_init(smem_u32(&s.empty[i]), 1);
+    }
+    for (int i = 0; i < ACC; ++i) {
+        mbar_init(smem_u32(&s.tfull[i]), 1);
+        mbar_init(smem_u32(&s.tempty[i]), tempty_count);
+    }
+    for (int i = 0; i < WQ; ++i) {
+        mbar_init(smem_u32(&s.wfull[i]), 1);
+        mbar_init(smem_u32(&s.wempty[i]), wempty_count);
+    }
+    mbar_init(smem_u32(&s.drain), 1);
+    fence_mbar_init();
+    s.abort = 0;
+    s.issued = 0;
+    s.peer_issued = 0;
+    uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
+    if (e == 0u) e = 1u;
+    s.epoch = e;
+}
+
+// ======================================================================= one-SM tiles
+template <int BN>
+__device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_t *stages, const Ctx &c) {
+    using T = Cfg1<BN>;
+    const ClaimGeom g{static_cast<uint32_t>(p.num_units), static_cast<uint32_t>(p.num_tiles), blockIdx.x,
+                      gridDim.x, 1u};
+    int stage = 0, wq = 0;
+    uint32_t phase = 0, wphase = 0;
+    bool exhausted = false, stop = false;
+    while (!stop) {
+        const int2 it = claim_work(p, c, g, exhausted);
+        if (!wait_bar<false>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
+        s.items[wq] = it;
+        mbar_arrive(smem_u32(&s.wfull[wq]));
+        if (++wq == WQ) {
+            wq = 0;
+            wphase ^= 1u;
+        }
+        if (it.x == ITEM_END) break;
+        if (it.x != ITEM_COMPUTE) continue;
+        const int u = it.y, t = u / p.P, r = u - t * p.P;
+        int tm, tn;
+        raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
+                stop = true;
+                break;
+            }
+            const uint32_t fb = smem_u32(&s.full[stage]);
+            uint8_t *sa = stages + stage * T::STAGE_BYTES;
+            uint8_t *sb = sa + T::A_BYTES;
+            mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
+            tma_load_2d(smem_u32(sa), &p.tmA[r], fb, kb * MK_BK, tm * MK_BM);
+#pragma unroll
+            for (int j = 0; j < T::B_BOXES; ++j)
+                tma_load_2d(smem_u32(sb + j * T::B_BOX_BYTES), &p.tmB[r], fb, tn * BN + j * 64, kb * MK_BK);
+            ++s.issued;
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // Every TMA load this thread issued must have landed before the block exits (normally the
+    // MMA warp has waited for all of them already; this matters after a pipeline timeout).
+    const uint32_t n = s.issued;
+    for (uint32_t i = n > T::STAGES ? n - T::STAGES : 0; i < n; ++i)
+        wait_bar<false>(smem_u32(&s.full[i % T::STAGES]), (i / T::STAGES) & 1u, c, SITE_DRAIN, i);
+}
+
+template <int BN>
+__device__ void run1_mma(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
+                         uint32_t tmem_base) {
+    using T = Cfg1<BN>;
+    int stage = 0, acc = 0, wq = 0;
+    uint32_t phase = 0, aphase = 0, wphase = 0;
+    for (;;) {
+        if (!wait_bar<false>(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0)) break;
+        const int2 it = s.items[wq];
+        mbar_arrive(smem_u32(&s.wempty[wq]));
+        if (++wq == WQ) {
+            wq = 0;
+            wphase ^= 1u;
+        }
+        if (it.x == ITEM_END) break;
+        if (it.x != ITEM_COMPUTE) continue;
+        if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
+        tc_fence_after();
+        const long long t0 = clock64();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bar<false>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
+            const uint32_t sb = sa + T::A_BYTES;
+            // A: K-major, rows 128 B apart, 8-row groups 1024 B apart; K step of 16 = +32 B.
+            // B: MN-major, 64-column boxes 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO);
+            //    K step of 16 rows = +2048 B.
+            const uint64_t ad = sw128_desc(sa, 16, 1024);
+            const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
+#pragma unroll
+            for (int kk = 0; kk < MK_BK / 16; ++kk)
+                umma_bf16(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128), T::IDESC,
+                          static_cast<uint32_t>((kb | kk) != 0));
+            umma_commit(smem_u32(&s.empty[stage]));
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&s.tfull[acc]));
+        if (++acc == ACC) {
+            acc = 0;
+            aphase ^= 1u;
+        }
+        atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
+                  static_cast<unsigned long long>(clock64() - t0));
+    }
+    // Every MMA issued by this thread must complete before TMEM is released.
+    umma_commit(smem_u32(&s.drain));
+    wait_bar<false>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
+}
+
+template <int BN>
+__device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base,
+                              uint32_t epoch) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int etid = threadIdx.x - MK_EPI_WARP0 * 32;
+    int acc = 0, wq = 0;
+    uint32_t aphase = 0, wphase = 0;
+    for (;;) {
+        bool ok = true;
+        if (lane == 0) ok = wait_bar<false>(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0);
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!bar_and(1, MK_EPI_THREADS, ok)) break;
+        const int2 it = s.items[wq];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.wempty[wq]));
+        if (++wq == WQ) {
+            wq = 0;
+            wphase ^= 1u;
+        }
+        if (it.x == ITEM_END) break;
+        if (it.x == ITEM_COMPUTE) {
+            const int u = it.y, t = u / p.P, r = u - t * p.P;
+            int tm, tn;
+            raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+            const int lt = tm * p.tiles_n + tn;
+            ok = true;
+            if (lane == 0) ok = wait_bar<false>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
+            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+            if (!bar_and(1, MK_EPI_THREADS, ok)) break;
+            tc_fence_after();
+            store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[acc]));
+            if (++acc == ACC) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+            bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
+            if (etid == 0) {
+                st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
+                atomicAdd(&c.hdr->units_done, 1u);
+            }
+        } else {
+            int tm, tn;
+            raster(it.y, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+            do_reduce<BN>(p, c, tm, tn, etid, epoch);
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(MK_THREADS, 1) mk_persistent_kernel(const __grid_constant__ MkParams p) {
-    using T = TileCfg<BN>;
+    using T = Cfg1<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                   ~static_cast<uintptr_t>(1023));
-    SmemCtl<BN> &s = *reinterpret_cast<SmemCtl<BN> *>(stages + T::STAGES * T::STAGE_BYTES);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    SmemCtl<T::STAGES> &s = *reinterpret_cast<SmemCtl<T::STAGES> *>(stages + T::STAGES * T::STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < T::STAGES; ++i) {
-            mbar_init(smem_u32(&s.full[i]), 1);
-            mbar_init(smem_u32(&s.empty[i]), 1);
-        }
-        for (int i = 0; i < T::ACC; ++i) {
-            mbar_init(smem_u32(&s.tfull[i]), 1);
-            mbar_init(smem_u32(&s.tempty[i]), MK_EPI_THREADS / 32);
-        }
-        for (int i = 0; i < T::WQ; ++i) {
-            mbar_init(smem_u32(&s.wfull[i]), 1);
-            mbar_init(smem_u32(&s.wempty[i]), 1 + MK_EPI_THREADS / 32);
-        }
-        mbar_init(smem_u32(&s.drain), 1);
-        fence_mbar_init();
-        s.abort = 0;
-        uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
-        if (e == 0u) e = 1u;
-        s.epoch = e;
-    }
-    if (warp == 0 && lane == 0) {
+    if (threadIdx.x == 0) init_barriers<T::STAGES>(s, p, 1, MK_EPI_THREADS / 32, 1 + MK_EPI_THREADS / 32);
+    if (warp == 0 && lane == 0)
         for (int r = 0; r < p.P; ++r) {
             prefetch_tmap(&p.tmA[r]);
             prefetch_tmap(&p.tmB[r]);
         }
-    }
     if (warp == 1) {
         tmem_alloc(smem_u32(&s.tmem_base), T::TMEM_COLS);
         tmem_relinquish();
@@ -659,22 +690,18 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_persistent_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem_base = s.tmem_base;
     const uint32_t epoch = s.epoch;
-    Ctx c{p.hdr, &s.abort, p.timeout_ns};
+    const Ctx c{p.hdr, &s.abort, p.timeout_ns, 4 * p.timeout_ns};
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN>(p, s, stages, c);
-        __syncwarp();
+        if (lane == 0) run1_producer<BN>(p, s, stages, c);
     } else if (warp == 1) {
-        if (lane == 0) run_mma<BN>(p, s, stages, c, tmem_base);
-        __syncwarp();
+        if (lane == 0) run1_mma<BN>(p, s, stages, c, tmem_base);
     } else if (warp < MK_CTRL_WARP) {
-        run_epilogue<BN>(p, s, c, tmem_base, epoch);
-        __syncwarp();
-    } else {
-        if (lane == 0 && blockIdx.x == 0 && p.mode == MK_MODE_ADAPTIVE) run_controller(p, c);
-        __syncwarp();
+        run1_epilogue<BN>(p, s, c, tmem_base, epoch);
+    } else if (lane == 0 && blockIdx.x == 0 && p.mode == MK_MODE_ADAPTIVE) {
+        run_controller(p, c, p.num_units, p.num_tiles, 1, gridDim.x, 1);
     }
-
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -682,63 +709,396 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_persistent_kernel(const __gr
     if (threadIdx.x == 0) finish_call(p, epoch);
 }
 
+// ======================================================================= SM-pair tiles
+// Pair geometry: pair tile (sm, tn) covers tile rows 2*sm (even CTA) and 2*sm+1 (odd CTA).
+// Compute unit u = pair_tile * P + r; reduce item i = pair tile i (each CTA reduces its row).
+//
+// Barriers (same offsets in both CTAs; the even CTA's copy is the one used where noted):
+//   full[s]   even CTA, 2 arrivals (both producers' expect_tx) + both CTAs' TMA bytes
+//   empty[s]  both, 1 arrival: the MMA commit multicast to both CTAs
+//   tfull[a]  both, 1 arrival: commit multicast
+//   tempty[a] even CTA, 16 arrivals: 8 epilogue warps of each CTA
+//   wfull[q]  both, 1 arrival: the even CTA's scheduler
+//   wempty[q] even CTA, 18 arrivals: MMA + 8 epilogue warps (even), producer + 8 epilogue (odd)
+template <int BN>
+__device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
+                              uint32_t crank) {
+    using T = Cfg2<BN>;
+    const bool leader = crank == 0;
+    const ClaimGeom g{static_cast<uint32_t>(p.num_pair_units), static_cast<uint32_t>(p.num_pair_tiles),
+                      blockIdx.x >> 1, gridDim.x >> 1, 2u};
+    const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
+    const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
+    const uint32_t peer_items = mapa_shared(smem_u32(&s.items[0]), 1);
+    const uint32_t peer_wfull = mapa_shared(smem_u32(&s.wfull[0]), 1);
+    int stage = 0, wq = 0;
+    uint32_t phase = 0, wphase = 0;
+    bool exhausted = false, stop = false;
+    while (!stop) {
+        int2 it;
+        if (leader) {
+            it = claim_work(p, c, g, exhausted);
+            if (!wait_bar<true>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
+            s.items[wq] = it;
+            st_cluster_v2(peer_items + 8u * wq, it.x, it.y);
+            mbar_arrive(smem_u32(&s.wfull[wq]));
+            mbar_arrive_cluster(peer_wfull + 8u * wq);
+        } else {
+            if (!wait_bar<true>(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0)) break;
+            it = s.items[wq];
+            mbar_arrive_cluster(wempty0 + 8u * wq);
+        }
+        if (++wq == WQ) {
+            wq = 0;
+            wphase ^= 1u;
+        }
+        if (it.x == ITEM_END) break;
+        if (it.x != ITEM_COMPUTE) continue;
+        const int u = it.y, pt = u / p.P, r = u - pt * p.P;
+        int sm, tn;
+        raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+        const int tm = 2 * sm + static_cast<int>(crank);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bar<true>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
+                stop = true;
+                break;
+            }
+            const uint32_t fb = full0 + 8u * stage;
+            const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
+            const uint32_t sb = sa + T::A_BYTES;
+            mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
+            tma_load_2d_pair(sa, &p.tmA[r], fb, kb * MK_BK, tm * MK_BM);
+#pragma unroll
+            for (int j = 0; j < T::B_BOXES; ++j)
+                tma_load_2d_pair(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
+                                 tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK);
+            ++s.issued;
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+template <int BN>
+__device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
+                         uint32_t tmem_base) {
+    using T = Cfg2<BN>;
+    int stage = 0, acc = 0, wq = 0;
+    uint32_t phase = 0, aphase = 0, wphase = 0;
+    for (;;) {
+        if (!wait_bar<true>(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0)) break;
+        const int2 it = s.items[wq];
+        mbar_arrive(smem_u32(&s.wempty[wq]));
+        if (++wq == WQ) {
+            wq = 0;
+            wphase ^= 1u;
+        }
+        if (it.x == ITEM_END) break;
+        if (it.x != ITEM_COMPUTE) continue;
+        if (!wait_bar<true>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
+        tc_fence_after();
+        const long long t0 = clock64();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bar<true>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
+            const uint32_t sb = sa + T::A_BYTES;
+            // Per-CTA halves at identical offsets in both CTAs: A 128 rows (K-major), B BN/2
+            // columns (MN-major, 64-column boxes 8 KiB apart).
+            const uint64_t ad = sw128_desc(sa, 16, 1024);
+            const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
+#pragma unroll
+            for (int kk = 0; kk < MK_BK / 16; ++kk)
+                umma_bf16_pair(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
+                               T::IDESC, static_cast<uint32_t>((kb | kk) != 0));
+            umma_commit_pair(smem_u32(&s.empty[stage]), 0x3);
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&s.tfull[acc]), 0x3);
+        if (++acc == ACC) {
+            acc = 0;
+            aphase ^= 1u;
+        }
+        atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
+                  static_cast<unsigned long long>(clock64() - t0));
+    }
+    umma_commit_pair(smem_u32(&s.drain), 0x1);
+    wait_bar<true>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
+}
+
+template <int BN>
+__device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base,
+                              uint32_t epoch, uint32_t crank) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int etid = threadIdx.x - MK_EPI_WARP0 * 32;
+    const bool leader = crank == 0;
+    const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
+    const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
+    int acc = 0, wq = 0;
+    uint32_t aphase = 0, wphase = 0;
+    for (;;) {
+        bool ok = true;
+        if (lane == 0) ok = wait_bar<true>(smem_u32(&s.wfull[wq]), wphase, c, SITE_WORK_FULL, 0);
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!bar_and(1, MK_EPI_THREADS, ok)) break;
+        const int2 it = s.items[wq];
+        __syncwarp();
+        if (lane == 0) {
+            if (leader) mbar_arrive(smem_u32(&s.wempty[wq]));
+            else mbar_arrive_cluster(wempty0 + 8u * wq);
+        }
+        if (++wq == WQ) {
+            wq = 0;
+            wphase ^= 1u;
+        }
+        if (it.x == ITEM_END) break;
+        if (it.x == ITEM_COMPUTE) {
+            const int u = it.y, pt = u / p.P, r = u - pt * p.P;
+            int sm, tn;
+            raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+            const int tm = 2 * sm + static_cast<int>(crank);
+            const bool exists = tm < p.tiles_m;
+            const int lt = tm * p.tiles_n + tn;
+            ok = true;
+            if (lane == 0) ok = wait_bar<true>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
+            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+            if (!bar_and(1, MK_EPI_THREADS, ok)) break;
+            tc_fence_after();
+            if (exists) store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(smem_u32(&s.tempty[acc]));
+                else mbar_arrive_cluster(tempty0 + 8u * acc);
+            }
+            if (++acc == ACC) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+            bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
+            if (etid == 0) {
+                if (exists) st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
+                atomicAdd(&c.hdr->units_done, 1u);
+            }
+        } else {
+            int sm, tn;
+            raster(it.y, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+            do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, etid, epoch);
+        }
+    }
+}
+
+// Run by the even CTA's thread 0 between two cluster barriers at exit: make sure every K-slice
+// load either producer issued has landed.  Both producers issue loads in the same stage order,
+// so load i uses full[i % STAGES] in phase (i / STAGES) & 1, and only the last STAGES loads can
+// be outstanding.  A load armed by one producer only (the other stopped after a pipeline
+// timeout) gets the missing arrival here, so its phase completes once its bytes land.
+template <int STAGES>
+__device__ void pair_drain_loads(SmemCtl<STAGES> &s, const Ctx &c) {
+    const uint32_t nl = s.issued, np = s.peer_issued;
+    const uint32_t n = nl > np ? nl : np;
+    for (uint32_t i = n > STAGES ? n - STAGES : 0; i < n; ++i) {
+        const uint32_t bar = smem_u32(&s.full[i % STAGES]);
+        if (i >= nl) mbar_arrive(bar);
+        if (i >= np) mbar_arrive(bar);
+        wait_bar<true>(bar, (i / STAGES) & 1u, c, SITE_DRAIN, i);
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(MK_THREADS, 1) mk_pair_kernel(const __grid_constant__ MkParams p) {
+    using T = Cfg2<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~static_cast<uintptr_t>(1023));
+    SmemCtl<T::STAGES> &s = *reinterpret_cast<SmemCtl<T::STAGES> *>(stages + T::STAGES * T::STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_ctarank();
+
+    if (threadIdx.x == 0)
+        init_barriers<T::STAGES>(s, p, 2, 2 * (MK_EPI_THREADS / 32), 2 * (1 + MK_EPI_THREADS / 32));
+    if (warp == 0 && lane == 0)
+        for (int r = 0; r < p.P; ++r) {
+            prefetch_tmap(&p.tmA[r]);
+            prefetch_tmap(&p.tmB[r]);
+        }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&s.tmem_base), T::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    const uint32_t epoch = s.epoch;
+    const Ctx c{p.hdr, &s.abort, p.timeout_ns, 4 * p.timeout_ns};
+
+    if (warp == 0) {
+        if (lane == 0) run2_producer<BN>(p, s, stages, c, crank);
+    } else if (warp == 1) {
+        if (lane == 0 && crank == 0) run2_mma<BN>(p, s, stages, c, tmem_base);
+    } else if (warp < MK_CTRL_WARP) {
+        run2_epilogue<BN>(p, s, c, tmem_base, epoch, crank);
+    } else if (lane == 0 && blockIdx.x == 0 && p.mode == MK_MODE_ADAPTIVE) {
+        run_controller(p, c, p.num_pair_units, 2 * p.num_pair_tiles, 2, gridDim.x >> 1, 2);
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && crank == 1) st_cluster_u32(mapa_shared(smem_u32(&s.peer_issued), 0), s.issued);
+    tc_fence_before();
+    cluster_sync();
+    if (threadIdx.x == 0 && crank == 0) pair_drain_loads<T::STAGES>(s, c);
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, T::TMEM_COLS);
+    if (threadIdx.x == 0) finish_call(p, epoch);
+}
+
 // Second kernel of the unfused baseline: reduce every tile after the GEMM kernel finished
 // (stream order replaces the readiness flags).
 template <int BN>
 __global__ void __launch_bounds__(MK_EPI_THREADS) mk_reduce_kernel(const __grid_constant__ MkParams p) {
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        reduce_tile_body<BN>(p, t, threadIdx.x);
+    for (int lt = blockIdx.x; lt < p.num_tiles; lt += gridDim.x) {
+        reduce_tile_body<BN>(p, lt / p.tiles_n, lt % p.tiles_n, threadIdx.x);
         __syncthreads();
-        if (p.discard) discard_tile<BN>(p, t, threadIdx.x, MK_EPI_THREADS);
+        if (p.discard) discard_tile<BN>(p, lt, threadIdx.x, MK_EPI_THREADS);
     }
 }
 
 }  // namespace mk
 
 // ------------------------------------------------------------------ host-side launch helpers
-template <int BN>
+template <int BN, bool PAIR>
 static size_t smem_bytes_for() {
-    using T = mk::TileCfg<BN>;
-    return static_cast<size_t>(T::STAGES) * T::STAGE_BYTES + sizeof(mk::SmemCtl<BN>) + 1024;
+    if (PAIR) {
+        using T = mk::Cfg2<BN>;
+        return static_cast<size_t>(T::STAGES) * T::STAGE_BYTES + sizeof(mk::SmemCtl<T::STAGES>) + 1024;
+    }
+    using T = mk::Cfg1<BN>;
+    return static_cast<size_t>(T::STAGES) * T::STAGE_BYTES + sizeof(mk::SmemCtl<T::STAGES>) + 1024;
 }
 
-size_t mk_persistent_smem_bytes(int bn) { return bn == 256 ? smem_bytes_for<256>() : smem_bytes_for<128>(); }
-
-cudaError_t mk_prepare_kernels(int bn) {
-    if (bn == 256)
-        return cudaFuncSetAttribute(mk::mk_persistent_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem_bytes_for<256>()));
-    return cudaFuncSetAttribute(mk::mk_persistent_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem_bytes_for<128>()));
+template <int BN, bool PAIR>
+static void *kernel_ptr() {
+    return PAIR ? reinterpret_cast<void *>(mk::mk_pair_kernel<BN>)
+                : reinterpret_cast<void *>(mk::mk_persistent_kernel<BN>);
 }
 
-cudaError_t mk_max_persistent_ctas(int bn, int *ctas_per_sm) {
-    cudaError_t e = mk_prepare_kernels(bn);
+template <int BN, bool PAIR>
+static cudaError_t prepare() {
+    return cudaFuncSetAttribute(kernel_ptr<BN, PAIR>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_bytes_for<BN, PAIR>()));
+}
+
+template <int BN, bool PAIR>
+static cudaError_t max_ctas(int *ctas) {
+    cudaError_t e = prepare<BN, PAIR>();
     if (e != cudaSuccess) return e;
-    if (bn == 256)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, mk::mk_persistent_kernel<256>,
-                                                             MK_THREADS, smem_bytes_for<256>());
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, mk::mk_persistent_kernel<128>, MK_THREADS,
-                                                         smem_bytes_for<128>());
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (!PAIR) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mk::mk_persistent_kernel<BN>, MK_THREADS,
+                                                          smem_bytes_for<BN, PAIR>());
+        *ctas = per_sm * sms;
+        return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    cfg.blockDim = dim3(MK_THREADS);
+    cfg.dynamicSmemBytes = smem_bytes_for<BN, PAIR>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, mk::mk_pair_kernel<BN>, &cfg);
+    *ctas = 2 * clusters;
+    return e;
 }
 
-template <int BN>
-static cudaError_t launch_persistent_bn(const MkParams &p, int num_ctas, cudaStream_t s) {
+// Whether this process's runtime accepted a cooperative launch of the clustered kernel
+// (-1 unknown, 0 no, 1 yes).  Without it, co-residency rests on the occupancy check the host
+// makes before every launch, and the bounded device waits turn a starved grid into an error.
+static int g_coop_cluster = -1;
+
+template <int BN, bool PAIR>
+static cudaError_t launch_bn(const MkParams &p, int num_ctas, cudaStream_t s) {
+    if (PAIR && g_coop_cluster != 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
+        cfg.blockDim = dim3(MK_THREADS);
+        cfg.dynamicSmemBytes = smem_bytes_for<BN, PAIR>();
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, mk::mk_pair_kernel<BN>, p);
+        if (e == cudaSuccess) {
+            g_coop_cluster = 1;
+            return e;
+        }
+        if (g_coop_cluster == 1) return e;
+        (void)cudaGetLastError();   // configuration error, not sticky: retry without it
+        g_coop_cluster = 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
     cfg.blockDim = dim3(MK_THREADS);
-    cfg.dynamicSmemBytes = smem_bytes_for<BN>();
+    cfg.dynamicSmemBytes = smem_bytes_for<BN, PAIR>();
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;   // all blocks co-resident, or no launch
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (!PAIR) {
+        attr[n].id = cudaLaunchAttributeCooperative;   // all blocks co-resident, or no launch
+        attr[n].val.cooperative = 1;
+        ++n;
+    } else {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
+    if (PAIR) return cudaLaunchKernelEx(&cfg, mk::mk_pair_kernel<BN>, p);
     return cudaLaunchKernelEx(&cfg, mk::mk_persistent_kernel<BN>, p);
 }
 
-cudaError_t mk_launch_persistent(const MkParams &p, int bn, int num_ctas, cudaStream_t s) {
-    return bn == 256 ? launch_persistent_bn<256>(p, num_ctas, s) : launch_persistent_bn<128>(p, num_ctas, s);
+size_t mk_persistent_smem_bytes(int bn, bool pair) {
+    if (pair) return bn == 256 ? smem_bytes_for<256, true>() : smem_bytes_for<128, true>();
+    return bn == 256 ? smem_bytes_for<256, false>() : smem_bytes_for<128, false>();
+}
+
+cudaError_t mk_max_persistent_ctas(int bn, bool pair, int *ctas) {
+    if (pair) return bn == 256 ? max_ctas<256, true>(ctas) : max_ctas<128, true>(ctas);
+    return bn == 256 ? max_ctas<256, false>(ctas) : max_ctas<128, false>(ctas);
+}
+
+cudaError_t mk_launch_persistent(const MkParams &p, int bn, bool pair, int num_ctas, cudaStream_t s) {
+    if (pair) return bn == 256 ? launch_bn<256, true>(p, num_ctas, s) : launch_bn<128, true>(p, num_ctas, s);
+    return bn == 256 ? launch_bn<256, false>(p, num_ctas, s) : launch_bn<128, false>(p, num_ctas, s);
 }
 
 cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s) {

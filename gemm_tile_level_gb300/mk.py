@@ -35,6 +35,7 @@ MK_SPLIT_STATIC = 1
 MK_SPLIT_UNFUSED = 2
 
 MK_FLAG_KEEP_PARTIALS = 1
+MK_FLAG_SINGLE_SM_TILES = 2
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",

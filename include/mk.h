@@ -68,25 +68,31 @@ typedef enum {
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */
-#define MK_FLAG_KEEP_PARTIALS 1u /* do not discard consumed partial tiles from L2 (default: discard) */
+#define MK_FLAG_KEEP_PARTIALS 1u   /* do not discard consumed partial tiles from L2 (default: discard) */
+#define MK_FLAG_SINGLE_SM_TILES 2u /* one SM per 128 x 256 compute tile instead of an SM pair per 256 x 256 */
 
 /*
  * Options.  Start from mk_opts_default() and change fields; a NULL mk_opts*
  * means the defaults.
  *   split_mode      : mk_split_mode.
- *   comm_sms        : MK_SPLIT_STATIC: number of communication-role blocks,
- *                     1 <= comm_sms < persistent grid size.  MK_SPLIT_ADAPTIVE:
- *                     initial target (0 = derived from the shape).  Ignored
- *                     for MK_SPLIT_UNFUSED.
+ *   comm_sms        : MK_SPLIT_STATIC: number of SMs in the communication role,
+ *                     1 <= comm_sms <= grid size - 2 (SM-pair tiles, the
+ *                     default, assign roles per pair, so an odd count is
+ *                     rounded up to whole pairs; with MK_FLAG_SINGLE_SM_TILES
+ *                     roles are per SM and comm_sms <= grid size - 1).
+ *                     MK_SPLIT_ADAPTIVE: initial target (0 = derived from the
+ *                     shape).  Ignored for MK_SPLIT_UNFUSED.
  *   wait_timeout_ns : limit of every device-side wait (readiness flags,
  *                     pipeline barriers, the controller's progress watchdog);
  *                     0 = 2 s.  A wait that runs out sets MK_ERR_TIMEOUT.
  *   trace, trace_bytes : optional device buffer receiving controller records
  *                     (mk_trace_record, see below); NULL/0 = off.
- *   num_ctas        : persistent grid size, 0 = one block per SM.
+ *   num_ctas        : persistent grid size (blocks, one per SM; even with
+ *                     SM-pair tiles), 0 = as many as can be co-resident.
  *   flags           : MK_FLAG_* bits.
  *   debug_skip_unit : fault injection for tests: the compute unit with this
- *                     index (tile * P + rank) is never produced, so the
+ *                     index (tile * P + rank, tiles of 256 rows with SM-pair
+ *                     tiles, of 128 rows otherwise) is never produced, so the
  *                     consumer's bounded wait must run out.  -1 = off.
  */
 typedef struct {

@@ -16,19 +16,22 @@ if torch.cuda.is_available():
     import gpu_util as gu
 
 
+@pytest.mark.parametrize("tiles", ["pair", "single"])
 @pytest.mark.parametrize("split", ["adaptive", "static"])
-def test_missing_unit_times_out_then_recovers(split):
+def test_missing_unit_times_out_then_recovers(split, tiles):
     wl = ig.Workload("fault", "allreduce", 4, 512, 512, 128, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32")
     A, B, Ad, Bd = gu.upload(wl)
     ws = api.workspace(mk.MK_OP_ALLREDUCE, 4, 512, 512, 128)
     mode = mk.MK_SPLIT_ADAPTIVE if split == "adaptive" else mk.MK_SPLIT_STATIC
-    o = api.make_opts(mode, comm_sms=3 if split == "static" else 0, timeout_ns=20_000_000, skip_unit=5)
+    fl = mk.MK_FLAG_SINGLE_SM_TILES if tiles == "single" else 0
+    o = api.make_opts(mode, comm_sms=4 if split == "static" else 0, timeout_ns=20_000_000, skip_unit=5, flags=fl)
     C, st = api.gemm_allreduce(Ad, Bd, mk.MK_F32, ws=ws, opts=o)
     assert st == mk.MK_OK                       # the launch itself is fine
     assert mk.mk_status_check(ws) == mk.MK_ERR_TIMEOUT
     assert "timed out" in mk.mk_last_error()
     assert mk.mk_status_check(ws) == mk.MK_OK   # read-and-clear
-    C = gu.call_ar(Ad, Bd, mk.MK_F32, ws=ws, opts=api.make_opts(mode, comm_sms=3 if split == "static" else 0))
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, ws=ws,
+                   opts=api.make_opts(mode, comm_sms=4 if split == "static" else 0, flags=fl))
     gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
 
 
@@ -58,6 +61,8 @@ def test_device_dependent_argument_checks():
     assert st == mk.MK_ERR_INVALID_ARG
     _, st = api.gemm_allreduce(Ad, Bd, mk.MK_F32, opts=api.make_opts(num_ctas=S + 1))
     assert st == mk.MK_ERR_NOT_RESIDENT
+    _, st = api.gemm_allreduce(Ad, Bd, mk.MK_F32, opts=api.make_opts(num_ctas=7))
+    assert st == mk.MK_ERR_INVALID_ARG      # SM pairs need an even grid
     # a smaller persistent grid is fine
     C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=api.make_opts(num_ctas=8))
     assert not C.any()

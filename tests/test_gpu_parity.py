@@ -19,9 +19,12 @@ if torch.cuda.is_available():
     import gpu_util as gu
 
 MODES = ("adaptive", "static", "unfused")
+TILES = ("pair", "single")   # SM-pair 256 x BN tiles (default) or one-SM 128 x BN tiles
 
 
-def opts_for(mode, comm_sms=4, **kw):
+def opts_for(mode, comm_sms=4, tiles="pair", **kw):
+    if tiles == "single":
+        kw["flags"] = kw.get("flags", 0) | mk.MK_FLAG_SINGLE_SM_TILES
     if mode == "adaptive":
         return api.make_opts(mk.MK_SPLIT_ADAPTIVE, **kw)
     if mode == "static":
@@ -37,19 +40,21 @@ def dtype_code(s):
 SMALL = ig.WORKLOADS["ar_p2_m128_n128_k256"]
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("mode", MODES)
-def test_small_integer_bit_exact(mode):
+def test_small_integer_bit_exact(mode, tiles):
     A, B, Ad, Bd = gu.upload(SMALL, integer=True)
     ref = oracle.allreduce(A, B)
-    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=1))
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=1, tiles=tiles))
     gu.assert_bit_exact(gu.host_values(C), ref)
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("mode", MODES)
-def test_small_random_within_tolerance(mode):
+def test_small_random_within_tolerance(mode, tiles):
     A, B, Ad, Bd = gu.upload(SMALL)
     ref = oracle.allreduce(A, B)
-    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=1))
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=1, tiles=tiles))
     gu.check_tolerance(gu.host_values(C), ref, out_bf16=False)
 
 
@@ -73,9 +78,10 @@ def test_edge_shapes_integer_bit_exact(P, M, N, Kr, out):
     wl = ig.Workload("edge", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, out, seed=P + M)
     A, B, Ad, Bd = gu.upload(wl)
     ref = gu.rounded_reference(oracle.allreduce(A, B), out == "bf16")
-    for mode in MODES:
-        C = gu.call_ar(Ad, Bd, dtype_code(out), opts=opts_for(mode, comm_sms=2))
-        gu.assert_bit_exact(gu.host_values(C), ref)
+    for tiles in TILES:
+        for mode in MODES:
+            C = gu.call_ar(Ad, Bd, dtype_code(out), opts=opts_for(mode, comm_sms=2, tiles=tiles))
+            gu.assert_bit_exact(gu.host_values(C), ref)
 
 
 @pytest.mark.parametrize("P,M,N,Kr", EDGE_SHAPES)
@@ -84,9 +90,10 @@ def test_edge_shapes_random_within_tolerance(P, M, N, Kr):
                      "bf16", seed=3)
     A, B, Ad, Bd = gu.upload(wl)
     ref = oracle.allreduce(A, B)
-    for out in ("f32", "bf16"):
-        C = gu.call_ar(Ad, Bd, dtype_code(out))
-        gu.check_tolerance(gu.host_values(C), ref, out_bf16=(out == "bf16"))
+    for tiles in TILES:
+        for out in ("f32", "bf16"):
+            C = gu.call_ar(Ad, Bd, dtype_code(out), opts=opts_for("adaptive", tiles=tiles))
+            gu.check_tolerance(gu.host_values(C), ref, out_bf16=(out == "bf16"))
 
 
 def test_zero_k_gives_zeros_and_empty_is_noop():
@@ -117,10 +124,11 @@ def test_reducescatter_small_and_ragged_shards():
         wl = ig.Workload("rs", "reducescatter", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16")
         A, B, Ad, Bd = gu.upload(wl)
         want = [gu.rounded_reference(s, True) for s in oracle.reducescatter(A, B)]
-        for mode in MODES:
-            shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=opts_for(mode, comm_sms=2))
-            for s in range(P):
-                gu.assert_bit_exact(gu.host_values(shards[s]), want[s])
+        for tiles in TILES:
+            for mode in MODES:
+                shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=opts_for(mode, comm_sms=2, tiles=tiles))
+                for s in range(P):
+                    gu.assert_bit_exact(gu.host_values(shards[s]), want[s])
 
 
 def test_workspace_reuse_across_calls_and_shapes():
@@ -130,9 +138,10 @@ def test_workspace_reuse_across_calls_and_shapes():
         wl = ig.Workload("reuse", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32",
                          seed=i)
         A, B, Ad, Bd = gu.upload(wl)
-        for mode in MODES:
-            C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode), ws=ws)
-            gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
+        for tiles in TILES:
+            for mode in MODES:
+                C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, tiles=tiles), ws=ws)
+                gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
 
 
 # ------------------------------------------------------------------ the 2048 x 4096 workload
@@ -148,6 +157,8 @@ def test_mid_workload_full_oracle_comparison():
         gu.check_tolerance(gu.host_values(outs[mode]), ref, out_bf16=True)
     c32 = gu.call_ar(Ad, Bd, mk.MK_F32)
     gu.check_tolerance(gu.host_values(c32), ref, out_bf16=False)
+    single = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for("adaptive", tiles="single"))
+    gu.check_tolerance(gu.host_values(single), ref, out_bf16=True)
     # one fixed-order sum regardless of the schedule, and bf16 = RNE(fp32) of that sum
     assert torch.equal(outs["adaptive"], outs["unfused"]) and torch.equal(outs["static"], outs["unfused"])
     assert torch.equal(outs["adaptive"], c32.to(torch.bfloat16))
@@ -181,7 +192,7 @@ MLP = ig.WORKLOADS["ar_mlp_down_p8_m8192_n8192_k3584"]
 
 def test_mlp_down_projection_sampled_and_schedule_invariant():
     Ad, Bd, C = sampled_check(MLP, lambda Ad, Bd: gu.call_ar(Ad, Bd, mk.MK_BF16))
-    for mode, nr in (("unfused", 0), ("static", 1), ("static", 16), ("static", gu.num_sms() // 2)):
+    for mode, nr in (("unfused", 0), ("static", 2), ("static", 16), ("static", gu.num_sms() // 2)):
         other = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for(mode, comm_sms=nr))
         assert torch.equal(C, other), (mode, nr)
 
@@ -210,6 +221,6 @@ def test_reducescatter_full_size_sampled_and_equal_to_allreduce_rows():
 def test_sweep_shapes_sampled_and_split_invariant(M):
     wl = ig.sweep_workload(M)
     Ad, Bd, C = sampled_check(wl, lambda Ad, Bd: gu.call_ar(Ad, Bd, mk.MK_BF16), n=1024)
-    for nr in (1, gu.num_sms() - 1):
+    for nr in (2, gu.num_sms() - 2):
         assert torch.equal(C, gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for("static", comm_sms=nr)))
     assert torch.equal(C, gu.call_ar(Ad, Bd, mk.MK_BF16, opts=opts_for("unfused")))
