@@ -259,12 +259,15 @@ def reference_arm(args, wl, ranks):
 
 
 # ------------------------------------------------------------------ GPU arm
+_EXTRA_FLAGS = 0   # MK_FLAG_SINGLE_SM_TILES (--tiles single), MK_FLAG_NO_COOPERATIVE (--no-cooperative)
+
+
 def split_opts(api, mk, split: str, comm_sms: int):
     if split == "adaptive":
-        return api.make_opts(mk.MK_SPLIT_ADAPTIVE, comm_sms=comm_sms)
+        return api.make_opts(mk.MK_SPLIT_ADAPTIVE, comm_sms=comm_sms, flags=_EXTRA_FLAGS)
     if split == "static":
-        return api.make_opts(mk.MK_SPLIT_STATIC, comm_sms=comm_sms)
-    return api.make_opts(mk.MK_SPLIT_UNFUSED)
+        return api.make_opts(mk.MK_SPLIT_STATIC, comm_sms=comm_sms, flags=_EXTRA_FLAGS)
+    return api.make_opts(mk.MK_SPLIT_UNFUSED, flags=_EXTRA_FLAGS)
 
 
 class Problem:
@@ -383,7 +386,8 @@ def gpu_arm(args, wl, ranks):
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json, burst)" if peak_src == "measured" else "fallback"
     roof["roofline_frac"] = max(t_tensor, t_hbm) / (kernel_ms * 1e-3)
     roof["algorithmic_bytes"] = bytes_alg
-    roof["kernel"] = "mk_persistent_kernel<256>" if wl.N > 128 else "mk_persistent_kernel<128>"
+    roof["kernel"] = ("mk_persistent_kernel" if _EXTRA_FLAGS & 2 else "mk_pair_kernel") + (
+        "<256>" if wl.N > 128 else "<128>")
 
     if ranks.rank != 0:
         return
@@ -400,7 +404,7 @@ def gpu_arm(args, wl, ranks):
             "data": "synthetic",
             "config": {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
                        "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype, "split": args.split,
-                       "accumulate": "fp32", "seed": wl.seed,
+                       "accumulate": "fp32", "seed": wl.seed, "tiles": args.tiles,
                        "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
                        "parallelism": f"{wl.P} logical ranks on one GPU" + (
                            f"; {ranks.world} replicas" if ranks.world > 1 else "")},
@@ -467,7 +471,9 @@ def sweep(args):
                 return tot / steps
 
             adaptive = ms(split_opts(api, mk, "adaptive", 0))
-            static = {nr: ms(split_opts(api, mk, "static", nr)) for nr in range(1, S, args.sweep_stride)}
+            # SM-pair tiles assign roles per pair: sweep even SM counts 2..S-2
+            lo, step = (1, args.sweep_stride) if _EXTRA_FLAGS & 2 else (2, max(2, args.sweep_stride))
+            static = {nr: ms(split_opts(api, mk, "static", nr)) for nr in range(lo, S - 1, step)}
             unf = ms(split_opts(api, mk, "unfused", 0))
             best_nr = min(static, key=static.get)
             rec = {"M": M, "adaptive_ms": adaptive, "best_static_ms": static[best_nr],
@@ -493,6 +499,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--split", choices=["adaptive", "static", "unfused"], default="adaptive")
     ap.add_argument("--comm-sms", type=int, default=0)
+    ap.add_argument("--tiles", choices=["pair", "single"], default="pair",
+                    help="SM-pair 256 x BN compute tiles (default) or one-SM 128 x BN tiles")
+    ap.add_argument("--no-cooperative", action="store_true",
+                    help="launch without the cooperative attribute (for profilers that cannot replay it)")
     ap.add_argument("--shape", default="", help="P,M,N,K_per_rank override (same distributions); "
                     "for small profiling cases")
     ap.add_argument("--no-e2e", action="store_true")
@@ -507,6 +517,8 @@ def main():
     ap.add_argument("--sweep-out", default="")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    global _EXTRA_FLAGS
+    _EXTRA_FLAGS = (2 if args.tiles == "single" else 0) | (8 if args.no_cooperative else 0)
     if args.sweep:
         sweep(args)
         return

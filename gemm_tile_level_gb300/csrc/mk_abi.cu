@@ -26,7 +26,17 @@ mk_status fail_cuda(cudaError_t e, const char *what) {
 }
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
-constexpr int kRasterGroup = 8;
+constexpr double kRasterL2Budget = 32e6;   // bytes of A rows (all ranks) kept resident per group
+
+// Rows of compute tiles per raster group: the group's A rows of all P ranks should fit in a
+// slice of L2 so that each B column streamed past them is reused by the whole group.
+int auto_raster_group(bool pair, int P, int64_t Kr, int64_t row_tiles) {
+    const double per_row = static_cast<double>(P) * (pair ? 2 * MK_BM : MK_BM) * static_cast<double>(Kr) * 2.0;
+    int64_t g = per_row > 0 ? static_cast<int64_t>(kRasterL2Budget / per_row) : row_tiles;
+    if (g > row_tiles) g = row_tiles;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
 constexpr int kCtrlPeriodNs = 1000;
 
 int choose_bn(int64_t N) { return N > 128 ? 256 : 128; }
@@ -107,6 +117,7 @@ mk_status check_opts(const mk_opts *o) {
         return fail(MK_ERR_INVALID_ARG, "static split needs comm_sms >= 1");
     if (o->comm_sms < 0) return fail(MK_ERR_INVALID_ARG, "comm_sms < 0");
     if (o->num_ctas < 0) return fail(MK_ERR_INVALID_ARG, "num_ctas < 0");
+    if (o->raster_group < 0) return fail(MK_ERR_INVALID_ARG, "raster_group < 0");
     if (o->trace_bytes && !o->trace) return fail(MK_ERR_INVALID_ARG, "trace_bytes without trace buffer");
     if (o->trace && !aligned16(o->trace)) return fail(MK_ERR_ALIGNMENT, "trace buffer not 16-byte aligned");
     return MK_OK;
@@ -214,7 +225,10 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
         if (init > role_units - 1) init = role_units - 1;
         p.init_nr = init < 1 ? 1 : init;
     }
-    p.raster_group = kRasterGroup;
+    p.raster_group = o.raster_group > 0 ? o.raster_group
+                                        : auto_raster_group(pair, P, Kr, pair ? g.pair_tiles_m : g.tiles_m);
+    p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
+    p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
     p.ctrl_period_ns = kCtrlPeriodNs;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -248,6 +262,8 @@ void mk_opts_default(mk_opts *o) {
     o->num_ctas = 0;
     o->flags = 0;
     o->debug_skip_unit = -1;
+    o->raster_group = 0;
+    o->reserved = 0;
 }
 
 size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank) {

@@ -70,6 +70,8 @@ struct MkParams {
     int32_t op, out_bf16, num_out, rows_per_shard;
     int32_t mode, static_nr, init_nr, raster_group;
     int32_t discard;
+    int32_t l2_hints;            // TMA loads: A rows evict_last, B columns evict_first
+    int32_t cooperative;         // launch attribute (host side only)
     int32_t ctrl_period_ns;
 };
 

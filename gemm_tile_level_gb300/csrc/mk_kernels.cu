@@ -516,6 +516,9 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
     int stage = 0, wq = 0;
     uint32_t phase = 0, wphase = 0;
     bool exhausted = false, stop = false;
+    // A rows are reused by every column of the raster group: keep them; B columns stream.
+    const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+    const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
     while (!stop) {
         const int2 it = claim_work(p, c, g, exhausted);
         if (!wait_bar<false>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
@@ -539,10 +542,11 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
             uint8_t *sa = stages + stage * T::STAGE_BYTES;
             uint8_t *sb = sa + T::A_BYTES;
             mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
-            tma_load_2d(smem_u32(sa), &p.tmA[r], fb, kb * MK_BK, tm * MK_BM);
+            tma_load_2d_hint(smem_u32(sa), &p.tmA[r], fb, kb * MK_BK, tm * MK_BM, pol_a);
 #pragma unroll
             for (int j = 0; j < T::B_BOXES; ++j)
-                tma_load_2d(smem_u32(sb + j * T::B_BOX_BYTES), &p.tmB[r], fb, tn * BN + j * 64, kb * MK_BK);
+                tma_load_2d_hint(smem_u32(sb + j * T::B_BOX_BYTES), &p.tmB[r], fb, tn * BN + j * 64, kb * MK_BK,
+                                 pol_b);
             ++s.issued;
             if (++stage == T::STAGES) {
                 stage = 0;
@@ -734,6 +738,8 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     int stage = 0, wq = 0;
     uint32_t phase = 0, wphase = 0;
     bool exhausted = false, stop = false;
+    const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+    const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
     while (!stop) {
         int2 it;
         if (leader) {
@@ -759,7 +765,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
         const int tm = 2 * sm + static_cast<int>(crank);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bar<true>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
+            if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
                 stop = true;
                 break;
             }
@@ -767,11 +773,11 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
             const uint32_t sb = sa + T::A_BYTES;
             mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
-            tma_load_2d_pair(sa, &p.tmA[r], fb, kb * MK_BK, tm * MK_BM);
+            tma_load_2d_pair_hint(sa, &p.tmA[r], fb, kb * MK_BK, tm * MK_BM, pol_a);
 #pragma unroll
             for (int j = 0; j < T::B_BOXES; ++j)
-                tma_load_2d_pair(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
-                                 tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK);
+                tma_load_2d_pair_hint(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
+                                      tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK, pol_b);
             ++s.issued;
             if (++stage == T::STAGES) {
                 stage = 0;
@@ -779,6 +785,12 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             }
         }
     }
+    // The even CTA's MMA commits arrive (multicast) on this CTA's empty barriers once the MMAs
+    // that read each stage complete.  Wait for the arrivals that free the last stages this
+    // producer filled, so that no such arrive is still in flight when the CTA exits.
+    const uint32_t n = s.issued;
+    for (uint32_t i = n > T::STAGES ? n - T::STAGES : 0; i < n; ++i)
+        wait_bar<false>(smem_u32(&s.empty[i % T::STAGES]), (i / T::STAGES) & 1u, c, SITE_DRAIN, i);
 }
 
 template <int BN>
@@ -797,13 +809,13 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
         }
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
-        if (!wait_bar<true>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
+        if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
         tc_fence_after();
         const long long t0 = clock64();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bar<true>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
+            if (!wait_bar<false>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
                 ok = false;
                 break;
             }
@@ -834,7 +846,7 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
                   static_cast<unsigned long long>(clock64() - t0));
     }
     umma_commit_pair(smem_u32(&s.drain), 0x1);
-    wait_bar<true>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
+    wait_bar<false>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
 }
 
 template <int BN>
@@ -871,7 +883,7 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, c
             const bool exists = tm < p.tiles_m;
             const int lt = tm * p.tiles_n + tn;
             ok = true;
-            if (lane == 0) ok = wait_bar<true>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
+            if (lane == 0) ok = wait_bar<false>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
             ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             if (!bar_and(1, MK_EPI_THREADS, ok)) break;
             tc_fence_after();
@@ -880,7 +892,7 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, c
             __syncwarp();
             if (lane == 0) {
                 if (leader) mbar_arrive(smem_u32(&s.tempty[acc]));
-                else mbar_arrive_cluster(tempty0 + 8u * acc);
+                else mbar_arrive_remote(tempty0 + 8u * acc);
             }
             if (++acc == ACC) {
                 acc = 0;
@@ -912,7 +924,7 @@ __device__ void pair_drain_loads(SmemCtl<STAGES> &s, const Ctx &c) {
         const uint32_t bar = smem_u32(&s.full[i % STAGES]);
         if (i >= nl) mbar_arrive(bar);
         if (i >= np) mbar_arrive(bar);
-        wait_bar<true>(bar, (i / STAGES) & 1u, c, SITE_DRAIN, i);
+        wait_bar<false>(bar, (i / STAGES) & 1u, c, SITE_DRAIN, i);
     }
 }
 
@@ -1038,7 +1050,7 @@ static int g_coop_cluster = -1;
 
 template <int BN, bool PAIR>
 static cudaError_t launch_bn(const MkParams &p, int num_ctas, cudaStream_t s) {
-    if (PAIR && g_coop_cluster != 0) {
+    if (PAIR && p.cooperative && g_coop_cluster != 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
         cfg.blockDim = dim3(MK_THREADS);
@@ -1070,9 +1082,11 @@ static cudaError_t launch_bn(const MkParams &p, int num_ctas, cudaStream_t s) {
     cudaLaunchAttribute attr[2];
     int n = 0;
     if (!PAIR) {
-        attr[n].id = cudaLaunchAttributeCooperative;   // all blocks co-resident, or no launch
-        attr[n].val.cooperative = 1;
-        ++n;
+        if (p.cooperative) {
+            attr[n].id = cudaLaunchAttributeCooperative;   // all blocks co-resident, or no launch
+            attr[n].val.cooperative = 1;
+            ++n;
+        }
     } else {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = 2;

@@ -36,6 +36,8 @@ MK_SPLIT_UNFUSED = 2
 
 MK_FLAG_KEEP_PARTIALS = 1
 MK_FLAG_SINGLE_SM_TILES = 2
+MK_FLAG_NO_L2_HINTS = 4
+MK_FLAG_NO_COOPERATIVE = 8
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",
@@ -46,7 +48,8 @@ class mk_opts(ctypes.Structure):
     _fields_ = [("split_mode", ctypes.c_int32), ("comm_sms", ctypes.c_int32),
                 ("wait_timeout_ns", ctypes.c_uint64), ("trace", ctypes.c_void_p),
                 ("trace_bytes", ctypes.c_uint64), ("num_ctas", ctypes.c_int32),
-                ("flags", ctypes.c_uint32), ("debug_skip_unit", ctypes.c_int64)]
+                ("flags", ctypes.c_uint32), ("debug_skip_unit", ctypes.c_int64),
+                ("raster_group", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class mk_trace_record(ctypes.Structure):

@@ -70,6 +70,10 @@ typedef enum {
 /* Bits of mk_opts.flags */
 #define MK_FLAG_KEEP_PARTIALS 1u   /* do not discard consumed partial tiles from L2 (default: discard) */
 #define MK_FLAG_SINGLE_SM_TILES 2u /* one SM per 128 x 256 compute tile instead of an SM pair per 256 x 256 */
+#define MK_FLAG_NO_L2_HINTS 4u     /* load operands without L2 eviction-priority hints */
+#define MK_FLAG_NO_COOPERATIVE 8u  /* launch without the cooperative attribute (some profilers cannot replay
+                                      cooperative cluster launches); co-residency then rests on the
+                                      occupancy check made before every launch */
 
 /*
  * Options.  Start from mk_opts_default() and change fields; a NULL mk_opts*
@@ -94,6 +98,12 @@ typedef enum {
  *                     index (tile * P + rank, tiles of 256 rows with SM-pair
  *                     tiles, of 128 rows otherwise) is never produced, so the
  *                     consumer's bounded wait must run out.  -1 = off.
+ *   raster_group    : compute tiles are visited in groups of this many tile
+ *                     rows (256-row rows with SM-pair tiles), column by column
+ *                     inside a group, so that the group's A rows stay in L2
+ *                     while B columns stream past them; 0 = sized from the
+ *                     shape so that the group's A rows of all P ranks take
+ *                     about 32 MB.
  */
 typedef struct {
     int32_t split_mode;
@@ -104,6 +114,8 @@ typedef struct {
     int32_t num_ctas;
     uint32_t flags;
     int64_t debug_skip_unit;
+    int32_t raster_group;
+    int32_t reserved;
 } mk_opts;
 
 /* One controller record written to mk_opts.trace (32 bytes). */

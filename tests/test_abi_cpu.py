@@ -44,10 +44,10 @@ def test_struct_layout_matches_header(mk, tmp_path):
 #include <stddef.h>
 #include "mk.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(mk_opts), offsetof(mk_opts, comm_sms),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(mk_opts), offsetof(mk_opts, comm_sms),
          offsetof(mk_opts, wait_timeout_ns), offsetof(mk_opts, trace), offsetof(mk_opts, trace_bytes),
          offsetof(mk_opts, num_ctas), offsetof(mk_opts, flags), offsetof(mk_opts, debug_skip_unit),
-         sizeof(mk_trace_record));
+         sizeof(mk_trace_record), offsetof(mk_opts, raster_group));
   return 0;
 }
 """)
@@ -57,7 +57,7 @@ int main(void) {
     o = mk.mk_opts
     want = [ctypes.sizeof(o), o.comm_sms.offset, o.wait_timeout_ns.offset, o.trace.offset,
             o.trace_bytes.offset, o.num_ctas.offset, o.flags.offset, o.debug_skip_unit.offset,
-            ctypes.sizeof(mk.mk_trace_record)]
+            ctypes.sizeof(mk.mk_trace_record), o.raster_group.offset]
     assert got == want
 
 
