@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmk.so")
-SOURCES = ["mk_abi.cu", "mk_kernels.cu"]
+SOURCES = ["mk_abi.cu", "mk_kernels.cu", "mk_noalloc.cu"]
 HEADERS = ["mk_internal.h", "mk_ptx.cuh"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 

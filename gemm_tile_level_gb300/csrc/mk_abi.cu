@@ -249,6 +249,14 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
 
 }  // namespace
 
+void mk_internal_set_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+size_t mk_internal_flags_bytes(int P, int64_t M, int64_t N, int64_t K_per_rank) {
+    Geometry g;
+    if (!make_geometry(P, M, N, K_per_rank, &g)) return 0;
+    return g.partials_off - g.flags_off;
+}
+
 extern "C" {
 
 void mk_opts_default(mk_opts *o) {

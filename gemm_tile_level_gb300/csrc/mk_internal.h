@@ -75,6 +75,11 @@ struct MkParams {
     int32_t ctrl_period_ns;
 };
 
+// Implemented in mk_abi.cu: set the host thread's mk_last_error() text; bytes of the readiness
+// flag region (which follows the 256-byte header) of the AllReduce workspace for a shape.
+void mk_internal_set_error(const char *msg);
+size_t mk_internal_flags_bytes(int P, int64_t M, int64_t N, int64_t K_per_rank);
+
 // Implemented in mk_kernels.cu.  `pair` selects the SM-pair (cta_group::2, 256 x BN) kernel,
 // otherwise the one-SM (128 x BN) kernel.
 size_t mk_persistent_smem_bytes(int bn, bool pair);

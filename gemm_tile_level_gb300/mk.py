@@ -41,7 +41,10 @@ MK_FLAG_NO_COOPERATIVE = 8
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",
-            "mk_allgather_gemm", "mk_status_check", "mk_status_string", "mk_last_error")
+            "mk_allgather_gemm", "mk_gemm_allreduce_noalloc", "mk_status_check", "mk_status_string",
+            "mk_last_error")
+
+MK_NOALLOC_MAX_WS_BYTES = 64 << 20
 
 
 class mk_opts(ctypes.Structure):
@@ -82,6 +85,9 @@ for _name in ("mk_gemm_allreduce", "mk_gemm_reducescatter"):
 _lib.mk_allgather_gemm.argtypes = [_i32, _i64, _i64, _i64, _PP, _PP, _PP, _PP, _i32, _vp,
                                    ctypes.c_size_t, ctypes.POINTER(mk_opts), _vp]
 _lib.mk_allgather_gemm.restype = _i32
+_lib.mk_gemm_allreduce_noalloc.argtypes = [_i32, _i64, _i64, _i64, _PP, _PP, _PP, _i32,
+                                           ctypes.POINTER(mk_opts), _vp]
+_lib.mk_gemm_allreduce_noalloc.restype = _i32
 _lib.mk_status_check.argtypes = [_vp, _vp]
 _lib.mk_status_check.restype = _i32
 _lib.mk_status_string.argtypes = [_i32]
@@ -151,6 +157,13 @@ def mk_allgather_gemm(P, M, N, K, A_shard, B, A_gathered, C, out_dtype, ws, ws_b
                                       _nbytes(ws) if ws_bytes is None else ws_bytes,
                                       ctypes.byref(opts) if opts is not None else None,
                                       _stream(stream)))
+
+
+def mk_gemm_allreduce_noalloc(P, M, N, K_per_rank, A, B, C, out_dtype, opts=None, stream=None) -> int:
+    """mk_gemm_allreduce with the library's static workspace (for callers that cannot allocate)."""
+    return int(_lib.mk_gemm_allreduce_noalloc(P, M, N, K_per_rank, _ptrs(A), _ptrs(B), _ptrs(C), out_dtype,
+                                              ctypes.byref(opts) if opts is not None else None,
+                                              _stream(stream)))
 
 
 def mk_status_check(ws, stream=None) -> int:

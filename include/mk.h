@@ -189,6 +189,34 @@ mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *
                             void *cuda_stream);
 
 /*
+ * GEMM + AllReduce without any device allocation by the caller.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot obtain device
+ * memory at run time: runtimes that reserve the whole device up front and hand out
+ * nothing more, plug-ins that are given no allocator, and latency-critical loops that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation.
+ *   Arguments and results are those of mk_gemm_allreduce without the workspace: the
+ *   library supplies it from one static device array of MK_NOALLOC_MAX_WS_BYTES per
+ *   GPU, held from the first call on that GPU until the process exits.  Shapes whose
+ *   mk_workspace_size(MK_OP_ALLREDUCE, ...) exceeds that return
+ *   MK_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *   The first call on a device sets the array up (looks up its device address and
+ *   zeroes it, synchronously); make that first call before any stream capture.
+ *   Every call on a device shares the array and finds the previous call's contents;
+ *   each call clears the part that must start at zero.  Calls whose kernels overlap
+ *   on the GPU (different streams without ordering, or several host threads) race on
+ *   the array and give wrong results: order them.
+ *   The return value covers argument, size and launch errors.  Errors the kernel
+ *   detects (a bounded wait that ran out) are recorded in the static array and are
+ *   not reported here; callers that need them use mk_gemm_allreduce and
+ *   mk_status_check with a workspace of their own.
+ *   This entry point calls no allocating routine.
+ */
+#define MK_NOALLOC_MAX_WS_BYTES (64u << 20)
+mk_status mk_gemm_allreduce_noalloc(int P, int64_t M, int64_t N, int64_t K_per_rank,
+                                    const void *const *A, const void *const *B, void *const *C,
+                                    mk_dtype out_dtype, const mk_opts *opts, void *cuda_stream);
+
+/*
  * Synchronize `cuda_stream`, then read and clear the workspace status word.
  * Returns MK_ERR_CUDA if the synchronization itself fails, otherwise the
  * status the kernels recorded since the last check (MK_OK if none).
