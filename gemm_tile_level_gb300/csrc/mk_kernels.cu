@@ -37,6 +37,8 @@ namespace mk {
 
 enum { ITEM_END = 0, ITEM_COMPUTE = 1, ITEM_REDUCE = 2 };
 
+#define MK_REDUCE_RING_BYTES (192u * 1024u)   // staging ring of the standalone reduce kernel
+
 // Which wait gave up (written to the workspace header with MK_ERR_TIMEOUT).
 enum {
     SITE_WORK_EMPTY = 1, SITE_WORK_FULL = 2, SITE_STAGE_EMPTY = 3, SITE_STAGE_FULL = 4,
@@ -82,13 +84,14 @@ struct SmemCtl {
     uint64_t wfull[WQ];
     uint64_t wempty[WQ];
     uint64_t drain;
+    uint64_t rfull[3];      // reduce staging: one per chunk set in flight
     int2 items[WQ];
     uint32_t tmem_base;
     uint32_t epoch;
     int abort;
     uint32_t peer_issued;   // pair kernel: number of K-slice loads the odd CTA's producer issued
     uint32_t issued;        // number of K-slice loads this CTA's producer issued
-    int pad;
+    uint32_t epi_done;      // work items the epilogue group has finished (read by the scheduler)
 };
 
 struct Ctx {
@@ -278,46 +281,6 @@ __device__ __forceinline__ float *partial_tile(const MkParams &p, int r, int lt)
     return p.partials + (static_cast<size_t>(r) * p.num_tiles + lt) * (MK_BM * BN);
 }
 
-// Sum the P partial tiles of output tile (tm, tn) in rank order and write the result.  Thread
-// `tid` (0..255) owns row tid % 128 and one half of the column groups, so each warp load
-// instruction reads 512 contiguous bytes.  No waits and no barriers inside.
-template <int BN>
-__device__ __forceinline__ void reduce_tile_body(const MkParams &p, int tm, int tn, int tid) {
-    const int row = tid & (MK_BM - 1);
-    const int grow = tm * MK_BM + row;
-    if (grow >= p.M) return;
-    const int lt = tm * p.tiles_n + tn;
-    const int g_begin = (tid >> 7) * (BN / 8);
-    const size_t rank_stride4 = static_cast<size_t>(p.num_tiles) * (MK_BM * BN / 4);
-    const float4 *tile4 = reinterpret_cast<const float4 *>(partial_tile<BN>(p, 0, lt));
-#pragma unroll 1
-    for (int g = g_begin; g < g_begin + BN / 8; g += 4) {
-        const int gcol = tn * BN + g * 4;
-        if (gcol >= p.N) break;
-        const float4 *src = tile4 + static_cast<size_t>(g) * MK_BM + row;
-        float4 a[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a[j] = ld_cg_f4(src + j * MK_BM);
-#pragma unroll 1
-        for (int r = 1; r < p.P; ++r) {
-            const float4 *sr = src + r * rank_stride4;
-            float4 x[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = ld_cg_f4(sr + j * MK_BM);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                a[j].x += x[j].x;
-                a[j].y += x[j].y;
-                a[j].z += x[j].z;
-                a[j].w += x[j].w;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (gcol + 4 * j < p.N) store_out4(p, grow, gcol + 4 * j, a[j]);
-    }
-}
-
 // Drop the consumed partial tiles of tile lt from L2 without write-back (scratch data).
 template <int BN>
 __device__ __forceinline__ void discard_tile(const MkParams &p, int lt, int tid, int nthreads) {
@@ -350,9 +313,115 @@ __device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int lt, uint32_
     return true;
 }
 
+// Reduce-role staging through the block's TMA ring, which is idle while the block reduces (the
+// producer reloads it only after the epilogue group has finished its last reduce item).
+struct Staging {
+    uint8_t *ring;          // 1024-byte aligned, ring_bytes long
+    uint32_t ring_bytes;
+    uint64_t *rfull;        // 3 mbarriers, one per chunk set in flight
+    uint32_t seq;           // chunk sets consumed so far by this block (phase bookkeeping)
+};
+
+// Eight fp32 values (columns gcol..gcol+7 of row grow) of the result, AllReduce or shard.
+__device__ __forceinline__ void store_out8(const MkParams &p, int grow, int gcol, float4 a, float4 b) {
+    void *base;
+    size_t idx;
+    int nout = 1;
+    if (p.op == MK_IOP_RS) {
+        const int sh = grow / p.rows_per_shard;
+        base = p.out[sh];
+        idx = static_cast<size_t>(grow - sh * p.rows_per_shard) * p.N + gcol;
+    } else {
+        base = p.out[0];
+        idx = static_cast<size_t>(grow) * p.N + gcol;
+        nout = p.num_out;
+    }
+    for (int d = 0; d < nout; ++d) {
+        void *o = d == 0 ? base : p.out[d];
+        if (p.out_bf16) {
+            st_u4(static_cast<uint16_t *>(o) + idx, pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                  pack_bf16x2(b.z, b.w));
+        } else {
+            st_f4(static_cast<float *>(o) + idx, a.x, a.y, a.z, a.w);
+            st_f4(static_cast<float *>(o) + idx + 4, b.x, b.y, b.z, b.w);
+        }
+    }
+}
+
+// Sum the P partial tiles of tile (tm, tn) in rank order r = 0..P-1.  The tiles are streamed in
+// chunks of CH bytes per rank (chunk c = column groups [c*CH/2048, ...) x 128 rows) by bulk copies
+// into the ring, up to three chunk sets (P x CH bytes each) in flight, so each SM keeps up to
+// 192 KiB of loads outstanding without holding them in registers.  Thread etid owns row
+// etid % 128 and two column groups (eight columns) of every 8 KiB chunk (one group of a 4 KiB
+// chunk when P > 8), read conflict-free from shared memory.
+template <int BN>
+__device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int tn, int etid, Staging &st) {
+    const int lt = tm * p.tiles_n + tn;
+    const uint32_t P = static_cast<uint32_t>(p.P);
+    const uint32_t CH = P <= 8 ? 8192u : 4096u;
+    const uint32_t set_bytes = CH * P;
+    const uint32_t NB = min(3u, st.ring_bytes / set_bytes);
+    constexpr uint32_t TILE_BYTES = MK_BM * BN * 4;
+    const uint32_t nch = TILE_BYTES / CH;
+    const char *src0 = reinterpret_cast<const char *>(partial_tile<BN>(p, 0, lt));
+    const size_t rank_stride = static_cast<size_t>(p.num_tiles) * TILE_BYTES;
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](uint32_t ch, uint32_t seq) {
+        const uint32_t b = seq % NB;
+        const uint32_t bar = smem_u32(&st.rfull[b]);
+        mbar_arrive_expect_tx(bar, set_bytes);
+        for (uint32_t r = 0; r < P; ++r)
+            bulk_load_evict_first(smem_u32(st.ring + b * set_bytes + r * CH), src0 + r * rank_stride + ch * CH, CH,
+                                  bar, pol);
+    };
+    if (etid == 0)
+        for (uint32_t k = 0; k < NB && k < nch; ++k) issue(k, st.seq + k);
+    const int row = etid & (MK_BM - 1);
+    const int half = etid >> 7;
+    const int grow = tm * MK_BM + row;
+    const uint32_t groups_per_chunk = CH / (MK_BM * 16);   // 4 (8 KiB) or 2 (4 KiB)
+    for (uint32_t ch = 0; ch < nch; ++ch) {
+        const uint32_t seq = st.seq + ch;
+        const uint32_t b = seq % NB;
+        wait_bar<false>(smem_u32(&st.rfull[b]), (seq / NB) & 1u, c, SITE_STAGE_FULL, ch);
+        const uint8_t *buf = st.ring + b * set_bytes;
+        if (groups_per_chunk == 4) {
+            const int g_local = 2 * half;   // this thread's two column groups in the chunk
+            const uint32_t off0 = (static_cast<uint32_t>(g_local) * MK_BM + row) * 16;
+            const uint32_t off1 = off0 + MK_BM * 16;
+            float4 a0 = *reinterpret_cast<const float4 *>(buf + off0);
+            float4 a1 = *reinterpret_cast<const float4 *>(buf + off1);
+            for (uint32_t r = 1; r < P; ++r) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(buf + r * CH + off0);
+                const float4 x1 = *reinterpret_cast<const float4 *>(buf + r * CH + off1);
+                a0.x += x0.x; a0.y += x0.y; a0.z += x0.z; a0.w += x0.w;
+                a1.x += x1.x; a1.y += x1.y; a1.z += x1.z; a1.w += x1.w;
+            }
+            const int gcol = tn * BN + static_cast<int>(ch * 4 + g_local) * 4;
+            if (grow < p.M && gcol < p.N) store_out8(p, grow, gcol, a0, a1);
+        } else {
+            const uint32_t off = (static_cast<uint32_t>(half) * MK_BM + row) * 16;
+            float4 a = *reinterpret_cast<const float4 *>(buf + off);
+            for (uint32_t r = 1; r < P; ++r) {
+                const float4 x = *reinterpret_cast<const float4 *>(buf + r * CH + off);
+                a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+            }
+            const int gcol = tn * BN + static_cast<int>(ch * 2 + half) * 4;
+            if (grow < p.M && gcol < p.N) store_out4(p, grow, gcol, a);
+        }
+        bar_sync(1, MK_EPI_THREADS);   // every thread is done with buffer b
+        if (etid == 0 && ch + NB < nch) {
+            fence_proxy_async_smem();
+            issue(ch + NB, seq + NB);
+        }
+    }
+    st.seq += nch;
+    if (etid == 0) fence_proxy_async_smem();   // the ring goes back to TMA loads after this item
+}
+
 // The reduce group (warps 2-9) handles one reduce item for tile (tm, tn).
 template <int BN>
-__device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int etid, uint32_t epoch) {
+__device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int etid, uint32_t epoch, Staging &st) {
     bool ok = true;
     const bool exists = tm < p.tiles_m;
     const int lt = tm * p.tiles_n + tn;
@@ -360,8 +429,7 @@ __device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int e
     ok = bar_and(1, MK_EPI_THREADS, ok);
     if (exists && ok) {
         const long long t0 = clock64();
-        reduce_tile_body<BN>(p, tm, tn, etid);
-        bar_sync(1, MK_EPI_THREADS);   // every read of the partials is done
+        reduce_tile_staged<BN>(p, c, tm, tn, etid, st);
         if (p.discard) discard_tile<BN>(p, lt, etid, MK_EPI_THREADS);
         if (etid == 0)
             atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->reduce_busy),
@@ -379,6 +447,8 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
     const int half = (warp - MK_EPI_WARP0) >> 2;      // which half of the tile's columns
     const int row = lq * 32 + lane;
     float *tile = partial_tile<BN>(p, r, lt);
+    // partial tiles should live in L2 until the reduce role has read them (then they are discarded)
+    const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
 #pragma unroll 1
     for (int cc = 0; cc < BN / 64; ++cc) {
         const int col0 = half * (BN / 2) + cc * 32;
@@ -392,8 +462,8 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             float *dst = tile + (static_cast<size_t>((col0 >> 2) + q) * MK_BM + row) * 4;
-            st_f4(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                  __uint_as_float(v[4 * q + 3]));
+            st_f4_hint(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                       __uint_as_float(v[4 * q + 3]), pol);
         }
     }
 }
@@ -411,8 +481,10 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
                                uint32_t done_per_unit, int role_units, int sms_per_role) {
     MkWsHeader *h = c.hdr;
     const int S = role_units * sms_per_role;
-    int cur = p.init_nr;
-    st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
+    // In static mode the warp only records the trace (the split is the caller's).
+    const bool adaptive = p.mode == MK_MODE_ADAPTIVE;
+    int cur = adaptive ? p.init_nr : p.static_nr;
+    if (adaptive) st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
     const uint64_t start = globaltimer();
     uint64_t last_change = start;
     uint32_t last_u = 0, last_d = 0;
@@ -442,7 +514,7 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
             break;
         }
         const uint32_t units = u / done_per_unit;
-        if (units > 0 && d > 0) {
+        if (adaptive && units > 0 && d > 0) {
             const double tau_c = sms_per_role * static_cast<double>(ld_relaxed_gpu64(&h->compute_busy)) / units;
             const double tau_r = static_cast<double>(ld_relaxed_gpu64(&h->reduce_busy)) / d;
             const double wc = static_cast<double>(num_units - min(units, num_units)) * tau_c;
@@ -498,13 +570,29 @@ __device__ void init_barriers(SmemCtl<STAGES> &s, const MkParams &p, uint32_t fu
         mbar_init(smem_u32(&s.wempty[i]), wempty_count);
     }
     mbar_init(smem_u32(&s.drain), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&s.rfull[i]), 1);
     fence_mbar_init();
     s.abort = 0;
     s.issued = 0;
     s.peer_issued = 0;
+    s.epi_done = 0;
     uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
     if (e == 0u) e = 1u;
     s.epoch = e;
+}
+
+// Producer side of the ring hand-over: a reduce item borrows the TMA ring for staging, so after
+// queueing one the producer issues no further loads until the epilogue group has finished it.
+__device__ bool wait_epilogue_done(const volatile uint32_t *epi_done, uint32_t count, const Ctx &c) {
+    if (*epi_done >= count) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1; i != 0u; ++i) {
+        if (*epi_done >= count) return true;
+        if ((i & 63u) == 0u && globaltimer() - t0 > c.pipe_timeout_ns) break;
+        __nanosleep(64);
+    }
+    raise_error(c, MK_ERR_TIMEOUT, SITE_STAGE_EMPTY, count);
+    return false;
 }
 
 // ======================================================================= one-SM tiles
@@ -519,11 +607,14 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
     // A rows are reused by every column of the raster group: keep them; B columns stream.
     const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
     const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
+    uint32_t pushed = 0, ring_free_at = 0;   // ring free once the epilogue has finished ring_free_at items
     while (!stop) {
         const int2 it = claim_work(p, c, g, exhausted);
         if (!wait_bar<false>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
         s.items[wq] = it;
         mbar_arrive(smem_u32(&s.wfull[wq]));
+        ++pushed;
+        if (it.x == ITEM_REDUCE) ring_free_at = pushed;
         if (++wq == WQ) {
             wq = 0;
             wphase ^= 1u;
@@ -533,6 +624,7 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
         const int u = it.y, t = u / p.P, r = u - t * p.P;
         int tm, tn;
         raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+        if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
         for (int kb = 0; kb < p.num_kb; ++kb) {
             if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
                 stop = true;
@@ -620,10 +712,11 @@ __device__ void run1_mma(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_
 }
 
 template <int BN>
-__device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base,
-                              uint32_t epoch) {
+__device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
+                              uint32_t tmem_base, uint32_t epoch) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int etid = threadIdx.x - MK_EPI_WARP0 * 32;
+    Staging st{stages, Cfg1<BN>::STAGES * Cfg1<BN>::STAGE_BYTES, s.rfull, 0};
     int acc = 0, wq = 0;
     uint32_t aphase = 0, wphase = 0;
     for (;;) {
@@ -665,8 +758,9 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, c
         } else {
             int tm, tn;
             raster(it.y, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
-            do_reduce<BN>(p, c, tm, tn, etid, epoch);
+            do_reduce<BN>(p, c, tm, tn, etid, epoch, st);
         }
+        if (etid == 0) *reinterpret_cast<volatile uint32_t *>(&s.epi_done) = s.epi_done + 1;
     }
 }
 
@@ -701,8 +795,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_persistent_kernel(const __gr
     } else if (warp == 1) {
         if (lane == 0) run1_mma<BN>(p, s, stages, c, tmem_base);
     } else if (warp < MK_CTRL_WARP) {
-        run1_epilogue<BN>(p, s, c, tmem_base, epoch);
-    } else if (lane == 0 && blockIdx.x == 0 && p.mode == MK_MODE_ADAPTIVE) {
+        run1_epilogue<BN>(p, s, stages, c, tmem_base, epoch);
+    } else if (lane == 0 && blockIdx.x == 0 &&
+               (p.mode == MK_MODE_ADAPTIVE || (p.mode == MK_MODE_STATIC && p.trace))) {
         run_controller(p, c, p.num_units, p.num_tiles, 1, gridDim.x, 1);
     }
     __syncwarp();
@@ -740,6 +835,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     bool exhausted = false, stop = false;
     const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
     const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
+    uint32_t pushed = 0, ring_free_at = 0;
     while (!stop) {
         int2 it;
         if (leader) {
@@ -758,12 +854,15 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             wq = 0;
             wphase ^= 1u;
         }
+        ++pushed;
+        if (it.x == ITEM_REDUCE) ring_free_at = pushed;
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
         const int u = it.y, pt = u / p.P, r = u - pt * p.P;
         int sm, tn;
         raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
         const int tm = 2 * sm + static_cast<int>(crank);
+        if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
         for (int kb = 0; kb < p.num_kb; ++kb) {
             if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
                 stop = true;
@@ -850,10 +949,11 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
 }
 
 template <int BN>
-__device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base,
-                              uint32_t epoch, uint32_t crank) {
+__device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
+                              uint32_t tmem_base, uint32_t epoch, uint32_t crank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int etid = threadIdx.x - MK_EPI_WARP0 * 32;
+    Staging st{stages, Cfg2<BN>::STAGES * Cfg2<BN>::STAGE_BYTES, s.rfull, 0};
     const bool leader = crank == 0;
     const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
     const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
@@ -906,8 +1006,9 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, c
         } else {
             int sm, tn;
             raster(it.y, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
-            do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, etid, epoch);
+            do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, etid, epoch, st);
         }
+        if (etid == 0) *reinterpret_cast<volatile uint32_t *>(&s.epi_done) = s.epi_done + 1;
     }
 }
 
@@ -961,8 +1062,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_pair_kernel(const __grid_con
     } else if (warp == 1) {
         if (lane == 0 && crank == 0) run2_mma<BN>(p, s, stages, c, tmem_base);
     } else if (warp < MK_CTRL_WARP) {
-        run2_epilogue<BN>(p, s, c, tmem_base, epoch, crank);
-    } else if (lane == 0 && blockIdx.x == 0 && p.mode == MK_MODE_ADAPTIVE) {
+        run2_epilogue<BN>(p, s, stages, c, tmem_base, epoch, crank);
+    } else if (lane == 0 && blockIdx.x == 0 &&
+               (p.mode == MK_MODE_ADAPTIVE || (p.mode == MK_MODE_STATIC && p.trace))) {
         run_controller(p, c, p.num_pair_units, 2 * p.num_pair_tiles, 2, gridDim.x >> 1, 2);
     }
     __syncwarp();
@@ -979,10 +1081,25 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_pair_kernel(const __grid_con
 // Second kernel of the unfused baseline: reduce every tile after the GEMM kernel finished
 // (stream order replaces the readiness flags).
 template <int BN>
-__global__ void __launch_bounds__(MK_EPI_THREADS) mk_reduce_kernel(const __grid_constant__ MkParams p) {
+__global__ void __launch_bounds__(MK_EPI_THREADS, 1) mk_reduce_kernel(const __grid_constant__ MkParams p) {
+    // The same staged reduction as the fused kernel's reduce role, one block per SM with a
+    // 192 KiB staging ring, so that the baseline differs from the fused kernel only in when the
+    // reduction runs.
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t rfull[3];
+    __shared__ int s_abort;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&rfull[i]), 1);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    __syncthreads();
+    const Ctx c{p.hdr, &s_abort, p.timeout_ns, 4 * p.timeout_ns};
+    Staging st{ring, MK_REDUCE_RING_BYTES, rfull, 0};
     for (int lt = blockIdx.x; lt < p.num_tiles; lt += gridDim.x) {
-        reduce_tile_body<BN>(p, lt / p.tiles_n, lt % p.tiles_n, threadIdx.x);
-        __syncthreads();
+        reduce_tile_staged<BN>(p, c, lt / p.tiles_n, lt % p.tiles_n, threadIdx.x, st);
         if (p.discard) discard_tile<BN>(p, lt, threadIdx.x, MK_EPI_THREADS);
     }
 }
@@ -1118,9 +1235,18 @@ cudaError_t mk_launch_persistent(const MkParams &p, int bn, bool pair, int num_c
 cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s) {
     const int grid = num_ctas < p.num_tiles ? num_ctas : p.num_tiles;
     if (grid <= 0) return cudaSuccess;
-    if (bn == 256)
-        mk::mk_reduce_kernel<256><<<grid, MK_EPI_THREADS, 0, s>>>(p);
-    else
-        mk::mk_reduce_kernel<128><<<grid, MK_EPI_THREADS, 0, s>>>(p);
+    const size_t smem = MK_REDUCE_RING_BYTES + 1024;
+    cudaError_t e;
+    if (bn == 256) {
+        e = cudaFuncSetAttribute(mk::mk_reduce_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        mk::mk_reduce_kernel<256><<<grid, MK_EPI_THREADS, smem, s>>>(p);
+    } else {
+        e = cudaFuncSetAttribute(mk::mk_reduce_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        mk::mk_reduce_kernel<128><<<grid, MK_EPI_THREADS, smem, s>>>(p);
+    }
     return cudaGetLastError();
 }

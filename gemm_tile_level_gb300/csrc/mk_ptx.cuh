@@ -87,6 +87,24 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
     return pol;
 }
 
+// Order this thread's generic-proxy shared-memory accesses before later async-proxy ones (bulk
+// copies, TMA) to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned addresses, size a
+// multiple of 16), completion counted in bytes on `bar`; the source lines are marked
+// evict-first in L2.
+__device__ __forceinline__ void bulk_load_evict_first(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -332,6 +350,13 @@ __device__ __forceinline__ float4 ld_cg_f4(const float4 *p) {
 
 __device__ __forceinline__ void st_f4(void *p, float a, float b, float c, float d) {
     asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// 16-byte store with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_f4_hint(void *p, float a, float b, float c, float d, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d), "l"(policy)
                  : "memory");
 }
 
