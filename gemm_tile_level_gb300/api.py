@@ -70,3 +70,24 @@ def gemm_reducescatter(A, B, out_dtype=mk.MK_BF16, shards=None, ws=None, opts=No
         ws = workspace(mk.MK_OP_REDUCESCATTER, P, M, N, Kr, A[0].device)
     st = mk.mk_gemm_reducescatter(P, M, N, Kr, A, B, shards, out_dtype, ws, opts=opts, stream=stream)
     return shards, st
+
+
+def allgather_gemm(A_shards, B, out_dtype=mk.MK_BF16, gather=True, C=None, gathered=None, ws=None, opts=None,
+                   stream=None):
+    """C[r] = [A_shards[0]; ...; A_shards[P-1]] @ B[r] via mk_allgather_gemm.  With gather=True the
+    shards are also copied into P gathered buffers (returned); otherwise they are read in place.
+    Returns (C, gathered, status)."""
+    P = len(A_shards)
+    Mp, K = A_shards[0].shape
+    M = Mp * P
+    N = B[0].shape[1]
+    dev = A_shards[0].device
+    if C is None:
+        C = [torch.empty((M, N), dtype=_TORCH_OUT[out_dtype], device=dev) for _ in range(P)]
+    if gather and gathered is None:
+        gathered = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    if ws is None:
+        ws = workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K, dev)
+    st = mk.mk_allgather_gemm(P, M, N, K, A_shards, B, gathered if gather else None, C, out_dtype, ws, opts=opts,
+                              stream=stream)
+    return C, gathered, st

@@ -247,6 +247,146 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     return MK_OK;
 }
 
+// AllGather + GEMM workspace: the header and one readiness flag per 128-row chunk of A (rounded
+// up to whole 256-row pair tiles).
+size_t ag_workspace_bytes(const Geometry &g) {
+    return MK_WS_HEADER_BYTES + align_up(static_cast<size_t>(2 * g.pair_tiles_m) * sizeof(uint32_t), MK_WS_ALIGN);
+}
+
+// First split of AllGather + GEMM (roles are fixed for the call): SMs for the copies in proportion
+// to their share of the work, with the same per-SM rates as the row-parallel heuristic.
+int initial_copy_pairs(int role_units, int P, int64_t M, int64_t N, int64_t K) {
+    const double copy = static_cast<double>(M) * K * 2.0 * (P + 1) / 120e9;
+    const double gemm = static_cast<double>(P) * 2.0 * M * N * K / 11e12;
+    int nr = static_cast<int>(role_units * copy / (copy + gemm) + 0.5);
+    if (nr < 1) nr = 1;
+    if (nr > role_units - 1) nr = role_units - 1;
+    return nr;
+}
+
+mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *const *A_shard, const void *const *B,
+                        void *const *A_gathered, void *const *C, mk_dtype out_dtype, void *ws, size_t ws_bytes,
+                        const mk_opts *opts_in, void *stream) {
+    g_last_error[0] = '\0';
+    if (P < 1 || P > MK_MAX_P) return fail(MK_ERR_INVALID_ARG, "P=%d outside [1, %d]", P, MK_MAX_P);
+    if (M < 0 || N < 0 || K < 0) return fail(MK_ERR_INVALID_ARG, "negative dimension");
+    if (out_dtype != MK_BF16 && out_dtype != MK_F32) return fail(MK_ERR_INVALID_ARG, "unknown out_dtype");
+    if (!A_shard || !B || !C || !ws) return fail(MK_ERR_INVALID_ARG, "null pointer array or workspace");
+    mk_opts o;
+    mk_opts_default(&o);
+    if (opts_in) o = *opts_in;
+    mk_status st = check_opts(&o);
+    if (st != MK_OK) return st;
+    if (N % 8 || K % 8)
+        return fail(MK_ERR_UNSUPPORTED_SHAPE, "N=%lld and K=%lld must be multiples of 8", (long long)N, (long long)K);
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "dimension above 2^31-1");
+    if (M % P) return fail(MK_ERR_UNSUPPORTED_SHAPE, "M=%lld not divisible by P=%d", (long long)M, P);
+    int n_gather = 0;
+    for (int r = 0; r < P && A_gathered; ++r) n_gather += A_gathered[r] != nullptr;
+    if (n_gather != 0 && n_gather != P)
+        return fail(MK_ERR_INVALID_ARG, "A_gathered must hold P buffers or none");
+    const bool gather = n_gather == P;
+    if (!gather && (M / P) % MK_BM)
+        return fail(MK_ERR_UNSUPPORTED_SHAPE, "without gathered buffers each shard (M/P=%lld rows) must be a "
+                    "multiple of %d rows", (long long)(M / P), MK_BM);
+    Geometry g;
+    make_geometry(P, M, N, K, &g);
+    if (g.num_pair_units > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "too many tiles");
+    if (M == 0 || N == 0) return MK_OK;
+    for (int r = 0; r < P; ++r) {
+        if (!C[r]) return fail(MK_ERR_INVALID_ARG, "C[%d] is null", r);
+        if (!aligned16(C[r])) return fail(MK_ERR_ALIGNMENT, "C[%d] not 16-byte aligned", r);
+        if (K > 0) {
+            if (!A_shard[r] || !B[r]) return fail(MK_ERR_INVALID_ARG, "A_shard[%d] or B[%d] is null", r, r);
+            if (!aligned16(A_shard[r]) || !aligned16(B[r]) || (gather && !aligned16(A_gathered[r])))
+                return fail(MK_ERR_ALIGNMENT, "operand of rank %d not 16-byte aligned", r);
+        }
+    }
+    if (reinterpret_cast<uintptr_t>(ws) % MK_WS_ALIGN) return fail(MK_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    const size_t need = ag_workspace_bytes(g);
+    if (ws_bytes < need) return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, need);
+
+    int resident = 0;
+    cudaError_t e = mk_max_persistent_ctas(g.bn, true, &resident);
+    if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
+    const int S = o.num_ctas > 0 ? o.num_ctas : resident;
+    if (S > resident)
+        return fail(MK_ERR_NOT_RESIDENT, "persistent grid of %d blocks cannot be co-resident (%d fit)", S, resident);
+    if (S & 1) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d must be even with SM-pair tiles", S);
+    if (S < 4) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d too small for two roles", S);
+    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > S - 2)
+        return fail(MK_ERR_INVALID_ARG, "comm_sms=%d leaves no compute SMs in a grid of %d", o.comm_sms, S);
+    const int role_units = S / 2;
+
+    MkParams p;
+    memset(&p, 0, sizeof p);
+    for (int r = 0; r < P && K > 0; ++r) {
+        st = gather ? encode_2d(&p.tmA[r], A_gathered[r], M, K, MK_BK, MK_BM)
+                    : encode_2d(&p.tmA[r], A_shard[r], M / P, K, MK_BK, MK_BM);
+        if (st != MK_OK) return st;
+        st = encode_2d(&p.tmB[r], B[r], K, N, 64, MK_BK);
+        if (st != MK_OK) return st;
+    }
+    for (int r = 0; r < P; ++r) {
+        p.out[r] = C[r];
+        p.ag_src[r] = A_shard[r];
+        p.ag_dst[r] = gather ? A_gathered[r] : nullptr;
+    }
+    p.num_out = P;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    p.hdr = reinterpret_cast<MkWsHeader *>(wsb);
+    p.flags = reinterpret_cast<uint32_t *>(wsb + MK_WS_HEADER_BYTES);
+    p.partials = nullptr;
+    p.trace = o.trace;
+    p.trace_cap = static_cast<uint32_t>(o.trace_bytes / sizeof(mk_trace_record));
+    p.skip_unit = o.debug_skip_unit;
+    p.timeout_ns = o.wait_timeout_ns ? o.wait_timeout_ns : kDefaultTimeoutNs;
+    p.P = P;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.Kr = static_cast<int32_t>(K);
+    p.tiles_m = static_cast<int32_t>(g.tiles_m);
+    p.tiles_n = static_cast<int32_t>(g.tiles_n);
+    p.num_tiles = static_cast<int32_t>(g.num_tiles);
+    p.num_units = static_cast<int32_t>(g.num_units);
+    p.num_kb = static_cast<int32_t>(g.num_kb);
+    p.pair_tiles_m = static_cast<int32_t>(g.pair_tiles_m);
+    p.num_pair_tiles = static_cast<int32_t>(g.num_pair_tiles);
+    p.num_pair_units = static_cast<int32_t>(g.num_pair_units);
+    p.op = MK_IOP_AG;
+    p.out_bf16 = out_dtype == MK_BF16;
+    p.rows_per_shard = static_cast<int32_t>(M / P);
+    int nr = o.comm_sms > 0 ? (o.comm_sms + 1) / 2 : initial_copy_pairs(role_units, P, M, N, K);
+    if (nr > role_units - 1) nr = role_units - 1;
+    p.static_nr = p.init_nr = nr < 1 ? 1 : nr;
+    p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(true, 1, K, g.pair_tiles_m);
+    p.discard = 0;
+    p.ctrl_period_ns = kCtrlPeriodNs;
+    p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
+    p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
+    p.ag_gather = gather;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!gather) {
+        p.mode = MK_MODE_COMPUTE_ONLY;   // nothing to move: the compute role reads the shards in place
+        e = mk_launch_persistent(p, g.bn, true, S, s);
+        return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the GEMM kernel");
+    }
+    if (o.split_mode == MK_SPLIT_UNFUSED) {
+        p.mode = MK_MODE_COMM_ONLY;      // baseline: gather every chunk, then one GEMM kernel
+        e = mk_launch_persistent(p, g.bn, true, S, s);
+        if (e != cudaSuccess) return fail_cuda(e, "launch of the gather kernel");
+        p.mode = MK_MODE_COMPUTE_ONLY;
+        p.ag_wait = 0;                   // stream order replaces the chunk flags
+        e = mk_launch_persistent(p, g.bn, true, S, s);
+        return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the GEMM kernel");
+    }
+    // Roles stay fixed for the call (see the claim rules); adaptive mode uses the shape's split.
+    p.mode = MK_MODE_STATIC;
+    p.ag_wait = 1;
+    e = mk_launch_persistent(p, g.bn, true, S, s);
+    return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the fused kernel");
+}
+
 }  // namespace
 
 void mk_internal_set_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
@@ -276,10 +416,9 @@ void mk_opts_default(mk_opts *o) {
 
 size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank) {
     Geometry g;
-    if (op == MK_OP_ALLREDUCE || op == MK_OP_REDUCESCATTER) {
-        if (!make_geometry(P, M, N, K_per_rank, &g)) return 0;
-        return g.total;
-    }
+    if (!make_geometry(P, M, N, K_per_rank, &g)) return 0;
+    if (op == MK_OP_ALLREDUCE || op == MK_OP_REDUCESCATTER) return g.total;
+    if (op == MK_OP_ALLGATHER_GEMM) return ag_workspace_bytes(g);
     return 0;
 }
 
@@ -299,9 +438,7 @@ mk_status mk_gemm_reducescatter(int P, int64_t M, int64_t N, int64_t K_per_rank,
 mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *const *A_shard,
                             const void *const *B, void *const *A_gathered, void *const *C, mk_dtype out_dtype,
                             void *ws, size_t ws_bytes, const mk_opts *opts, void *cuda_stream) {
-    (void)P; (void)M; (void)N; (void)K; (void)A_shard; (void)B; (void)A_gathered; (void)C; (void)out_dtype;
-    (void)ws; (void)ws_bytes; (void)opts; (void)cuda_stream;
-    return fail(MK_ERR_UNSUPPORTED_SHAPE, "mk_allgather_gemm: not available in this build");
+    return run_allgather(P, M, N, K, A_shard, B, A_gathered, C, out_dtype, ws, ws_bytes, opts, cuda_stream);
 }
 
 mk_status mk_status_check(void *ws, void *cuda_stream) {

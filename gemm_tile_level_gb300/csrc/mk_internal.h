@@ -27,10 +27,11 @@
 enum MkMode {
     MK_MODE_ADAPTIVE = 0,   // fused, controller publishes the split
     MK_MODE_STATIC = 1,     // fused, fixed split
-    MK_MODE_COMPUTE_ONLY = 2 // unfused baseline, first kernel
+    MK_MODE_COMPUTE_ONLY = 2, // unfused baseline: the GEMM kernel
+    MK_MODE_COMM_ONLY = 3     // unfused AllGather baseline: the copy kernel
 };
 
-enum MkOpInternal { MK_IOP_AR = 0, MK_IOP_RS = 1 };
+enum MkOpInternal { MK_IOP_AR = 0, MK_IOP_RS = 1, MK_IOP_AG = 2 };
 
 // Lives at the start of the workspace; zero-initialised once by the caller.
 struct MkWsHeader {
@@ -72,6 +73,11 @@ struct MkParams {
     int32_t discard;
     int32_t l2_hints;            // TMA loads: A rows evict_last, B columns evict_first
     int32_t cooperative;         // launch attribute (host side only)
+    // AllGather + GEMM: A_shard[s] ((M/P) x K) copied in 128-row chunks into every A_gathered[r]
+    // (M x K); the compute role waits on the chunk flags (ag_wait) before loading A rows.
+    const void *ag_src[MK_MAX_P];
+    void *ag_dst[MK_MAX_P];
+    int32_t ag_gather, ag_wait;
     int32_t ctrl_period_ns;
 };
 

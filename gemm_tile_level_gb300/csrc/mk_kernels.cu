@@ -84,7 +84,7 @@ struct SmemCtl {
     uint64_t wfull[WQ];
     uint64_t wempty[WQ];
     uint64_t drain;
-    uint64_t rfull[3];      // reduce staging: one per chunk set in flight
+    uint64_t rfull[4];      // reduce / copy staging: one per chunk in flight
     int2 items[WQ];
     uint32_t tmem_base;
     uint32_t epoch;
@@ -204,6 +204,21 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
     for (uint32_t spin = 0; spin != 0xFFFFFFFFu; ++spin) {
         if (global_abort(c)) return make_int2(ITEM_END, 0);
         if (p.mode == MK_MODE_COMPUTE_ONLY) {
+            const uint32_t u = atomicAdd(&h->compute_next, 1u);
+            if (u >= g.num_units) return make_int2(ITEM_END, 0);
+            if (static_cast<int64_t>(u) == p.skip_unit) continue;
+            return make_int2(ITEM_COMPUTE, static_cast<int>(u));
+        }
+        if (p.op == MK_IOP_AG) {
+            // AllGather + GEMM, roles fixed for the call: communication units claim chunk copies
+            // (which depend on nothing) and, once every copy is claimed, help compute; compute
+            // units never claim copies.  A compute item then waits only on copies queued ahead of
+            // every compute item of their block, so the wait-for relation has no cycle.
+            if (p.mode == MK_MODE_COMM_ONLY || static_cast<int>(g.role_index) >= static_cast<int>(g.role_units) - p.static_nr) {
+                const uint32_t i = atomicAdd(&h->reduce_next, 1u);
+                if (i < g.num_items) return make_int2(ITEM_REDUCE, static_cast<int>(i));
+                if (p.mode == MK_MODE_COMM_ONLY) return make_int2(ITEM_END, 0);
+            }
             const uint32_t u = atomicAdd(&h->compute_next, 1u);
             if (u >= g.num_units) return make_int2(ITEM_END, 0);
             if (static_cast<int64_t>(u) == p.skip_unit) continue;
@@ -570,7 +585,7 @@ __device__ void init_barriers(SmemCtl<STAGES> &s, const MkParams &p, uint32_t fu
         mbar_init(smem_u32(&s.wempty[i]), wempty_count);
     }
     mbar_init(smem_u32(&s.drain), 1);
-    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&s.rfull[i]), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&s.rfull[i]), 1);
     fence_mbar_init();
     s.abort = 0;
     s.issued = 0;
@@ -579,6 +594,136 @@ __device__ void init_barriers(SmemCtl<STAGES> &s, const MkParams &p, uint32_t fu
     uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
     if (e == 0u) e = 1u;
     s.epoch = e;
+}
+
+// ----------------------------------------------------------------- AllGather + GEMM helpers
+// Producer thread: acquire the flag of 128-row chunk `chunk` of the gathered A (bounded), then
+// order the acquire before the TMA (async-proxy) reads of that chunk.
+__device__ bool wait_chunk_ready(const MkParams &p, const Ctx &c, int chunk, uint32_t epoch) {
+    const uint32_t *f = p.flags + chunk;
+    uint64_t t0 = 0;
+    for (uint32_t polls = 0; ld_acquire_gpu(f) != epoch; ++polls) {
+        if (t0 == 0) t0 = globaltimer();
+        if ((polls & 15u) == 15u) {
+            if (global_abort(c)) return false;
+            if (globaltimer() - t0 > c.timeout_ns || polls > (1u << 30)) {
+                raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, static_cast<uint32_t>(chunk));
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+    fence_proxy_async_global();
+    return true;
+}
+
+// Epilogue group: TMEM accumulator (128 rows x BN fp32) -> rows tm*128.., columns tn*BN.. of the
+// row-major M x N output C_r, in eight-column pieces (N is a multiple of 8).
+template <int BN>
+__device__ __forceinline__ void store_output_tile(const MkParams &p, uint32_t tmem_acc, int r, int tm, int tn,
+                                                  int warp, int lane) {
+    const int lq = warp & 3;
+    const int half = (warp - MK_EPI_WARP0) >> 2;
+    const int row = lq * 32 + lane;
+    const int grow = tm * MK_BM + row;
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 64; ++cc) {
+        const int col0 = half * (BN / 2) + cc * 32;
+        uint32_t v[32];
+        if (p.num_kb > 0) {
+            tmem_ld32(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0), v);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0u;
+        }
+        if (grow >= p.M) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int gcol = tn * BN + col0 + 8 * q;
+            if (gcol >= p.N) break;
+            const size_t idx = static_cast<size_t>(grow) * p.N + gcol;
+            const float *f = reinterpret_cast<const float *>(&v[8 * q]);
+            if (p.out_bf16)
+                st_u4(static_cast<uint16_t *>(p.out[r]) + idx, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+            else {
+                st_f4(static_cast<float *>(p.out[r]) + idx, f[0], f[1], f[2], f[3]);
+                st_f4(static_cast<float *>(p.out[r]) + idx + 4, f[4], f[5], f[6], f[7]);
+            }
+        }
+    }
+}
+
+// Communication item of AllGather + GEMM: copy rows [chunk*128, chunk*128+128) of the
+// concatenated shards into every rank's gathered buffer, then release the chunk flag.  One
+// thread drives bulk copies through the block's TMA ring: global -> shared in pieces of up to
+// 48 KiB (two pieces ahead), shared -> global to the P destinations as bulk groups.  The
+// chunk's rows are contiguous in the gathered buffers and, within one shard, in the source.
+__device__ void do_copy_chunk(const MkParams &p, const Ctx &c, int chunk, int etid, uint32_t epoch, Staging &st) {
+    if (etid == 0 && chunk < p.tiles_m) {
+        constexpr uint32_t PIECE = 48u * 1024u;
+        const size_t row_bytes = static_cast<size_t>(p.Kr) * 2;
+        const int row_begin = chunk * MK_BM;
+        const int row_end = min(p.M, row_begin + MK_BM);
+        // pieces: walk shard segments, each cut into PIECE-sized slices
+        struct Piece { const char *src; size_t dst_off; uint32_t bytes; };
+        auto piece_at = [&](uint32_t k, Piece &pc) -> bool {
+            uint32_t seen = 0;
+            for (int row = row_begin; row < row_end;) {
+                const int sh = row / p.rows_per_shard;
+                const int seg_end = min(row_end, (sh + 1) * p.rows_per_shard);
+                const size_t seg_bytes = static_cast<size_t>(seg_end - row) * row_bytes;
+                const uint32_t np = static_cast<uint32_t>((seg_bytes + PIECE - 1) / PIECE);
+                if (k < seen + np) {
+                    const size_t off = static_cast<size_t>(k - seen) * PIECE;
+                    pc.src = static_cast<const char *>(p.ag_src[sh]) +
+                             static_cast<size_t>(row - sh * p.rows_per_shard) * row_bytes + off;
+                    pc.dst_off = static_cast<size_t>(row) * row_bytes + off;
+                    pc.bytes = static_cast<uint32_t>(seg_bytes - off < PIECE ? seg_bytes - off : PIECE);
+                    return true;
+                }
+                seen += np;
+                row = seg_end;
+            }
+            return false;
+        };
+        auto load = [&](uint32_t k, const Piece &pc) {
+            const uint32_t b = (st.seq + k) & 3u;
+            const uint32_t bar = smem_u32(&st.rfull[b]);
+            mbar_arrive_expect_tx(bar, pc.bytes);
+            bulk_load(smem_u32(st.ring + b * PIECE), pc.src, pc.bytes, bar);
+        };
+        Piece pc[2];
+        uint32_t k = 0;
+        bool have0 = piece_at(0, pc[0]);
+        bool have1 = have0 && piece_at(1, pc[1]);
+        if (have0) load(0, pc[0]);
+        if (have1) load(1, pc[1]);
+        while (have0) {
+            const uint32_t b = (st.seq + k) & 3u;
+            wait_bar<false>(smem_u32(&st.rfull[b]), ((st.seq + k) >> 2) & 1u, c, SITE_STAGE_FULL, k);
+            for (int r = 0; r < p.P; ++r)
+                bulk_store(static_cast<char *>(p.ag_dst[r]) + pc[0].dst_off, smem_u32(st.ring + b * PIECE), pc[0].bytes);
+            bulk_commit();
+            Piece next2;
+            const bool have2 = have1 && piece_at(k + 2, next2);
+            if (have2) {
+                bulk_wait_read<2>();   // piece k - 2, the last user of buffer (k + 2) & 3, has been read
+                load(k + 2, next2);
+            }
+            pc[0] = pc[1];
+            pc[1] = next2;
+            have0 = have1;
+            have1 = have2;
+            ++k;
+        }
+        bulk_wait_all();
+        fence_proxy_async_global();
+        st_release_gpu(p.flags + chunk, epoch);
+        st.seq += k;
+    }
+    bar_sync(1, MK_EPI_THREADS);
+    if (etid == 0) atomicAdd(&c.hdr->tiles_done, 1u);
 }
 
 // Producer side of the ring hand-over: a reduce item borrows the TMA ring for staging, so after
@@ -824,8 +969,9 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                               uint32_t crank) {
     using T = Cfg2<BN>;
     const bool leader = crank == 0;
-    const ClaimGeom g{static_cast<uint32_t>(p.num_pair_units), static_cast<uint32_t>(p.num_pair_tiles),
-                      blockIdx.x >> 1, gridDim.x >> 1, 2u};
+    const ClaimGeom g{static_cast<uint32_t>(p.num_pair_units),
+                      static_cast<uint32_t>(p.op == MK_IOP_AG ? p.pair_tiles_m : p.num_pair_tiles), blockIdx.x >> 1,
+                      gridDim.x >> 1, 2u};
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
     const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
     const uint32_t peer_items = mapa_shared(smem_u32(&s.items[0]), 1);
@@ -863,6 +1009,18 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
         const int tm = 2 * sm + static_cast<int>(crank);
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
+        const CUtensorMap *amap = &p.tmA[r];
+        int ay = tm * MK_BM;
+        if (p.op == MK_IOP_AG) {
+            if (p.ag_gather) {
+                // a failed wait has raised the abort: the loads still go ahead so the pipeline drains
+                if (p.ag_wait && tm < p.tiles_m) (void)wait_chunk_ready(p, c, tm, s.epoch);
+            } else {
+                const int sh = min(p.P - 1, tm * MK_BM / p.rows_per_shard);   // rows_per_shard % 128 == 0
+                amap = &p.tmA[sh];
+                ay = tm * MK_BM - sh * p.rows_per_shard;
+            }
+        }
         for (int kb = 0; kb < p.num_kb; ++kb) {
             if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
                 stop = true;
@@ -872,7 +1030,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
             const uint32_t sb = sa + T::A_BYTES;
             mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
-            tma_load_2d_pair_hint(sa, &p.tmA[r], fb, kb * MK_BK, tm * MK_BM, pol_a);
+            tma_load_2d_pair_hint(sa, amap, fb, kb * MK_BK, ay, pol_a);
 #pragma unroll
             for (int j = 0; j < T::B_BOXES; ++j)
                 tma_load_2d_pair_hint(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
@@ -987,7 +1145,12 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             if (!bar_and(1, MK_EPI_THREADS, ok)) break;
             tc_fence_after();
-            if (exists) store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
+            if (exists) {
+                if (p.op == MK_IOP_AG)
+                    store_output_tile<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, tm, tn, warp, lane);
+                else
+                    store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -1000,13 +1163,16 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             }
             bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
             if (etid == 0) {
-                if (exists) st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
+                if (exists && p.op != MK_IOP_AG) st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
                 atomicAdd(&c.hdr->units_done, 1u);
             }
         } else {
             int sm, tn;
             raster(it.y, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
-            do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, etid, epoch, st);
+            if (p.op == MK_IOP_AG)
+                do_copy_chunk(p, c, 2 * it.y + static_cast<int>(crank), etid, epoch, st);
+            else
+                do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, etid, epoch, st);
         }
         if (etid == 0) *reinterpret_cast<volatile uint32_t *>(&s.epi_done) = s.epi_done + 1;
     }
@@ -1065,7 +1231,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_pair_kernel(const __grid_con
         run2_epilogue<BN>(p, s, stages, c, tmem_base, epoch, crank);
     } else if (lane == 0 && blockIdx.x == 0 &&
                (p.mode == MK_MODE_ADAPTIVE || (p.mode == MK_MODE_STATIC && p.trace))) {
-        run_controller(p, c, p.num_pair_units, 2 * p.num_pair_tiles, 2, gridDim.x >> 1, 2);
+        run_controller(p, c, p.num_pair_units, 2 * (p.op == MK_IOP_AG ? p.pair_tiles_m : p.num_pair_tiles), 2,
+                       gridDim.x >> 1, 2);
     }
     __syncwarp();
     if (threadIdx.x == 0 && crank == 1) st_cluster_u32(mapa_shared(smem_u32(&s.peer_issued), 0), s.issued);

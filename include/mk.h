@@ -176,12 +176,17 @@ mk_status mk_gemm_reducescatter(int P, int64_t M, int64_t N, int64_t K_per_rank,
  * row shards of the activations gathered in 128-row chunks.)
  *   A_shard[s]    : (M/P) x K bf16, rank s's row shard; M divisible by P
  *   B[r]          : K x N bf16, rank r's column shard of the weights
- *   A_gathered[r] : M x K bf16 buffer receiving the gathered activations on
- *                   rank r, or NULL entries (then the compute role reads the
- *                   shards in place and only waits on nothing)
+ *   A_gathered[r] : M x K bf16 buffer that receives the gathered activations
+ *                   on rank r (all P given), or NULL / all entries NULL: then
+ *                   nothing is moved and the compute role reads the shards in
+ *                   place (requires M/P to be a multiple of 128)
  *   C[r]          : M x N, out_dtype
- * Communication-role blocks copy 128-row chunks and release a readiness flag
- * per chunk; compute-role blocks acquire the flags of the rows they need.
+ * Communication-role blocks copy 128-row chunks into every gathered buffer
+ * and release one readiness flag per chunk; compute-role blocks acquire the
+ * flag of the rows they load.  The split of SMs between the roles is fixed
+ * for the call (comm_sms, or derived from the shape in adaptive mode);
+ * MK_SPLIT_UNFUSED gathers in one kernel and multiplies in a second.
+ * Workspace: mk_workspace_size(MK_OP_ALLGATHER_GEMM, P, M, N, K).
  */
 mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *const *A_shard,
                             const void *const *B, void *const *A_gathered, void *const *C,

@@ -82,6 +82,8 @@ def test_workspace_size_arithmetic(mk):
     assert mk.mk_workspace_size(0, 3, 130, 264, 8) == 256 + 256 + 3 * tiles * 128 * 256 * 4
     assert mk.mk_workspace_size(mk.MK_OP_REDUCESCATTER, 8, 16384, 8192, 1024) == \
         mk.mk_workspace_size(mk.MK_OP_ALLREDUCE, 8, 16384, 8192, 1024)
+    # AllGather + GEMM: header + one flag per 128-row chunk (rounded up to pair tiles)
+    assert mk.mk_workspace_size(mk.MK_OP_ALLGATHER_GEMM, 4, 512, 128, 64) == 256 + 256
     assert mk.mk_workspace_size(0, 0, 128, 128, 64) == 0
     assert mk.mk_workspace_size(0, 17, 128, 128, 64) == 0
     assert mk.mk_workspace_size(0, 2, -1, 128, 64) == 0
