@@ -39,6 +39,19 @@ int auto_raster_group(bool pair, int P, int64_t Kr, int64_t row_tiles) {
 }
 constexpr int kCtrlPeriodNs = 1000;
 
+// Column slices per output tile's reduction: by default the smallest power of two (at most 8)
+// that gives every communication-capable role unit two reduce items; never more slices than the
+// staged reducer has chunks in a tile (CH = 8 KiB per rank for P <= 8, else 4 KiB).
+int choose_reduce_split(int requested, int64_t items, int role_units, int bn, int P) {
+    const int nch = MK_BM * bn * 4 / (P <= 8 ? 8192 : 4096);
+    int s = requested;
+    if (s <= 0) {
+        s = 1;
+        while (s < 8 && items * s < 2LL * role_units) s *= 2;
+    }
+    return s < nch ? s : nch;
+}
+
 int choose_bn(int64_t N) { return N > 128 ? 256 : 128; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -118,6 +131,8 @@ mk_status check_opts(const mk_opts *o) {
     if (o->comm_sms < 0) return fail(MK_ERR_INVALID_ARG, "comm_sms < 0");
     if (o->num_ctas < 0) return fail(MK_ERR_INVALID_ARG, "num_ctas < 0");
     if (o->raster_group < 0) return fail(MK_ERR_INVALID_ARG, "raster_group < 0");
+    if (o->reduce_split < 0 || o->reduce_split > 64)
+        return fail(MK_ERR_INVALID_ARG, "reduce_split %d outside [0, 64]", o->reduce_split);
     if (o->trace_bytes && !o->trace) return fail(MK_ERR_INVALID_ARG, "trace_bytes without trace buffer");
     if (o->trace && !aligned16(o->trace)) return fail(MK_ERR_ALIGNMENT, "trace buffer not 16-byte aligned");
     return MK_OK;
@@ -231,10 +246,12 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
     p.ctrl_period_ns = kCtrlPeriodNs;
+    p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (o.split_mode == MK_SPLIT_UNFUSED) {
         p.mode = MK_MODE_COMPUTE_ONLY;
+        p.red_split = choose_reduce_split(o.reduce_split, g.num_tiles, S, g.bn, P);
         e = mk_launch_persistent(p, g.bn, pair, S, s);
         if (e != cudaSuccess) return fail_cuda(e, "launch of the per-rank GEMM kernel");
         e = mk_launch_reduce(p, g.bn, S, s);
@@ -362,6 +379,7 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(true, 1, K, g.pair_tiles_m);
     p.discard = 0;
     p.ctrl_period_ns = kCtrlPeriodNs;
+    p.red_split = 1;
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.ag_gather = gather;
@@ -411,7 +429,7 @@ void mk_opts_default(mk_opts *o) {
     o->flags = 0;
     o->debug_skip_unit = -1;
     o->raster_group = 0;
-    o->reserved = 0;
+    o->reduce_split = 0;
 }
 
 size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank) {

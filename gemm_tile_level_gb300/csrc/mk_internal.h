@@ -79,6 +79,7 @@ struct MkParams {
     void *ag_dst[MK_MAX_P];
     int32_t ag_gather, ag_wait;
     int32_t ctrl_period_ns;
+    int32_t red_split;           // reduce items per output tile (column slices), >= 1
 };
 
 // Implemented in mk_abi.cu: set the host thread's mk_last_error() text; bytes of the readiness

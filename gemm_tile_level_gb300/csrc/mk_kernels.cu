@@ -177,10 +177,11 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, i
 // SM pair whose two CTAs each count their half).
 struct ClaimGeom {
     uint32_t num_units;   // compute units (tile, rank)
-    uint32_t num_items;   // reduce items (tiles, or tile pairs)
+    uint32_t num_items;   // reduce items (tiles, or tile pairs, times split)
     uint32_t role_index;  // this role unit
     uint32_t role_units;  // role units in the grid
     uint32_t done_per_unit;
+    uint32_t split;       // reduce items per tile (column slices of its reduction)
 };
 
 __device__ bool wait_claimed(const Ctx &c, uint32_t need) {
@@ -242,8 +243,8 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
                 if (next >= g.num_items) return make_int2(ITEM_END, 0);
                 const uint32_t done = ld_relaxed_gpu(&h->units_done);
                 const uint32_t issued = ld_relaxed_gpu(&h->compute_next);
-                const uint64_t per_item = static_cast<uint64_t>(P) * g.done_per_unit;
-                if (issued < g.num_units && (static_cast<uint64_t>(next) + 1) * per_item > done + per_item) {
+                const uint64_t per_tile = static_cast<uint64_t>(P) * g.done_per_unit;
+                if (issued < g.num_units && (static_cast<uint64_t>(next / g.split) + 1) * per_tile > done + per_tile) {
                     // nothing ready yet: wait for compute progress (bounded), then re-read the role
                     if (done != gate_seen) {
                         gate_seen = done;
@@ -259,7 +260,7 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
         }
         const uint32_t i = atomicAdd(&h->reduce_next, 1u);
         if (i >= g.num_items) return make_int2(ITEM_END, 0);
-        const uint64_t need64 = (static_cast<uint64_t>(i) + 1) * P;
+        const uint64_t need64 = (static_cast<uint64_t>(i / g.split) + 1) * P;
         const uint32_t need = need64 < g.num_units ? static_cast<uint32_t>(need64) : g.num_units;
         if (!wait_claimed(c, need)) return make_int2(ITEM_END, 0);
         return make_int2(ITEM_REDUCE, static_cast<int>(i));
@@ -296,13 +297,27 @@ __device__ __forceinline__ float *partial_tile(const MkParams &p, int r, int lt)
     return p.partials + (static_cast<size_t>(r) * p.num_tiles + lt) * (MK_BM * BN);
 }
 
-// Drop the consumed partial tiles of tile lt from L2 without write-back (scratch data).
+// Byte range [*b0, *b1) of a partial tile that reduce slice `sub` of `nsub` covers: whole chunks
+// of the staged reduction (CH bytes per rank, see reduce_tile_staged).
 template <int BN>
-__device__ __forceinline__ void discard_tile(const MkParams &p, int lt, int tid, int nthreads) {
-    constexpr int LINES = MK_BM * BN * 4 / 128;
+__device__ __forceinline__ void slice_chunks(const MkParams &p, int sub, int nsub, uint32_t &c0, uint32_t &c1,
+                                             uint32_t &ch_bytes) {
+    ch_bytes = p.P <= 8 ? 8192u : 4096u;
+    const uint32_t nch = MK_BM * BN * 4 / ch_bytes;
+    c0 = static_cast<uint32_t>(sub) * nch / static_cast<uint32_t>(nsub);
+    c1 = static_cast<uint32_t>(sub + 1) * nch / static_cast<uint32_t>(nsub);
+}
+
+// Drop the consumed part (slice sub of nsub) of the partial tiles of tile lt from L2 without
+// write-back (scratch data).
+template <int BN>
+__device__ __forceinline__ void discard_tile(const MkParams &p, int lt, int sub, int nsub, int tid, int nthreads) {
+    uint32_t c0, c1, chb;
+    slice_chunks<BN>(p, sub, nsub, c0, c1, chb);
+    const int l0 = static_cast<int>(c0 * chb / 128), l1 = static_cast<int>(c1 * chb / 128);
     for (int r = 0; r < p.P; ++r) {
         const char *base = reinterpret_cast<const char *>(partial_tile<BN>(p, r, lt));
-        for (int l = tid; l < LINES; l += nthreads) discard_l2_line(base + static_cast<size_t>(l) * 128);
+        for (int l = l0 + tid; l < l1; l += nthreads) discard_l2_line(base + static_cast<size_t>(l) * 128);
     }
 }
 
@@ -363,22 +378,25 @@ __device__ __forceinline__ void store_out8(const MkParams &p, int grow, int gcol
     }
 }
 
-// Sum the P partial tiles of tile (tm, tn) in rank order r = 0..P-1.  The tiles are streamed in
-// chunks of CH bytes per rank (chunk c = column groups [c*CH/2048, ...) x 128 rows) by bulk copies
-// into the ring, up to three chunk sets (P x CH bytes each) in flight, so each SM keeps up to
-// 192 KiB of loads outstanding without holding them in registers.  Thread etid owns row
-// etid % 128 and two column groups (eight columns) of every 8 KiB chunk (one group of a 4 KiB
-// chunk when P > 8), read conflict-free from shared memory.
+// Sum the P partial tiles of tile (tm, tn) in rank order r = 0..P-1, over column slice `sub` of
+// `nsub` (a reduce item covers one slice, so that a few large tiles still spread over many SMs).
+// The tiles are streamed in chunks of CH bytes per rank (chunk c = column groups
+// [c*CH/2048, ...) x 128 rows) by bulk copies into the ring, up to three chunk sets (P x CH bytes
+// each) in flight, so each SM keeps up to 192 KiB of loads outstanding without holding them in
+// registers.  Thread etid owns row etid % 128 and two column groups (eight columns) of every
+// 8 KiB chunk (one group of a 4 KiB chunk when P > 8), read conflict-free from shared memory.
 template <int BN>
-__device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int tn, int etid, Staging &st) {
+__device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int tn, int sub, int nsub, int etid,
+                                   Staging &st) {
     const int lt = tm * p.tiles_n + tn;
     const uint32_t P = static_cast<uint32_t>(p.P);
-    const uint32_t CH = P <= 8 ? 8192u : 4096u;
+    uint32_t c0, c1, CH;
+    slice_chunks<BN>(p, sub, nsub, c0, c1, CH);
     const uint32_t set_bytes = CH * P;
     const uint32_t NB = min(3u, st.ring_bytes / set_bytes);
     constexpr uint32_t TILE_BYTES = MK_BM * BN * 4;
-    const uint32_t nch = TILE_BYTES / CH;
-    const char *src0 = reinterpret_cast<const char *>(partial_tile<BN>(p, 0, lt));
+    const uint32_t nch = c1 - c0;   // chunks of this slice
+    const char *src0 = reinterpret_cast<const char *>(partial_tile<BN>(p, 0, lt)) + static_cast<size_t>(c0) * CH;
     const size_t rank_stride = static_cast<size_t>(p.num_tiles) * TILE_BYTES;
     const uint64_t pol = policy_evict_first();
     auto issue = [&](uint32_t ch, uint32_t seq) {
@@ -412,7 +430,7 @@ __device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int 
                 a0.x += x0.x; a0.y += x0.y; a0.z += x0.z; a0.w += x0.w;
                 a1.x += x1.x; a1.y += x1.y; a1.z += x1.z; a1.w += x1.w;
             }
-            const int gcol = tn * BN + static_cast<int>(ch * 4 + g_local) * 4;
+            const int gcol = tn * BN + static_cast<int>((c0 + ch) * 4 + g_local) * 4;
             if (grow < p.M && gcol < p.N) store_out8(p, grow, gcol, a0, a1);
         } else {
             const uint32_t off = (static_cast<uint32_t>(half) * MK_BM + row) * 16;
@@ -421,7 +439,7 @@ __device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int 
                 const float4 x = *reinterpret_cast<const float4 *>(buf + r * CH + off);
                 a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
             }
-            const int gcol = tn * BN + static_cast<int>(ch * 2 + half) * 4;
+            const int gcol = tn * BN + static_cast<int>((c0 + ch) * 2 + half) * 4;
             if (grow < p.M && gcol < p.N) store_out4(p, grow, gcol, a);
         }
         bar_sync(1, MK_EPI_THREADS);   // every thread is done with buffer b
@@ -434,9 +452,10 @@ __device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int 
     if (etid == 0) fence_proxy_async_smem();   // the ring goes back to TMA loads after this item
 }
 
-// The reduce group (warps 2-9) handles one reduce item for tile (tm, tn).
+// The reduce group (warps 2-9) handles one reduce item: slice sub of nsub of tile (tm, tn).
 template <int BN>
-__device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int etid, uint32_t epoch, Staging &st) {
+__device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int sub, int nsub, int etid,
+                          uint32_t epoch, Staging &st) {
     bool ok = true;
     const bool exists = tm < p.tiles_m;
     const int lt = tm * p.tiles_n + tn;
@@ -444,8 +463,8 @@ __device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int e
     ok = bar_and(1, MK_EPI_THREADS, ok);
     if (exists && ok) {
         const long long t0 = clock64();
-        reduce_tile_staged<BN>(p, c, tm, tn, etid, st);
-        if (p.discard) discard_tile<BN>(p, lt, etid, MK_EPI_THREADS);
+        reduce_tile_staged<BN>(p, c, tm, tn, sub, nsub, etid, st);
+        if (p.discard) discard_tile<BN>(p, lt, sub, nsub, etid, MK_EPI_THREADS);
         if (etid == 0)
             atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->reduce_busy),
                       static_cast<unsigned long long>(clock64() - t0));
@@ -744,8 +763,8 @@ __device__ bool wait_epilogue_done(const volatile uint32_t *epi_done, uint32_t c
 template <int BN>
 __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_t *stages, const Ctx &c) {
     using T = Cfg1<BN>;
-    const ClaimGeom g{static_cast<uint32_t>(p.num_units), static_cast<uint32_t>(p.num_tiles), blockIdx.x,
-                      gridDim.x, 1u};
+    const ClaimGeom g{static_cast<uint32_t>(p.num_units), static_cast<uint32_t>(p.num_tiles * p.red_split),
+                      blockIdx.x, gridDim.x, 1u, static_cast<uint32_t>(p.red_split)};
     int stage = 0, wq = 0;
     uint32_t phase = 0, wphase = 0;
     bool exhausted = false, stop = false;
@@ -902,8 +921,8 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
             }
         } else {
             int tm, tn;
-            raster(it.y, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
-            do_reduce<BN>(p, c, tm, tn, etid, epoch, st);
+            raster(it.y / p.red_split, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+            do_reduce<BN>(p, c, tm, tn, it.y % p.red_split, p.red_split, etid, epoch, st);
         }
         if (etid == 0) *reinterpret_cast<volatile uint32_t *>(&s.epi_done) = s.epi_done + 1;
     }
@@ -943,7 +962,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_persistent_kernel(const __gr
         run1_epilogue<BN>(p, s, stages, c, tmem_base, epoch);
     } else if (lane == 0 && blockIdx.x == 0 &&
                (p.mode == MK_MODE_ADAPTIVE || (p.mode == MK_MODE_STATIC && p.trace))) {
-        run_controller(p, c, p.num_units, p.num_tiles, 1, gridDim.x, 1);
+        run_controller(p, c, p.num_units, p.num_tiles * p.red_split, 1, gridDim.x, 1);
     }
     __syncwarp();
     tc_fence_before();
@@ -969,9 +988,10 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                               uint32_t crank) {
     using T = Cfg2<BN>;
     const bool leader = crank == 0;
+    const bool ag = p.op == MK_IOP_AG;
     const ClaimGeom g{static_cast<uint32_t>(p.num_pair_units),
-                      static_cast<uint32_t>(p.op == MK_IOP_AG ? p.pair_tiles_m : p.num_pair_tiles), blockIdx.x >> 1,
-                      gridDim.x >> 1, 2u};
+                      static_cast<uint32_t>(ag ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), blockIdx.x >> 1,
+                      gridDim.x >> 1, 2u, ag ? 1u : static_cast<uint32_t>(p.red_split)};
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
     const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
     const uint32_t peer_items = mapa_shared(smem_u32(&s.items[0]), 1);
@@ -1167,12 +1187,14 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                 atomicAdd(&c.hdr->units_done, 1u);
             }
         } else {
-            int sm, tn;
-            raster(it.y, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
-            if (p.op == MK_IOP_AG)
+            if (p.op == MK_IOP_AG) {
                 do_copy_chunk(p, c, 2 * it.y + static_cast<int>(crank), etid, epoch, st);
-            else
-                do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, etid, epoch, st);
+            } else {
+                int sm, tn;
+                raster(it.y / p.red_split, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+                do_reduce<BN>(p, c, 2 * sm + static_cast<int>(crank), tn, it.y % p.red_split, p.red_split, etid,
+                              epoch, st);
+            }
         }
         if (etid == 0) *reinterpret_cast<volatile uint32_t *>(&s.epi_done) = s.epi_done + 1;
     }
@@ -1231,7 +1253,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_pair_kernel(const __grid_con
         run2_epilogue<BN>(p, s, stages, c, tmem_base, epoch, crank);
     } else if (lane == 0 && blockIdx.x == 0 &&
                (p.mode == MK_MODE_ADAPTIVE || (p.mode == MK_MODE_STATIC && p.trace))) {
-        run_controller(p, c, p.num_pair_units, 2 * (p.op == MK_IOP_AG ? p.pair_tiles_m : p.num_pair_tiles), 2,
+        run_controller(p, c, p.num_pair_units,
+                       2 * (p.op == MK_IOP_AG ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), 2,
                        gridDim.x >> 1, 2);
     }
     __syncwarp();
@@ -1265,9 +1288,11 @@ __global__ void __launch_bounds__(MK_EPI_THREADS, 1) mk_reduce_kernel(const __gr
     __syncthreads();
     const Ctx c{p.hdr, &s_abort, p.timeout_ns, 4 * p.timeout_ns};
     Staging st{ring, MK_REDUCE_RING_BYTES, rfull, 0};
-    for (int lt = blockIdx.x; lt < p.num_tiles; lt += gridDim.x) {
-        reduce_tile_staged<BN>(p, c, lt / p.tiles_n, lt % p.tiles_n, threadIdx.x, st);
-        if (p.discard) discard_tile<BN>(p, lt, threadIdx.x, MK_EPI_THREADS);
+    const int items = p.num_tiles * p.red_split;
+    for (int i = blockIdx.x; i < items; i += gridDim.x) {
+        const int lt = i / p.red_split, sub = i % p.red_split;
+        reduce_tile_staged<BN>(p, c, lt / p.tiles_n, lt % p.tiles_n, sub, p.red_split, threadIdx.x, st);
+        if (p.discard) discard_tile<BN>(p, lt, sub, p.red_split, threadIdx.x, MK_EPI_THREADS);
     }
 }
 

@@ -104,6 +104,15 @@ typedef enum {
  *                     while B columns stream past them; 0 = sized from the
  *                     shape so that the group's A rows of all P ranks take
  *                     about 32 MB.
+ *   reduce_split    : the reduction of each output tile is cut into this many
+ *                     column slices, each claimed as its own item, so that the
+ *                     final reductions of a shape with few tiles spread over
+ *                     the whole grid; 0 = the smallest power of two (at most
+ *                     8) giving two items per communication-capable block.
+ *                     Values above the tile's chunk count (16 for 256-column
+ *                     tiles with P <= 8) are clamped to it.  Every element is
+ *                     still summed over ranks 0..P-1 in order, so results do
+ *                     not depend on it.  Ignored by AllGather + GEMM.
  */
 typedef struct {
     int32_t split_mode;
@@ -115,7 +124,7 @@ typedef struct {
     uint32_t flags;
     int64_t debug_skip_unit;
     int32_t raster_group;
-    int32_t reserved;
+    int32_t reduce_split;
 } mk_opts;
 
 /* One controller record written to mk_opts.trace (32 bytes). */

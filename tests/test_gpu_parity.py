@@ -96,6 +96,25 @@ def test_edge_shapes_random_within_tolerance(P, M, N, Kr):
             gu.check_tolerance(gu.host_values(C), ref, out_bf16=(out == "bf16"))
 
 
+# Each output tile's reduction cut into column slices claimed as separate items: every element is
+# still the rank-ordered sum, so integer inputs stay bit-exact for any slicing, including counts
+# that do not divide the tile's chunks (3), the chunk count itself (16), and a clamped request.
+@pytest.mark.parametrize("split", [1, 3, 16, 64])
+@pytest.mark.parametrize("P,M,N,Kr", [(3, 130, 520, 72), (8, 640, 1032, 128), (12, 256, 264, 64)])
+def test_reduce_slices_integer_bit_exact(P, M, N, Kr, split):
+    wl = ig.Workload("slices", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32", seed=split)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = oracle.allreduce(A, B)
+    for tiles in TILES:
+        for mode in MODES:
+            C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=2, tiles=tiles, reduce_split=split))
+            gu.assert_bit_exact(gu.host_values(C), ref)
+    if M % P == 0:
+        for mode in MODES:
+            out = gu.call_rs(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=2, reduce_split=split))
+            gu.assert_bit_exact(np.concatenate([gu.host_values(x) for x in out]), ref)
+
+
 def test_zero_k_gives_zeros_and_empty_is_noop():
     P, M, N = 3, 200, 136
     Ad = [torch.empty((M, 0), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
