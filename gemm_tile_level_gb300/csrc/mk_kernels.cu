@@ -29,6 +29,8 @@
 // MK_ERR_TIMEOUT plus a grid-wide abort; then every block stops claiming work, skips pending
 // reductions, and drains its queued compute items so that no TMA load or MMA is in flight at
 // exit.  Waits inside one block's (or pair's) pipeline only give up after 4 x timeout_ns.
+#include <atomic>
+
 #include "mk_internal.h"
 #include "mk_ptx.cuh"
 #include "mk.h"
@@ -1321,18 +1323,31 @@ static cudaError_t prepare() {
                                 static_cast<int>(smem_bytes_for<BN, PAIR>()));
 }
 
+// Per-device results of the one-time launch preparation (the kernel's shared-memory opt-in and its
+// occupancy), so that a call pays for the occupancy query only once per device.
+constexpr int kMaxDevices = 64;
+
 template <int BN, bool PAIR>
 static cudaError_t max_ctas(int *ctas) {
-    cudaError_t e = prepare<BN, PAIR>();
-    if (e != cudaSuccess) return e;
+    static std::atomic<int> cached[kMaxDevices];   // co-resident blocks + 1; 0 = not yet known
     int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *ctas = c - 1;
+            return cudaSuccess;
+        }
+    }
+    if ((e = prepare<BN, PAIR>()) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (!PAIR) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mk::mk_persistent_kernel<BN>, MK_THREADS,
                                                           smem_bytes_for<BN, PAIR>());
         *ctas = per_sm * sms;
+        if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) cached[dev].store(*ctas + 1);
         return e;
     }
     cudaLaunchConfig_t cfg = {};
@@ -1349,6 +1364,7 @@ static cudaError_t max_ctas(int *ctas) {
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, mk::mk_pair_kernel<BN>, &cfg);
     *ctas = 2 * clusters;
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) cached[dev].store(*ctas + 1);
     return e;
 }
 
@@ -1425,7 +1441,8 @@ cudaError_t mk_launch_persistent(const MkParams &p, int bn, bool pair, int num_c
 }
 
 cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s) {
-    const int grid = num_ctas < p.num_tiles ? num_ctas : p.num_tiles;
+    const int items = p.num_tiles * p.red_split;
+    const int grid = num_ctas < items ? num_ctas : items;
     if (grid <= 0) return cudaSuccess;
     const size_t smem = MK_REDUCE_RING_BYTES + 1024;
     cudaError_t e;
