@@ -261,10 +261,11 @@ def reference_arm(args, wl, ranks):
 # ------------------------------------------------------------------ GPU arm
 _EXTRA_FLAGS = 0   # MK_FLAG_SINGLE_SM_TILES (--tiles single), MK_FLAG_NO_COOPERATIVE (--no-cooperative)
 _REDUCE_SPLIT = 0  # --reduce-split (0 = chosen by the library)
+_RASTER_GROUP = 0  # --raster-group (0 = chosen by the library)
 
 
 def split_opts(api, mk, split: str, comm_sms: int):
-    kw = dict(flags=_EXTRA_FLAGS, reduce_split=_REDUCE_SPLIT)
+    kw = dict(flags=_EXTRA_FLAGS, reduce_split=_REDUCE_SPLIT, raster_group=_RASTER_GROUP)
     if split == "adaptive":
         return api.make_opts(mk.MK_SPLIT_ADAPTIVE, comm_sms=comm_sms, **kw)
     if split == "static":
@@ -505,6 +506,10 @@ def main():
                     help="SM-pair 256 x BN compute tiles (default) or one-SM 128 x BN tiles")
     ap.add_argument("--no-cooperative", action="store_true",
                     help="launch without the cooperative attribute (for profilers that cannot replay it)")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="tile rows per band of the compute order (0 = the library's choice)")
+    ap.add_argument("--tile-major", action="store_true",
+                    help="compute the P ranks of each tile back to back instead of band by band")
     ap.add_argument("--reduce-split", type=int, default=0,
                     help="column slices per output tile's reduction (0 = the library's choice)")
     ap.add_argument("--shape", default="", help="P,M,N,K_per_rank override (same distributions); "
@@ -521,9 +526,11 @@ def main():
     ap.add_argument("--sweep-out", default="")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
-    global _EXTRA_FLAGS, _REDUCE_SPLIT
-    _EXTRA_FLAGS = (2 if args.tiles == "single" else 0) | (8 if args.no_cooperative else 0)
+    global _EXTRA_FLAGS, _REDUCE_SPLIT, _RASTER_GROUP
+    _EXTRA_FLAGS = (2 if args.tiles == "single" else 0) | (8 if args.no_cooperative else 0) | \
+        (16 if args.tile_major else 0)
     _REDUCE_SPLIT = args.reduce_split
+    _RASTER_GROUP = args.raster_group
     if args.sweep:
         sweep(args)
         return

@@ -26,13 +26,35 @@ mk_status fail_cuda(cudaError_t e, const char *what) {
 }
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
-constexpr double kRasterL2Budget = 32e6;   // bytes of A rows (all ranks) kept resident per group
+constexpr double kRasterL2Budget = 32e6;   // tile-major: bytes of A rows (all ranks) resident per band
+constexpr double kBandL2Budget = 24e6;     // rank-major: bytes of one rank's A rows resident per band
+constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-major from this M on
+constexpr double kTailL2Bytes = 64e6;        // partial tiles that stay in L2 until the end of a call
+constexpr double kTailL2Bandwidth = 12e12;   // bytes/s the grid streams from L2
+constexpr double kHbmEfficiency = 0.8;       // streaming fraction of the nominal HBM bandwidth
 
-// Rows of compute tiles per raster group: the group's A rows of all P ranks should fit in a
-// slice of L2 so that each B column streamed past them is reused by the whole group.
-int auto_raster_group(bool pair, int P, int64_t Kr, int64_t row_tiles) {
-    const double per_row = static_cast<double>(P) * (pair ? 2 * MK_BM : MK_BM) * static_cast<double>(Kr) * 2.0;
-    int64_t g = per_row > 0 ? static_cast<int64_t>(kRasterL2Budget / per_row) : row_tiles;
+// Nominal HBM bandwidth of the current device (bytes/s) from its memory clock and bus width,
+// scaled to what a streaming kernel reaches; cached per process.
+double device_hbm_bandwidth() {
+    static double cached = 0.0;
+    if (cached > 0.0) return cached;
+    int dev = 0, khz = 0, bits = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&khz, cudaDevAttrMemoryClockRate, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&bits, cudaDevAttrGlobalMemoryBusWidth, dev) == cudaSuccess && khz > 0 && bits > 0)
+        cached = 2.0 * khz * 1e3 * bits / 8.0 * kHbmEfficiency;
+    else
+        cached = 6.5e12;
+    return cached;
+}
+
+// Rows of compute tiles per band: the A rows that are live while a band is computed (one rank's
+// in rank-major order, all P ranks' in tile-major order) should fit in a slice of L2 so that each
+// B column streamed past them is reused by the whole band.
+int auto_raster_group(bool pair, int P, int64_t Kr, int64_t row_tiles, bool rank_major) {
+    const double per_row = static_cast<double>(rank_major ? 1 : P) * (pair ? 2 * MK_BM : MK_BM) *
+                           static_cast<double>(Kr) * 2.0;
+    const double budget = rank_major ? kBandL2Budget : kRasterL2Budget;
+    int64_t g = per_row > 0 ? static_cast<int64_t>(budget / per_row) : row_tiles;
     if (g > row_tiles) g = row_tiles;
     if (g < 1) g = 1;
     return static_cast<int>(g);
@@ -111,17 +133,6 @@ mk_status encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t col
     return MK_OK;
 }
 
-// Shape of a reduce-role cost relative to a compute unit, used for the first target before
-// the controller has measurements: per-SM tensor rate ~11 TFLOP/s, per-SM streaming rate
-// ~120 GB/s.  Only the ratio matters.
-int initial_reduce_ctas(int S, int P, int bn, int64_t Kr) {
-    const double t_unit = 2.0 * MK_BM * bn * static_cast<double>(Kr) / 11e12;
-    const double t_tile = static_cast<double>(P) * MK_BM * bn * 4.0 / 120e9;
-    int nr = static_cast<int>(S * t_tile / (P * t_unit + t_tile) + 0.5);
-    if (nr < 1) nr = 1;
-    if (nr > S - 1) nr = S - 1;
-    return nr;
-}
 
 mk_status check_opts(const mk_opts *o) {
     if (o->split_mode < MK_SPLIT_ADAPTIVE || o->split_mode > MK_SPLIT_UNFUSED)
@@ -235,18 +246,29 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
         int nr = (o.comm_sms + per_role - 1) / per_role;
         if (nr > role_units - 1) nr = role_units - 1;
         p.static_nr = nr < 1 ? 1 : nr;
-        int init = o.comm_sms > 0 ? p.static_nr
-                                  : (initial_reduce_ctas(S, P, g.bn, Kr) + per_role - 1) / per_role;
-        if (init > role_units - 1) init = role_units - 1;
-        p.init_nr = init < 1 ? 1 : init;
+        // the adaptive controller starts from the caller's count, else from one role unit
+        p.init_nr = o.comm_sms > 0 ? p.static_nr : 1;
     }
+    // Rank-major bands pay off once there are several bands; a short M has a single band, whose
+    // tiles would all complete in the last 1/P of the GEMM, so it keeps the tile-major order.
+    p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : (o.flags & MK_FLAG_RANK_MAJOR) ? 1 : (M >= kRankMajorMinRows);
     p.raster_group = o.raster_group > 0 ? o.raster_group
-                                        : auto_raster_group(pair, P, Kr, pair ? g.pair_tiles_m : g.tiles_m);
+                                        : auto_raster_group(pair, P, Kr, pair ? g.pair_tiles_m : g.tiles_m,
+                                                            p.rank_major != 0);
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
     p.ctrl_period_ns = kCtrlPeriodNs;
     p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P);
+    {
+        // SM time of one reduce item when the whole grid reduces at the end of the call: the
+        // item's partial bytes at the grid's share of memory bandwidth (L2 when every partial
+        // tile of the call fits there, else HBM)
+        const double item_bytes = static_cast<double>(MK_BM) * g.bn * 4.0 * P / p.red_split;
+        const double partials = static_cast<double>(g.num_tiles) * MK_BM * g.bn * 4.0 * P;
+        const double bw = partials <= kTailL2Bytes ? kTailL2Bandwidth : device_hbm_bandwidth();
+        p.ctrl_tail_ns = static_cast<int32_t>(item_bytes * S / bw * 1e9);
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (o.split_mode == MK_SPLIT_UNFUSED) {
@@ -376,9 +398,11 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     int nr = o.comm_sms > 0 ? (o.comm_sms + 1) / 2 : initial_copy_pairs(role_units, P, M, N, K);
     if (nr > role_units - 1) nr = role_units - 1;
     p.static_nr = p.init_nr = nr < 1 ? 1 : nr;
-    p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(true, 1, K, g.pair_tiles_m);
+    p.rank_major = 0;
+    p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(true, 1, K, g.pair_tiles_m, false);
     p.discard = 0;
     p.ctrl_period_ns = kCtrlPeriodNs;
+    p.ctrl_tail_ns = 0;   // unused: AllGather + GEMM fixes the roles for the call
     p.red_split = 1;
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;

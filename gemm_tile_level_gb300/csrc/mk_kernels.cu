@@ -161,6 +161,37 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, i
     tn = local / gsize;
 }
 
+// Compute unit u -> (tile t in raster order, rank r).  Tile-major order visits the P ranks of a
+// tile back to back.  Rank-major order cuts the tile rows into bands of G rows (G = raster_group)
+// and computes a band for rank 0, then the same band for rank 1, and so on: while one rank's band
+// is computed, L2 holds that rank's A rows of the band and each B column is read once per band,
+// instead of all P ranks' operands competing for L2 at once.  `rows` is tiles_m, or pair_tiles_m
+// for SM-pair tiles.
+__device__ __forceinline__ void unit_tile(const MkParams &p, int rows, int u, int &t, int &r) {
+    if (!p.rank_major) {
+        t = u / p.P;
+        r = u - t * p.P;
+        return;
+    }
+    const int per_band = p.raster_group * p.tiles_n;
+    const int b = u / (per_band * p.P);
+    const int rem = u - b * per_band * p.P;
+    const int bt = min(p.raster_group, rows - b * p.raster_group) * p.tiles_n;   // tiles in band b
+    r = rem / bt;
+    t = b * per_band + (rem - r * bt);
+}
+
+// One past the largest compute unit index that tile t consumes (its rank P-1 unit).
+__device__ __forceinline__ uint32_t tile_units_end(const MkParams &p, int rows, uint32_t t) {
+    if (!p.rank_major) return (t + 1) * static_cast<uint32_t>(p.P);
+    const uint32_t per_band = static_cast<uint32_t>(p.raster_group * p.tiles_n);
+    const uint32_t b = t / per_band;
+    const uint32_t local = t - b * per_band;
+    const uint32_t bt = static_cast<uint32_t>(min(p.raster_group, rows - static_cast<int>(b) * p.raster_group) *
+                                              p.tiles_n);
+    return b * per_band * static_cast<uint32_t>(p.P) + static_cast<uint32_t>(p.P - 1) * bt + local + 1;
+}
+
 // ------------------------------------------------------------------ work claiming
 // Role of a role unit (a block, or an SM pair) for its next claim: reduce if its index is
 // >= R - target (the target is published by the controller or fixed by the caller); once the
@@ -172,8 +203,9 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, i
 // reduction waits only on units claimed before it, which in turn wait only on items claimed
 // earlier still: the wait-for relation follows claim order and has no cycle.
 //
-// A reduce-role unit claims the next item only when the units finished so far reach it (one
-// item of slack), so reducers do not park on items far ahead of the compute front.
+// A reduce-role unit claims the next item only when the units finished so far come within P of
+// the last unit it consumes, so reducers do not park on items far ahead of the compute front.
+// Reduce items follow the order in which tiles complete: tile index order for either unit order.
 //
 // units_done counts `done_per_unit` increments per compute unit (1 for one-SM tiles, 2 for an
 // SM pair whose two CTAs each count their half).
@@ -184,6 +216,7 @@ struct ClaimGeom {
     uint32_t role_units;  // role units in the grid
     uint32_t done_per_unit;
     uint32_t split;       // reduce items per tile (column slices of its reduction)
+    int rows;             // tile rows of the unit order (tiles_m, or pair_tiles_m)
 };
 
 __device__ bool wait_claimed(const Ctx &c, uint32_t need) {
@@ -245,8 +278,9 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
                 if (next >= g.num_items) return make_int2(ITEM_END, 0);
                 const uint32_t done = ld_relaxed_gpu(&h->units_done);
                 const uint32_t issued = ld_relaxed_gpu(&h->compute_next);
-                const uint64_t per_tile = static_cast<uint64_t>(P) * g.done_per_unit;
-                if (issued < g.num_units && (static_cast<uint64_t>(next / g.split) + 1) * per_tile > done + per_tile) {
+                const uint64_t slack = static_cast<uint64_t>(P) * g.done_per_unit;
+                const uint64_t need = tile_units_end(p, g.rows, next / g.split);
+                if (issued < g.num_units && need * g.done_per_unit > done + slack) {
                     // nothing ready yet: wait for compute progress (bounded), then re-read the role
                     if (done != gate_seen) {
                         gate_seen = done;
@@ -262,7 +296,7 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
         }
         const uint32_t i = atomicAdd(&h->reduce_next, 1u);
         if (i >= g.num_items) return make_int2(ITEM_END, 0);
-        const uint64_t need64 = (static_cast<uint64_t>(i / g.split) + 1) * P;
+        const uint64_t need64 = tile_units_end(p, g.rows, i / g.split);
         const uint32_t need = need64 < g.num_units ? static_cast<uint32_t>(need64) : g.num_units;
         if (!wait_claimed(c, need)) return make_int2(ITEM_END, 0);
         return make_int2(ITEM_REDUCE, static_cast<int>(i));
@@ -323,26 +357,35 @@ __device__ __forceinline__ void discard_tile(const MkParams &p, int lt, int sub,
     }
 }
 
-// Thread 0 of the reduce group: acquire flag[lt][r] == epoch for every rank.  False if the
+// The first warp of the reduce group: lane r acquires flag[lt][r] == epoch, all P flags polled at
+// once (one round trip per poll instead of P).  Every lane returns the same value: false if the
 // grid is aborting or the limit ran out (which raises MK_ERR_TIMEOUT).
-__device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int lt, uint32_t epoch) {
+__device__ bool wait_tile_ready(const MkParams &p, const Ctx &c, int lt, uint32_t epoch, int lane) {
     const uint32_t *f = p.flags + static_cast<size_t>(lt) * p.P;
+    bool seen = lane >= p.P;
     uint64_t t0 = 0;
-    for (int r = 0; r < p.P; ++r) {
-        for (uint32_t polls = 0; ld_acquire_gpu(f + r) != epoch; ++polls) {
-            if (*c.s_abort) return false;
-            if (t0 == 0) t0 = globaltimer();
-            if ((polls & 15u) == 15u) {
-                if (global_abort(c)) return false;
-                if (globaltimer() - t0 > c.timeout_ns || polls > (1u << 30)) {
-                    raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, static_cast<uint32_t>(lt * p.P + r));
-                    return false;
+    for (uint32_t polls = 0;; ++polls) {
+        if (!seen) seen = ld_acquire_gpu(f + lane) == epoch;
+        if (__all_sync(0xFFFFFFFFu, seen)) return true;
+        int stop = 0;
+        if (lane == 0) {
+            if (*c.s_abort) {
+                stop = 1;
+            } else {
+                if (t0 == 0) t0 = globaltimer();
+                if ((polls & 15u) == 15u) {
+                    if (global_abort(c)) {
+                        stop = 1;
+                    } else if (globaltimer() - t0 > c.timeout_ns || polls > (1u << 30)) {
+                        raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, static_cast<uint32_t>(lt * p.P));
+                        stop = 1;
+                    }
                 }
             }
-            __nanosleep(32);
         }
+        if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+        __nanosleep(32);
     }
-    return true;
 }
 
 // Reduce-role staging through the block's TMA ring, which is idle while the block reduces (the
@@ -461,7 +504,9 @@ __device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int s
     bool ok = true;
     const bool exists = tm < p.tiles_m;
     const int lt = tm * p.tiles_n + tn;
-    if (exists && etid == 0) ok = wait_tile_ready(p, c, lt, epoch);
+    if (exists && etid < 32) ok = wait_tile_ready(p, c, lt, epoch, etid);
+    // partials written by other blocks' generic-proxy stores are read below by bulk copies
+    if (exists && ok && etid == 0) fence_proxy_async_global();
     ok = bar_and(1, MK_EPI_THREADS, ok);
     if (exists && ok) {
         const long long t0 = clock64();
@@ -483,8 +528,11 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
     const int half = (warp - MK_EPI_WARP0) >> 2;      // which half of the tile's columns
     const int row = lq * 32 + lane;
     float *tile = partial_tile<BN>(p, r, lt);
-    // partial tiles should live in L2 until the reduce role has read them (then they are discarded)
-    const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+    // partial tiles should live in L2 until the reduce role has read them (then they are
+    // discarded); in rank-major order only the last rank's tiles are read soon after they are
+    // written, the others would only crowd out the band's A rows
+    const uint64_t pol = !p.l2_hints ? policy_evict_normal()
+                         : (p.rank_major && r < p.P - 1) ? policy_evict_first() : policy_evict_last();
 #pragma unroll 1
     for (int cc = 0; cc < BN / 64; ++cc) {
         const int col0 = half * (BN / 2) + cc * 32;
@@ -505,27 +553,38 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
 }
 
 // ------------------------------------------------------------------ split controller
-// Every ctrl_period_ns: with W_c compute units and W_r tiles left, and measured SM-cycle costs
-// tau_c per unit and tau_r per tile, publish
-//     n_r = clamp(round(S * W_r tau_r / (W_c tau_c + W_r tau_r)), 1, S - 1)
-// SMs of communication role (converted to role units), i.e. give each role SMs in proportion
-// to the work it still has, so both finish together.  As compute nears completion W_c -> 0 and
-// the target moves toward communication.  This formula is a reading of the controller's
-// stated intent; the pages do not give it.  The loop doubles as a watchdog: no progress for
-// timeout_ns raises MK_ERR_TIMEOUT.
-__device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_units, uint32_t num_tiles_total,
+// The split controller (one thread of block 0).  It reads the progress counters every
+// ctrl_period_ns and publishes the number of reduce-role units.  Moving one reduce item from the
+// end of the call into the compute phase costs the GEMM the SM time a reducer spends on it
+// (tau, measured: reduce-role SM time per item), while reducing it at the end, when every SM
+// reduces and the reduction runs at memory speed, costs the whole grid item_bytes / bandwidth,
+// i.e. S * item_bytes / bandwidth SM time (tau_tail, computed by the host).  So the controller
+// adds a reduce-role unit while the measured tau is below 0.8 tau_tail (early reduction is the
+// cheaper place for the work) and removes one while it is above tau_tail, waiting dwell_ns
+// between changes so the measurement can follow.  It starts from one unit.  Once the compute
+// queue is empty every unit reduces regardless of the target (see claim_work), the shift toward
+// communication near the end of the GEMM.  The pages state the controller's inputs (progress
+// counters) and output (a target number of communication blocks) but not its rule; this rule
+// is a reading of that intent.  In static mode the thread only records the trace.  The loop
+// doubles as a watchdog: no progress for timeout_ns raises MK_ERR_TIMEOUT.
+__device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_units, uint32_t num_items_total,
                                uint32_t done_per_unit, int role_units, int sms_per_role) {
     MkWsHeader *h = c.hdr;
     const int S = role_units * sms_per_role;
-    // In static mode the warp only records the trace (the split is the caller's).
-    const bool adaptive = p.mode == MK_MODE_ADAPTIVE;
-    int cur = adaptive ? p.init_nr : p.static_nr;
+    const bool adaptive = p.mode == MK_MODE_ADAPTIVE && p.op != MK_IOP_AG;
+    int cur = p.mode == MK_MODE_ADAPTIVE ? p.init_nr : p.static_nr;
     if (adaptive) st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
     const uint64_t start = globaltimer();
-    uint64_t last_change = start;
+    const long long clk0 = clock64();
+    uint64_t last_change = start, last_adjust = start;
     uint32_t last_u = 0, last_d = 0;
     mk_trace_record *trace = static_cast<mk_trace_record *>(p.trace);
     uint32_t nrec = 0;
+    uint64_t busy_mark = 0;
+    uint32_t items_mark = 0;
+    double tau_ns = -1.0;                        // EWMA of reduce-role SM time per item
+    const double tau_tail = static_cast<double>(p.ctrl_tail_ns);
+    const uint64_t dwell_ns = 4000;
     for (uint32_t it = 0; it < (1u << 30); ++it) {
         const uint32_t u = ld_relaxed_gpu(&h->units_done);
         const uint32_t d = ld_relaxed_gpu(&h->tiles_done);
@@ -540,7 +599,7 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
             rec.reserved = 0;
             trace[nrec++] = rec;
         }
-        if (d >= num_tiles_total || global_abort(c)) break;
+        if (d >= num_items_total || global_abort(c)) break;
         if (u != last_u || d != last_d) {
             last_u = u;
             last_d = d;
@@ -549,17 +608,22 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
             raise_error(c, MK_ERR_TIMEOUT, SITE_WATCHDOG, d);
             break;
         }
-        const uint32_t units = u / done_per_unit;
-        if (adaptive && units > 0 && d > 0) {
-            const double tau_c = sms_per_role * static_cast<double>(ld_relaxed_gpu64(&h->compute_busy)) / units;
-            const double tau_r = static_cast<double>(ld_relaxed_gpu64(&h->reduce_busy)) / d;
-            const double wc = static_cast<double>(num_units - min(units, num_units)) * tau_c;
-            const double wr = static_cast<double>(num_tiles_total - d) * tau_r;
-            if (wc + wr > 0.0) {
-                int nr = static_cast<int>(S * wr / (wc + wr) / sms_per_role + 0.5);
-                nr = max(1, min(role_units - 1, nr));
+        if (adaptive && u / done_per_unit < num_units) {
+            if (d >= items_mark + 4 && now > start + 1000) {
+                const uint64_t busy = ld_relaxed_gpu64(&h->reduce_busy);
+                const double cyc_per_ns = static_cast<double>(clock64() - clk0) / static_cast<double>(now - start);
+                const double t = static_cast<double>(busy - busy_mark) / (d - items_mark) / cyc_per_ns;
+                tau_ns = tau_ns < 0.0 ? t : 0.75 * tau_ns + 0.25 * t;
+                busy_mark = busy;
+                items_mark = d;
+            }
+            if (tau_ns > 0.0 && now - last_adjust > dwell_ns) {
+                int nr = cur;
+                if (tau_ns < 0.8 * tau_tail && nr < role_units - 1) ++nr;
+                else if (tau_ns > tau_tail && nr > 1) --nr;
                 if (nr != cur) {
                     cur = nr;
+                    last_adjust = now;
                     st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
                 }
             }
@@ -766,7 +830,7 @@ template <int BN>
 __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_t *stages, const Ctx &c) {
     using T = Cfg1<BN>;
     const ClaimGeom g{static_cast<uint32_t>(p.num_units), static_cast<uint32_t>(p.num_tiles * p.red_split),
-                      blockIdx.x, gridDim.x, 1u, static_cast<uint32_t>(p.red_split)};
+                      blockIdx.x, gridDim.x, 1u, static_cast<uint32_t>(p.red_split), p.tiles_m};
     int stage = 0, wq = 0;
     uint32_t phase = 0, wphase = 0;
     bool exhausted = false, stop = false;
@@ -787,8 +851,9 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
         }
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
-        const int u = it.y, t = u / p.P, r = u - t * p.P;
-        int tm, tn;
+        const int u = it.y;
+        int t, r, tm, tn;
+        unit_tile(p, p.tiles_m, u, t, r);
         raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -899,8 +964,9 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
         }
         if (it.x == ITEM_END) break;
         if (it.x == ITEM_COMPUTE) {
-            const int u = it.y, t = u / p.P, r = u - t * p.P;
-            int tm, tn;
+            const int u = it.y;
+            int t, r, tm, tn;
+            unit_tile(p, p.tiles_m, u, t, r);
             raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
             const int lt = tm * p.tiles_n + tn;
             ok = true;
@@ -993,7 +1059,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     const bool ag = p.op == MK_IOP_AG;
     const ClaimGeom g{static_cast<uint32_t>(p.num_pair_units),
                       static_cast<uint32_t>(ag ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), blockIdx.x >> 1,
-                      gridDim.x >> 1, 2u, ag ? 1u : static_cast<uint32_t>(p.red_split)};
+                      gridDim.x >> 1, 2u, ag ? 1u : static_cast<uint32_t>(p.red_split), p.pair_tiles_m};
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
     const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
     const uint32_t peer_items = mapa_shared(smem_u32(&s.items[0]), 1);
@@ -1026,8 +1092,9 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (it.x == ITEM_REDUCE) ring_free_at = pushed;
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
-        const int u = it.y, pt = u / p.P, r = u - pt * p.P;
-        int sm, tn;
+        const int u = it.y;
+        int pt, r, sm, tn;
+        unit_tile(p, p.pair_tiles_m, u, pt, r);
         raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
         const int tm = 2 * sm + static_cast<int>(crank);
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
@@ -1156,8 +1223,9 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         }
         if (it.x == ITEM_END) break;
         if (it.x == ITEM_COMPUTE) {
-            const int u = it.y, pt = u / p.P, r = u - pt * p.P;
-            int sm, tn;
+            const int u = it.y;
+            int pt, r, sm, tn;
+            unit_tile(p, p.pair_tiles_m, u, pt, r);
             raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
             const int tm = 2 * sm + static_cast<int>(crank);
             const bool exists = tm < p.tiles_m;

@@ -38,6 +38,8 @@ MK_FLAG_KEEP_PARTIALS = 1
 MK_FLAG_SINGLE_SM_TILES = 2
 MK_FLAG_NO_L2_HINTS = 4
 MK_FLAG_NO_COOPERATIVE = 8
+MK_FLAG_TILE_MAJOR = 16
+MK_FLAG_RANK_MAJOR = 32
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",

@@ -71,6 +71,9 @@ typedef enum {
 #define MK_FLAG_KEEP_PARTIALS 1u   /* do not discard consumed partial tiles from L2 (default: discard) */
 #define MK_FLAG_SINGLE_SM_TILES 2u /* one SM per 128 x 256 compute tile instead of an SM pair per 256 x 256 */
 #define MK_FLAG_NO_L2_HINTS 4u     /* load operands without L2 eviction-priority hints */
+#define MK_FLAG_TILE_MAJOR 16u    /* compute the P ranks of each tile back to back */
+#define MK_FLAG_RANK_MAJOR 32u    /* compute bands of tile rows rank by rank (see raster_group); without
+                                     either flag the order is rank-major for M >= 1024, else tile-major */
 #define MK_FLAG_NO_COOPERATIVE 8u  /* launch without the cooperative attribute (some profilers cannot replay
                                       cooperative cluster launches); co-residency then rests on the
                                       occupancy check made before every launch */
@@ -84,8 +87,9 @@ typedef enum {
  *                     default, assign roles per pair, so an odd count is
  *                     rounded up to whole pairs; with MK_FLAG_SINGLE_SM_TILES
  *                     roles are per SM and comm_sms <= grid size - 1).
- *                     MK_SPLIT_ADAPTIVE: initial target (0 = derived from the
- *                     shape).  Ignored for MK_SPLIT_UNFUSED.
+ *                     MK_SPLIT_ADAPTIVE: initial target (0 = one role unit;
+ *                     the controller then follows the backlog of ready tiles).
+ *                     Ignored for MK_SPLIT_UNFUSED.
  *   wait_timeout_ns : limit of every device-side wait (readiness flags,
  *                     pipeline barriers, the controller's progress watchdog);
  *                     0 = 2 s.  A wait that runs out sets MK_ERR_TIMEOUT.
@@ -94,16 +98,21 @@ typedef enum {
  *   num_ctas        : persistent grid size (blocks, one per SM; even with
  *                     SM-pair tiles), 0 = as many as can be co-resident.
  *   flags           : MK_FLAG_* bits.
- *   debug_skip_unit : fault injection for tests: the compute unit with this
- *                     index (tile * P + rank, tiles of 256 rows with SM-pair
- *                     tiles, of 128 rows otherwise) is never produced, so the
- *                     consumer's bounded wait must run out.  -1 = off.
- *   raster_group    : compute tiles are visited in groups of this many tile
- *                     rows (256-row rows with SM-pair tiles), column by column
- *                     inside a group, so that the group's A rows stay in L2
- *                     while B columns stream past them; 0 = sized from the
- *                     shape so that the group's A rows of all P ranks take
- *                     about 32 MB.
+ *   debug_skip_unit : fault injection for tests: the compute unit (one tile of
+ *                     one rank; tiles of 256 rows with SM-pair tiles, of 128
+ *                     rows otherwise) with this index in the compute order is
+ *                     never produced, so the consumer's bounded wait must run
+ *                     out.  -1 = off.
+ *   raster_group    : compute tiles are visited in groups ("bands") of this many
+ *                     tile rows (256-row rows with SM-pair tiles), column by
+ *                     column inside a band, so that the band's A rows stay in
+ *                     L2 while B columns stream past them.  In rank-major
+ *                     order each band is computed for rank 0, then for rank
+ *                     1, ..., so L2 holds one rank's band at a time, and 0
+ *                     sizes the band so that one rank's A rows of it take
+ *                     about 24 MB.  In tile-major order the P ranks of each
+ *                     tile are computed back to back and 0 sizes the band so
+ *                     that the A rows of all P ranks take about 32 MB.
  *   reduce_split    : the reduction of each output tile is cut into this many
  *                     column slices, each claimed as its own item, so that the
  *                     final reductions of a shape with few tiles spread over

@@ -115,6 +115,22 @@ def test_reduce_slices_integer_bit_exact(P, M, N, Kr, split):
             gu.assert_bit_exact(np.concatenate([gu.host_values(x) for x in out]), ref)
 
 
+# Both compute orders (bands of tile rows rank by rank, the default, or the P ranks of each tile
+# back to back) and band heights that leave a short last band must give the same bits.
+@pytest.mark.parametrize("order", ["rank_major", "tile_major"])
+@pytest.mark.parametrize("band", [0, 1, 3])
+def test_compute_orders_integer_bit_exact(order, band):
+    P, M, N, Kr = 6, 1400, 776, 136
+    wl = ig.Workload("order", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32", seed=band)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = oracle.allreduce(A, B)
+    fl = mk.MK_FLAG_TILE_MAJOR if order == "tile_major" else mk.MK_FLAG_RANK_MAJOR
+    for tiles in TILES:
+        for mode in MODES:
+            C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=opts_for(mode, comm_sms=6, tiles=tiles, flags=fl, raster_group=band))
+            gu.assert_bit_exact(gu.host_values(C), ref)
+
+
 def test_zero_k_gives_zeros_and_empty_is_noop():
     P, M, N = 3, 200, 136
     Ad = [torch.empty((M, 0), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
