@@ -411,7 +411,8 @@ def gpu_arm(args, wl, ranks):
                        "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
                        "parallelism": f"{wl.P} logical ranks on one GPU" + (
                            f"; {ranks.world} replicas" if ranks.world > 1 else "")},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * (2 if args.split == "unfused" else 1),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "unfused_baseline": unfused}
