@@ -62,14 +62,15 @@ int auto_raster_group(bool pair, int P, int64_t Kr, int64_t row_tiles, bool rank
 constexpr int kCtrlPeriodNs = 1000;
 
 // Column slices per output tile's reduction: by default the smallest power of two (at most 8)
-// that gives every communication-capable role unit two reduce items; never more slices than the
-// staged reducer has chunks in a tile (CH = 8 KiB per rank for P <= 8, else 4 KiB).
+// that gives every role unit a reduce item (each item restarts the staged pipeline, so finer
+// slices only pay while some units would otherwise get none); never more slices than the staged
+// reducer has chunks in a tile (CH = 8 KiB per rank for P <= 8, else 4 KiB).
 int choose_reduce_split(int requested, int64_t items, int role_units, int bn, int P) {
     const int nch = MK_BM * bn * 4 / (P <= 8 ? 8192 : 4096);
     int s = requested;
     if (s <= 0) {
         s = 1;
-        while (s < 8 && items * s < 2LL * role_units) s *= 2;
+        while (s < 8 && items * s < role_units) s *= 2;
     }
     return s < nch ? s : nch;
 }

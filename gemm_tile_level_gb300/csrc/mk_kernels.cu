@@ -818,7 +818,10 @@ __device__ bool wait_epilogue_done(const volatile uint32_t *epi_done, uint32_t c
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1; i != 0u; ++i) {
         if (*epi_done >= count) return true;
-        if ((i & 63u) == 0u && globaltimer() - t0 > c.pipe_timeout_ns) break;
+        if ((i & 63u) == 0u) {
+            if (global_abort(c)) return false;   // the epilogue stops on an abort
+            if (globaltimer() - t0 > c.pipe_timeout_ns) break;
+        }
         __nanosleep(64);
     }
     raise_error(c, MK_ERR_TIMEOUT, SITE_STAGE_EMPTY, count);
@@ -838,8 +841,13 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
     const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
     const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
     uint32_t pushed = 0, ring_free_at = 0;   // ring free once the epilogue has finished ring_free_at items
+    bool last_reduce = false;
     while (!stop) {
+        // Reduce items are claimed at most one ahead of the one in progress, so that the last
+        // items of a call spread over the grid instead of queueing behind a few blocks.
+        if (last_reduce && !wait_epilogue_done(&s.epi_done, pushed - 1, c)) break;
         const int2 it = claim_work(p, c, g, exhausted);
+        last_reduce = it.x == ITEM_REDUCE;
         if (!wait_bar<false>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
         s.items[wq] = it;
         mbar_arrive(smem_u32(&s.wfull[wq]));
@@ -1070,10 +1078,14 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
     const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
     uint32_t pushed = 0, ring_free_at = 0;
+    bool last_reduce = false;
     while (!stop) {
         int2 it;
         if (leader) {
+            // reduce items: at most one claimed ahead of the one in progress (see run1_producer)
+            if (last_reduce && !wait_epilogue_done(&s.epi_done, pushed - 1, c)) break;
             it = claim_work(p, c, g, exhausted);
+            last_reduce = it.x == ITEM_REDUCE;
             if (!wait_bar<true>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
             s.items[wq] = it;
             st_cluster_v2(peer_items + 8u * wq, it.x, it.y);

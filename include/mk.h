@@ -117,7 +117,7 @@ typedef enum {
  *                     column slices, each claimed as its own item, so that the
  *                     final reductions of a shape with few tiles spread over
  *                     the whole grid; 0 = the smallest power of two (at most
- *                     8) giving two items per communication-capable block.
+ *                     8) giving every block (SM pair) at least one item.
  *                     Values above the tile's chunk count (16 for 256-column
  *                     tiles with P <= 8) are clamped to it.  Every element is
  *                     still summed over ranks 0..P-1 in order, so results do
