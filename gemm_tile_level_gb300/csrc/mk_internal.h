@@ -41,7 +41,7 @@ struct MkWsHeader {
     uint32_t done_ctas;     // blocks finished in the current call
     uint32_t compute_next;  // next compute unit to claim
     uint32_t reduce_next;   // next output tile to claim for reduction
-    uint32_t target_nr;     // published number of reduce-role blocks (0 = not yet published)
+    uint32_t target_nr;     // published number of reduce-role units + 1 (0 = not yet published)
     uint32_t units_done;    // compute units whose partial tile is released
     uint32_t tiles_done;    // output tiles reduced and written
     uint32_t trace_count;   // controller records written

@@ -263,8 +263,8 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
         if (!exhausted) {
             int nr = p.static_nr;
             if (p.mode == MK_MODE_ADAPTIVE) {
-                const uint32_t pub = ld_relaxed_gpu(&h->target_nr);
-                nr = pub ? static_cast<int>(pub) : p.init_nr;
+                const uint32_t pub = ld_relaxed_gpu(&h->target_nr);   // target + 1, 0 = unpublished
+                nr = pub ? static_cast<int>(pub) - 1 : p.init_nr;
             }
             if (static_cast<int>(g.role_index) < static_cast<int>(g.role_units) - nr) {
                 const uint32_t u = atomicAdd(&h->compute_next, 1u);
@@ -561,7 +561,8 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
 // i.e. S * item_bytes / bandwidth SM time (tau_tail, computed by the host).  So the controller
 // adds a reduce-role unit while the measured tau is below 0.8 tau_tail (early reduction is the
 // cheaper place for the work) and removes one while it is above tau_tail, waiting dwell_ns
-// between changes so the measurement can follow.  It starts from one unit.  Once the compute
+// between changes so the measurement can follow.  It starts from one unit and may go down to
+// none, which leaves the whole reduction to the end of the call.  Once the compute
 // queue is empty every unit reduces regardless of the target (see claim_work), the shift toward
 // communication near the end of the GEMM.  The pages state the controller's inputs (progress
 // counters) and output (a target number of communication blocks) but not its rule; this rule
@@ -573,7 +574,7 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
     const int S = role_units * sms_per_role;
     const bool adaptive = p.mode == MK_MODE_ADAPTIVE && p.op != MK_IOP_AG;
     int cur = p.mode == MK_MODE_ADAPTIVE ? p.init_nr : p.static_nr;
-    if (adaptive) st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
+    if (adaptive) st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur) + 1u);   // 0 = unpublished
     const uint64_t start = globaltimer();
     const long long clk0 = clock64();
     uint64_t last_change = start, last_adjust = start;
@@ -620,11 +621,11 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
             if (tau_ns > 0.0 && now - last_adjust > dwell_ns) {
                 int nr = cur;
                 if (tau_ns < 0.8 * tau_tail && nr < role_units - 1) ++nr;
-                else if (tau_ns > tau_tail && nr > 1) --nr;
+                else if (tau_ns > tau_tail && nr > 0) --nr;
                 if (nr != cur) {
                     cur = nr;
                     last_adjust = now;
-                    st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur));
+                    st_relaxed_gpu(&h->target_nr, static_cast<uint32_t>(cur) + 1u);
                 }
             }
         }

@@ -47,7 +47,7 @@ def test_controller_trace_records():
     rec = rec[:n]
     S = gu.num_sms()
     assert (rec["blocks"] == S).all()
-    assert (rec["target"] >= 1).all() and (rec["target"] <= S - 1).all()
+    assert (rec["target"] >= 0).all() and (rec["target"] <= S - 1).all()
     assert (np.diff(rec["t"].astype(np.int64)) >= 0).all()
     assert (np.diff(rec["units"].astype(np.int64)) >= 0).all()
     assert (np.diff(rec["tiles"].astype(np.int64)) >= 0).all()
