@@ -136,7 +136,7 @@ mk_status encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t col
 
 
 mk_status check_opts(const mk_opts *o) {
-    if (o->split_mode < MK_SPLIT_ADAPTIVE || o->split_mode > MK_SPLIT_UNFUSED)
+    if (o->split_mode < MK_SPLIT_ADAPTIVE || o->split_mode > MK_SPLIT_ACCUMULATE)
         return fail(MK_ERR_INVALID_ARG, "split_mode %d out of range", o->split_mode);
     if (o->split_mode == MK_SPLIT_STATIC && o->comm_sms < 1)
         return fail(MK_ERR_INVALID_ARG, "static split needs comm_sms >= 1");
@@ -253,6 +253,9 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     // Rank-major bands pay off once there are several bands; a short M has a single band, whose
     // tiles would all complete in the last 1/P of the GEMM, so it keeps the tile-major order.
     p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : (o.flags & MK_FLAG_RANK_MAJOR) ? 1 : (M >= kRankMajorMinRows);
+    // accumulate mode wants the P ranks of a tile close together in time, so that the tile's
+    // accumulator stays in L2 across its P additions
+    if (o.split_mode == MK_SPLIT_ACCUMULATE && !(o.flags & MK_FLAG_RANK_MAJOR)) p.rank_major = 0;
     p.raster_group = o.raster_group > 0 ? o.raster_group
                                         : auto_raster_group(pair, P, Kr, pair ? g.pair_tiles_m : g.tiles_m,
                                                             p.rank_major != 0);
@@ -280,6 +283,11 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
         e = mk_launch_reduce(p, g.bn, S, s);
         if (e != cudaSuccess) return fail_cuda(e, "launch of the reduce kernel");
         return MK_OK;
+    }
+    if (o.split_mode == MK_SPLIT_ACCUMULATE) {
+        p.mode = MK_MODE_ACCUMULATE;
+        e = mk_launch_persistent(p, g.bn, pair, S, s);
+        return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the accumulating GEMM kernel");
     }
     p.mode = o.split_mode == MK_SPLIT_STATIC ? MK_MODE_STATIC : MK_MODE_ADAPTIVE;
     e = mk_launch_persistent(p, g.bn, pair, S, s);
@@ -317,6 +325,8 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     if (opts_in) o = *opts_in;
     mk_status st = check_opts(&o);
     if (st != MK_OK) return st;
+    if (o.split_mode == MK_SPLIT_ACCUMULATE)
+        return fail(MK_ERR_INVALID_ARG, "MK_SPLIT_ACCUMULATE applies to GEMM + AllReduce and GEMM + ReduceScatter");
     if (N % 8 || K % 8)
         return fail(MK_ERR_UNSUPPORTED_SHAPE, "N=%lld and K=%lld must be multiples of 8", (long long)N, (long long)K);
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "dimension above 2^31-1");

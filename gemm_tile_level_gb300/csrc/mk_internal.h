@@ -28,8 +28,12 @@ enum MkMode {
     MK_MODE_ADAPTIVE = 0,   // fused, controller publishes the split
     MK_MODE_STATIC = 1,     // fused, fixed split
     MK_MODE_COMPUTE_ONLY = 2, // unfused baseline: the GEMM kernel
-    MK_MODE_COMM_ONLY = 3     // unfused AllGather baseline: the copy kernel
+    MK_MODE_COMM_ONLY = 3,    // unfused AllGather baseline: the copy kernel
+    MK_MODE_ACCUMULATE = 4    // compute blocks add their partial tiles into one fp32 accumulator
 };
+
+// MkWsHeader::acc_state: whether the accumulator region is known to hold zeros
+enum { MK_ACC_FRESH = 0, MK_ACC_CLEAN = 1, MK_ACC_DIRTY = 2 };
 
 enum MkOpInternal { MK_IOP_AR = 0, MK_IOP_RS = 1, MK_IOP_AG = 2 };
 
@@ -49,7 +53,8 @@ struct MkWsHeader {
     uint64_t reduce_busy;   // SM cycles spent reducing ready tiles (sum over blocks)
     uint32_t err_site;      // which wait gave up (diagnostic)
     uint32_t err_index;     // the unit / tile it was waiting for (diagnostic)
-    uint32_t pad[(MK_WS_HEADER_BYTES - 64) / 4];
+    uint32_t acc_state;     // MK_ACC_*: set by every call, read by accumulate-mode calls
+    uint32_t pad[(MK_WS_HEADER_BYTES - 68) / 4];
 };
 static_assert(sizeof(MkWsHeader) == MK_WS_HEADER_BYTES, "workspace header size");
 

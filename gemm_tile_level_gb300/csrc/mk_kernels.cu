@@ -45,7 +45,7 @@ enum { ITEM_END = 0, ITEM_COMPUTE = 1, ITEM_REDUCE = 2 };
 enum {
     SITE_WORK_EMPTY = 1, SITE_WORK_FULL = 2, SITE_STAGE_EMPTY = 3, SITE_STAGE_FULL = 4,
     SITE_ACC_EMPTY = 5, SITE_ACC_FULL = 6, SITE_FLAG = 7, SITE_DRAIN = 8, SITE_GATE = 9,
-    SITE_WATCHDOG = 10, SITE_CLAIMED = 11
+    SITE_WATCHDOG = 10, SITE_CLAIMED = 11, SITE_ACC_STATE = 12
 };
 
 constexpr int WQ = 4;          // depth of the per-block work queue
@@ -149,6 +149,20 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool v) {
     return r != 0u;
 }
 
+// Named-barrier OR over n threads.
+__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0u;
+}
+
 // Grouped raster over a tiles_m x tiles_n grid: groups of G rows walked column by column, so
 // that concurrently computed tiles share A rows and B columns in L2.
 __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, int &tm, int &tn) {
@@ -239,7 +253,7 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
     uint32_t gate_seen = 0xFFFFFFFFu;
     for (uint32_t spin = 0; spin != 0xFFFFFFFFu; ++spin) {
         if (global_abort(c)) return make_int2(ITEM_END, 0);
-        if (p.mode == MK_MODE_COMPUTE_ONLY) {
+        if (p.mode == MK_MODE_COMPUTE_ONLY || p.mode == MK_MODE_ACCUMULATE) {
             const uint32_t u = atomicAdd(&h->compute_next, 1u);
             if (u >= g.num_units) return make_int2(ITEM_END, 0);
             if (static_cast<int64_t>(u) == p.skip_unit) continue;
@@ -552,6 +566,72 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
     }
 }
 
+// ------------------------------------------------------------------ accumulate mode
+// The ReduceScatter design the pages give for one node (Table 3, "GEMM + ReduceScatter"): the
+// compute blocks themselves add each partial tile into the owner's fp32 buffer, here one fp32
+// accumulator tile per output tile in the workspace (laid out like a partial tile), with L2
+// reductions (red.add.v4.f32), so no partial tile is stored and read back and no reduce role
+// exists.  The order in which the P ranks' additions land is not fixed, so results are exact
+// for integer inputs and within rounding otherwise.  The block whose addition is the P-th
+// (atomic count per tile, acquire-release) converts the tile to the output and clears the
+// accumulator and the count for the next call.
+template <int BN>
+__device__ __forceinline__ void accumulate_partial(const MkParams &p, uint32_t tmem_acc, int lt, int warp, int lane) {
+    const int lq = warp & 3;
+    const int half = (warp - MK_EPI_WARP0) >> 2;
+    const int row = lq * 32 + lane;
+    float *tile = p.partials + static_cast<size_t>(lt) * (MK_BM * BN);
+    const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 64; ++cc) {
+        const int col0 = half * (BN / 2) + cc * 32;
+        uint32_t v[32];
+        if (p.num_kb == 0) break;   // nothing to add
+        tmem_ld32(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0), v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float *dst = tile + (static_cast<size_t>((col0 >> 2) + q) * MK_BM + row) * 4;
+            red_add_f4_hint(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                            __uint_as_float(v[4 * q + 3]), pol);
+        }
+    }
+}
+
+// After every epilogue thread has issued its additions for tile (tm, tn): count this rank's
+// contribution; the last contributor writes the tile's output and clears its accumulator.
+template <int BN>
+__device__ void finish_accumulate(const MkParams &p, const Ctx &c, int tm, int tn, int etid) {
+    const int lt = tm * p.tiles_n + tn;
+    bar_sync(1, MK_EPI_THREADS);   // all additions of this block issued (ordered before the release below)
+    bool last = false;
+    if (etid == 0) {
+        __threadfence();
+        last = atom_add_acq_rel_gpu(p.flags + lt, 1u) == static_cast<uint32_t>(p.P - 1);
+    }
+    last = bar_or(1, MK_EPI_THREADS, last);
+    if (!last) return;
+    __threadfence();
+    const int row = etid & (MK_BM - 1);
+    const int half = etid >> 7;
+    const int grow = tm * MK_BM + row;
+    float *tile = p.partials + static_cast<size_t>(lt) * (MK_BM * BN);
+#pragma unroll 2
+    for (int u = 0; u < BN / 16; ++u) {
+        const int g0 = 4 * u + 2 * half;
+        float4 *q0 = reinterpret_cast<float4 *>(tile) + static_cast<size_t>(g0) * MK_BM + row;
+        const float4 a = ld_cg_f4(q0), b = ld_cg_f4(q0 + MK_BM);
+        const int gcol = tn * BN + g0 * 4;
+        if (grow < p.M && gcol < p.N) store_out8(p, grow, gcol, a, b);
+        st_f4(q0, 0.f, 0.f, 0.f, 0.f);
+        st_f4(q0 + MK_BM, 0.f, 0.f, 0.f, 0.f);
+    }
+    bar_sync(1, MK_EPI_THREADS);
+    if (etid == 0) {
+        st_relaxed_gpu(p.flags + lt, 0u);
+        atomicAdd(&c.hdr->tiles_done, 1u);
+    }
+}
+
 // ------------------------------------------------------------------ split controller
 // The split controller (one thread of block 0).  It reads the progress counters every
 // ctrl_period_ns and publishes the number of reduce-role units.  Moving one reduce item from the
@@ -648,6 +728,9 @@ __device__ void finish_call(const MkParams &p, uint32_t epoch) {
         h->target_nr = 0;
         h->compute_busy = 0;
         h->reduce_busy = 0;
+        // the accumulator region holds zeros after an accumulate call that ran to the end; any
+        // other call leaves partial tiles (or an unfinished sum) there
+        h->acc_state = (p.mode == MK_MODE_ACCUMULATE && h->abort == 0) ? MK_ACC_CLEAN : MK_ACC_DIRTY;
         h->abort = 0;
         h->epoch = epoch;
         h->done_ctas = 0;
@@ -680,6 +763,14 @@ __device__ void init_barriers(SmemCtl<STAGES> &s, const MkParams &p, uint32_t fu
     uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
     if (e == 0u) e = 1u;
     s.epoch = e;
+    // an accumulate call needs a zeroed accumulator: refuse (no block does any work) when the
+    // last call on this workspace left partial tiles or an unfinished sum there
+    if (p.mode == MK_MODE_ACCUMULATE && ld_relaxed_gpu(&p.hdr->acc_state) == MK_ACC_DIRTY) {
+        if (atomicCAS(&p.hdr->status, 0u, static_cast<uint32_t>(MK_ERR_INVALID_ARG)) == 0u)
+            p.hdr->err_site = SITE_ACC_STATE;
+        atomicExch(&p.hdr->abort, 1u);
+        s.abort = 1;
+    }
 }
 
 // ----------------------------------------------------------------- AllGather + GEMM helpers
@@ -983,7 +1074,11 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
             ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             if (!bar_and(1, MK_EPI_THREADS, ok)) break;
             tc_fence_after();
-            store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
+            const bool accumulate = p.mode == MK_MODE_ACCUMULATE;
+            if (accumulate)
+                accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, warp, lane);
+            else
+                store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[acc]));
@@ -991,10 +1086,15 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
                 acc = 0;
                 aphase ^= 1u;
             }
-            bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
-            if (etid == 0) {
-                st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
-                atomicAdd(&c.hdr->units_done, 1u);
+            if (accumulate) {
+                finish_accumulate<BN>(p, c, tm, tn, etid);
+                if (etid == 0) atomicAdd(&c.hdr->units_done, 1u);
+            } else {
+                bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
+                if (etid == 0) {
+                    st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
+                    atomicAdd(&c.hdr->units_done, 1u);
+                }
             }
         } else {
             int tm, tn;
@@ -1248,9 +1348,12 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             if (!bar_and(1, MK_EPI_THREADS, ok)) break;
             tc_fence_after();
+            const bool accumulate = p.mode == MK_MODE_ACCUMULATE;
             if (exists) {
                 if (p.op == MK_IOP_AG)
                     store_output_tile<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, tm, tn, warp, lane);
+                else if (accumulate)
+                    accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, warp, lane);
                 else
                     store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
             }
@@ -1264,10 +1367,16 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                 acc = 0;
                 aphase ^= 1u;
             }
-            bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
-            if (etid == 0) {
-                if (exists && p.op != MK_IOP_AG) st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
-                atomicAdd(&c.hdr->units_done, 1u);
+            if (accumulate) {
+                if (exists) finish_accumulate<BN>(p, c, tm, tn, etid);
+                if (etid == 0) atomicAdd(&c.hdr->units_done, 1u);
+            } else {
+                bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
+                if (etid == 0) {
+                    if (exists && p.op != MK_IOP_AG)
+                        st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
+                    atomicAdd(&c.hdr->units_done, 1u);
+                }
             }
         } else {
             if (p.op == MK_IOP_AG) {

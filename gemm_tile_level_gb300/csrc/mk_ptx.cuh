@@ -369,6 +369,20 @@ __device__ __forceinline__ void discard_l2_line(const void *p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
+// Four fp32 additions performed in L2 (relaxed, gpu scope), with an L2 eviction-priority policy.
+__device__ __forceinline__ void red_add_f4_hint(float *p, float a, float b, float c, float d, uint64_t policy) {
+    asm volatile("red.relaxed.gpu.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a),
+                 "f"(b), "f"(c), "f"(d), "l"(policy)
+                 : "memory");
+}
+
+// Atomic add with acquire-release semantics at gpu scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Streaming 16-byte load that is cached in L2 only.
 __device__ __forceinline__ float4 ld_cg_f4(const float4 *p) {
     float4 v;

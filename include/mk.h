@@ -64,7 +64,15 @@ typedef enum { MK_OP_ALLREDUCE = 0, MK_OP_REDUCESCATTER = 1, MK_OP_ALLGATHER_GEM
 typedef enum {
     MK_SPLIT_ADAPTIVE = 0, /* on-GPU controller publishes the reduce-role block count at run time */
     MK_SPLIT_STATIC = 1,   /* comm_sms blocks hold the communication role for the whole call */
-    MK_SPLIT_UNFUSED = 2   /* baseline: one kernel computes every per-rank tile, a second kernel reduces */
+    MK_SPLIT_UNFUSED = 2,  /* baseline: one kernel computes every per-rank tile, a second kernel reduces */
+    MK_SPLIT_ACCUMULATE = 3 /* no reduce role: compute blocks add their partial tiles into one fp32
+                               accumulator tile per output tile with L2 reductions; the last of the
+                               P contributions writes the output (AllReduce and ReduceScatter only).
+                               The order of the additions is not fixed: exact for integer inputs,
+                               within rounding otherwise.  Needs a workspace whose accumulator
+                               region is zero: freshly zeroed, or last used by an accumulate call
+                               that succeeded; otherwise the call does nothing and
+                               mk_status_check reports MK_ERR_INVALID_ARG (zero it again). */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */
