@@ -29,6 +29,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr double kRasterL2Budget = 32e6;   // tile-major: bytes of A rows (all ranks) resident per band
 constexpr double kBandL2Budget = 24e6;     // rank-major: bytes of one rank's A rows resident per band
 constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-major from this M on
+constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
 constexpr double kTailL2Bytes = 64e6;        // partial tiles that stay in L2 until the end of a call
 constexpr double kTailL2Bandwidth = 12e12;   // bytes/s the grid streams from L2
 constexpr double kHbmEfficiency = 0.8;       // streaming fraction of the nominal HBM bandwidth
@@ -253,12 +254,21 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     // Rank-major bands pay off once there are several bands; a short M has a single band, whose
     // tiles would all complete in the last 1/P of the GEMM, so it keeps the tile-major order.
     p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : (o.flags & MK_FLAG_RANK_MAJOR) ? 1 : (M >= kRankMajorMinRows);
-    // accumulate mode wants the P ranks of a tile close together in time, so that the tile's
-    // accumulator stays in L2 across its P additions
-    if (o.split_mode == MK_SPLIT_ACCUMULATE && !(o.flags & MK_FLAG_RANK_MAJOR)) p.rank_major = 0;
+    const int64_t order_rows = pair ? g.pair_tiles_m : g.tiles_m;
     p.raster_group = o.raster_group > 0 ? o.raster_group
-                                        : auto_raster_group(pair, P, Kr, pair ? g.pair_tiles_m : g.tiles_m,
-                                                            p.rank_major != 0);
+                                        : auto_raster_group(pair, P, Kr, order_rows, p.rank_major != 0);
+    if (o.split_mode == MK_SPLIT_ACCUMULATE) {
+        // Accumulate mode: rank-major bands sized so that the band's fp32 accumulator tiles stay
+        // in L2 while the P ranks add into them one after the other (the tile-major order has
+        // the P ranks of a tile add to the same lines at the same time)
+        p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : 1;
+        if (o.raster_group <= 0) {
+            const double row_bytes = static_cast<double>(pair ? 2 * MK_BM : MK_BM) * g.tiles_n * g.bn * 4.0;
+            int64_t band = static_cast<int64_t>(kAccumulatorL2Budget / row_bytes);
+            if (!p.rank_major) band = auto_raster_group(pair, P, Kr, order_rows, false);
+            p.raster_group = static_cast<int32_t>(band < 1 ? 1 : band > order_rows ? order_rows : band);
+        }
+    }
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;

@@ -576,14 +576,18 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
 // (atomic count per tile, acquire-release) converts the tile to the output and clears the
 // accumulator and the count for the next call.
 template <int BN>
-__device__ __forceinline__ void accumulate_partial(const MkParams &p, uint32_t tmem_acc, int lt, int warp, int lane) {
+__device__ __forceinline__ void accumulate_partial(const MkParams &p, uint32_t tmem_acc, int lt, int r, int warp,
+                                                   int lane) {
     const int lq = warp & 3;
     const int half = (warp - MK_EPI_WARP0) >> 2;
     const int row = lq * 32 + lane;
     float *tile = p.partials + static_cast<size_t>(lt) * (MK_BM * BN);
     const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+    // ranks of one tile often run at the same time: each starts on a different 32-column chunk,
+    // so that their additions to the same lines do not all arrive together
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 64; ++cc) {
+    for (int i = 0; i < BN / 64; ++i) {
+        const int cc = (i + r) % (BN / 64);
         const int col0 = half * (BN / 2) + cc * 32;
         uint32_t v[32];
         if (p.num_kb == 0) break;   // nothing to add
@@ -1076,7 +1080,7 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
             tc_fence_after();
             const bool accumulate = p.mode == MK_MODE_ACCUMULATE;
             if (accumulate)
-                accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, warp, lane);
+                accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, r, warp, lane);
             else
                 store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
             tc_fence_before();
@@ -1353,7 +1357,7 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                 if (p.op == MK_IOP_AG)
                     store_output_tile<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, tm, tn, warp, lane);
                 else if (accumulate)
-                    accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, warp, lane);
+                    accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, r, warp, lane);
                 else
                     store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
             }

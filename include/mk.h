@@ -121,6 +121,9 @@ typedef enum {
  *                     about 24 MB.  In tile-major order the P ranks of each
  *                     tile are computed back to back and 0 sizes the band so
  *                     that the A rows of all P ranks take about 32 MB.
+ *                     MK_SPLIT_ACCUMULATE computes rank-major unless
+ *                     MK_FLAG_TILE_MAJOR is set, and 0 sizes its bands so that
+ *                     a band's fp32 accumulator tiles take about 36 MB.
  *   reduce_split    : the reduction of each output tile is cut into this many
  *                     column slices, each claimed as its own item, so that the
  *                     final reductions of a shape with few tiles spread over

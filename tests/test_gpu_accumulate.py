@@ -47,8 +47,9 @@ def test_integer_bit_exact(P, M, N, Kr, out):
     ref = gu.rounded_reference(oracle.allreduce(A, B), out == "bf16")
     code = mk.MK_BF16 if out == "bf16" else mk.MK_F32
     for tiles in TILES:
-        C = gu.call_ar(Ad, Bd, code, opts=acc_opts(tiles))
-        gu.assert_bit_exact(gu.host_values(C), ref)
+        for fl, band in ((0, 0), (mk.MK_FLAG_TILE_MAJOR, 0), (0, 1)):   # rank-major (default), tile-major, 1-row bands
+            C = gu.call_ar(Ad, Bd, code, opts=acc_opts(tiles, flags=fl, raster_group=band))
+            gu.assert_bit_exact(gu.host_values(C), ref)
 
 
 @pytest.mark.parametrize("P,M,N,Kr", SHAPES)
