@@ -334,6 +334,8 @@ def gpu_arm(args, wl, ranks):
     with torch.cuda.stream(stream):
         prob = Problem(wl, torch, api, mk)
         opts = split_opts(api, mk, args.split, args.comm_sms)
+        if args.split == "accumulate":
+            prob.ws.zero_()
         for _ in range(args.warmup):
             mk.check(prob.call(opts, stream))
         mk.check(mk.mk_status_check(prob.ws, stream))
@@ -372,6 +374,16 @@ def gpu_arm(args, wl, ranks):
             n = max(3, min(args.steps, 20))
             unfused = {"value": wl.flops / (tot / n * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "ms_per_step": tot / n, "launches_per_step": 2}
+
+        # ---------------- the accumulate variant (no reduce role) on the same inputs (context)
+        accumulate = None
+        if args.split != "accumulate" and not args.no_baseline:
+            prob.ws.zero_()   # the other modes leave partial tiles where its accumulators go
+            n = max(3, min(args.steps, 20))
+            tot, _ = time_launches(torch, prob, split_opts(api, mk, "accumulate", 0), n, 2, stream)
+            accumulate = {"value": wl.flops / (tot / n * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "ms_per_step": tot / n, "launches_per_step": 1,
+                          "note": "MK_SPLIT_ACCUMULATE: L2 reductions into fp32 accumulators, order of additions not fixed"}
 
     peaks, peak_src = load_peaks()
     kernel_ms = statistics.mean(per_launch)
@@ -417,7 +429,7 @@ def gpu_arm(args, wl, ranks):
             "gpu_launches": args.steps * (2 if args.split == "unfused" else 1),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
-            "unfused_baseline": unfused}
+            "unfused_baseline": unfused, "accumulate_variant": accumulate}
     print(json.dumps(line), flush=True)
 
 
@@ -481,10 +493,13 @@ def sweep(args):
             lo, step = (1, args.sweep_stride) if _EXTRA_FLAGS & 2 else (2, max(2, args.sweep_stride))
             static = {nr: ms(split_opts(api, mk, "static", nr)) for nr in range(lo, S - 1, step)}
             unf = ms(split_opts(api, mk, "unfused", 0))
+            prob.ws.zero_()
+            acc = ms(split_opts(api, mk, "accumulate", 0))
             best_nr = min(static, key=static.get)
             rec = {"M": M, "adaptive_ms": adaptive, "best_static_ms": static[best_nr],
                    "best_static_comm_sms": best_nr, "adaptive_over_best_static": adaptive / static[best_nr],
                    "unfused_ms": unf, "fused_over_unfused": adaptive / unf,
+                   "accumulate_ms": acc, "accumulate_over_unfused": acc / unf,
                    "adaptive_tflops": wl.flops / (adaptive * 1e-3) / 1e12,
                    "static_ms": {str(k): v for k, v in static.items()}}
             results.append(rec)
