@@ -71,7 +71,7 @@ struct Cfg2 {
     static constexpr int B_BOX_BYTES = 64 * MK_BK * 2;
     static constexpr int B_BOXES = BN / 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BOXES * B_BOX_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 6 : 8;
+    static constexpr int STAGES = (BN == 256) ? 7 : 8;
     static constexpr int TMEM_COLS = ACC * BN;
     static constexpr int TILE_FLOATS = MK_BM * BN;
     static constexpr uint32_t IDESC = idesc_bf16_f32(2 * MK_BM, BN);
