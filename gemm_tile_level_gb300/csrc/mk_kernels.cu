@@ -725,6 +725,8 @@ __device__ void finish_call(const MkParams &p, uint32_t epoch) {
     const uint32_t prev = atomicAdd(&h->done_ctas, 1u);
     if (prev == gridDim.x - 1) {
         __threadfence();
+        const uint32_t tiles_done = ld_relaxed_gpu(&h->tiles_done);
+        const bool aborted = ld_relaxed_gpu(&h->abort) != 0u;
         h->compute_next = 0;
         h->reduce_next = 0;
         h->units_done = 0;
@@ -732,9 +734,19 @@ __device__ void finish_call(const MkParams &p, uint32_t epoch) {
         h->target_nr = 0;
         h->compute_busy = 0;
         h->reduce_busy = 0;
+        // accumulate mode has no waits to run out: a tile whose P contributions did not all
+        // arrive shows up here as a missing output tile
+        bool complete = true;
+        if (p.mode == MK_MODE_ACCUMULATE && !aborted && tiles_done != static_cast<uint32_t>(p.num_tiles)) {
+            complete = false;
+            if (atomicCAS(&h->status, 0u, static_cast<uint32_t>(MK_ERR_INTERNAL)) == 0u) {
+                h->err_site = SITE_ACC_STATE;
+                h->err_index = tiles_done;
+            }
+        }
         // the accumulator region holds zeros after an accumulate call that ran to the end; any
         // other call leaves partial tiles (or an unfinished sum) there
-        h->acc_state = (p.mode == MK_MODE_ACCUMULATE && h->abort == 0) ? MK_ACC_CLEAN : MK_ACC_DIRTY;
+        h->acc_state = (p.mode == MK_MODE_ACCUMULATE && !aborted && complete) ? MK_ACC_CLEAN : MK_ACC_DIRTY;
         h->abort = 0;
         h->epoch = epoch;
         h->done_ctas = 0;

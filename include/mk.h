@@ -72,7 +72,9 @@ typedef enum {
                                within rounding otherwise.  Needs a workspace whose accumulator
                                region is zero: freshly zeroed, or last used by an accumulate call
                                that succeeded; otherwise the call does nothing and
-                               mk_status_check reports MK_ERR_INVALID_ARG (zero it again). */
+                               mk_status_check reports MK_ERR_INVALID_ARG (zero it again).
+                               A tile that did not receive all P contributions is reported
+                               as MK_ERR_INTERNAL when the call ends. */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */

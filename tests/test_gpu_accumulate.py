@@ -102,6 +102,22 @@ def test_workspace_dirtied_by_another_mode_is_refused_until_zeroed():
     gu.assert_bit_exact(gu.host_values(gu.call_ar(Ad, Bd, mk.MK_F32, ws=ws, opts=acc_opts())), ref)
 
 
+def test_missing_contribution_is_reported_and_dirties_the_workspace():
+    # accumulate mode has no waits: a compute unit that never runs (host-side injection) leaves
+    # its tile unwritten, which the last block out reports as an internal error
+    P, M, N, Kr = 4, 512, 512, 128
+    wl = ig.Workload("acc_skip", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32", seed=4)
+    A, B, Ad, Bd = gu.upload(wl)
+    ws = api.workspace(mk.MK_OP_ALLREDUCE, P, M, N, Kr)
+    C, st = api.gemm_allreduce(Ad, Bd, mk.MK_F32, ws=ws, opts=acc_opts(skip_unit=5))
+    assert st == mk.MK_OK
+    assert mk.mk_status_check(ws) == mk.MK_ERR_INTERNAL
+    C, st = api.gemm_allreduce(Ad, Bd, mk.MK_F32, ws=ws, opts=acc_opts())
+    assert mk.mk_status_check(ws) == mk.MK_ERR_INVALID_ARG      # the accumulators are not known to be zero
+    ws.zero_()
+    gu.assert_bit_exact(gu.host_values(gu.call_ar(Ad, Bd, mk.MK_F32, ws=ws, opts=acc_opts())), oracle.allreduce(A, B))
+
+
 def test_reducescatter_full_size_sampled():
     wl = ig.WORKLOADS["rs_p8_m16384_n8192_k1024"]
     A, B, Ad, Bd = gu.upload(wl)
