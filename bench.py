@@ -272,6 +272,8 @@ def split_opts(api, mk, split: str, comm_sms: int):
         return api.make_opts(mk.MK_SPLIT_STATIC, comm_sms=comm_sms, **kw)
     if split == "accumulate":
         return api.make_opts(mk.MK_SPLIT_ACCUMULATE, **kw)
+    if split == "chained":
+        return api.make_opts(mk.MK_SPLIT_CHAINED, **kw)
     return api.make_opts(mk.MK_SPLIT_UNFUSED, **kw)
 
 
@@ -580,7 +582,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mk", "reference"], default="mk")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--split", choices=["adaptive", "static", "unfused", "accumulate"], default="adaptive")
+    ap.add_argument("--split", choices=["adaptive", "static", "unfused", "accumulate", "chained"], default="adaptive")
     ap.add_argument("--comm-sms", type=int, default=0)
     ap.add_argument("--tiles", choices=["pair", "single"], default="pair",
                     help="SM-pair 256 x BN compute tiles (default) or one-SM 128 x BN tiles")

@@ -137,7 +137,7 @@ mk_status encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t col
 
 
 mk_status check_opts(const mk_opts *o) {
-    if (o->split_mode < MK_SPLIT_ADAPTIVE || o->split_mode > MK_SPLIT_ACCUMULATE)
+    if (o->split_mode < MK_SPLIT_ADAPTIVE || o->split_mode > MK_SPLIT_CHAINED)
         return fail(MK_ERR_INVALID_ARG, "split_mode %d out of range", o->split_mode);
     if (o->split_mode == MK_SPLIT_STATIC && o->comm_sms < 1)
         return fail(MK_ERR_INVALID_ARG, "static split needs comm_sms >= 1");
@@ -257,10 +257,11 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     const int64_t order_rows = pair ? g.pair_tiles_m : g.tiles_m;
     p.raster_group = o.raster_group > 0 ? o.raster_group
                                         : auto_raster_group(pair, P, Kr, order_rows, p.rank_major != 0);
-    if (o.split_mode == MK_SPLIT_ACCUMULATE) {
-        // Accumulate mode: rank-major bands sized so that the band's fp32 accumulator tiles stay
-        // in L2 while the P ranks add into them one after the other (the tile-major order has
-        // the P ranks of a tile add to the same lines at the same time)
+    if (o.split_mode == MK_SPLIT_ACCUMULATE || o.split_mode == MK_SPLIT_CHAINED) {
+        // Accumulate and chained modes: rank-major bands sized so that the band's fp32
+        // accumulator (running-sum) tiles stay in L2 while the P ranks add into them one after
+        // the other (the tile-major order has the P ranks of a tile meet on the same lines at
+        // the same time)
         p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : 1;
         if (o.raster_group <= 0) {
             const double row_bytes = static_cast<double>(pair ? 2 * MK_BM : MK_BM) * g.tiles_n * g.bn * 4.0;
@@ -294,8 +295,8 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
         if (e != cudaSuccess) return fail_cuda(e, "launch of the reduce kernel");
         return MK_OK;
     }
-    if (o.split_mode == MK_SPLIT_ACCUMULATE) {
-        p.mode = MK_MODE_ACCUMULATE;
+    if (o.split_mode == MK_SPLIT_ACCUMULATE || o.split_mode == MK_SPLIT_CHAINED) {
+        p.mode = o.split_mode == MK_SPLIT_ACCUMULATE ? MK_MODE_ACCUMULATE : MK_MODE_CHAINED;
         e = mk_launch_persistent(p, g.bn, pair, S, s);
         return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the accumulating GEMM kernel");
     }
@@ -335,8 +336,9 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     if (opts_in) o = *opts_in;
     mk_status st = check_opts(&o);
     if (st != MK_OK) return st;
-    if (o.split_mode == MK_SPLIT_ACCUMULATE)
-        return fail(MK_ERR_INVALID_ARG, "MK_SPLIT_ACCUMULATE applies to GEMM + AllReduce and GEMM + ReduceScatter");
+    if (o.split_mode == MK_SPLIT_ACCUMULATE || o.split_mode == MK_SPLIT_CHAINED)
+        return fail(MK_ERR_INVALID_ARG, "MK_SPLIT_ACCUMULATE and MK_SPLIT_CHAINED apply to GEMM + AllReduce and "
+                    "GEMM + ReduceScatter");
     if (N % 8 || K % 8)
         return fail(MK_ERR_UNSUPPORTED_SHAPE, "N=%lld and K=%lld must be multiples of 8", (long long)N, (long long)K);
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "dimension above 2^31-1");

@@ -29,7 +29,8 @@ enum MkMode {
     MK_MODE_STATIC = 1,     // fused, fixed split
     MK_MODE_COMPUTE_ONLY = 2, // unfused baseline: the GEMM kernel
     MK_MODE_COMM_ONLY = 3,    // unfused AllGather baseline: the copy kernel
-    MK_MODE_ACCUMULATE = 4    // compute blocks add their partial tiles into one fp32 accumulator
+    MK_MODE_ACCUMULATE = 4,   // compute blocks add their partial tiles into one fp32 accumulator
+    MK_MODE_CHAINED = 5       // compute blocks fold their partial tile into a rank-ordered running sum
 };
 
 // MkWsHeader::acc_state: whether the accumulator region is known to hold zeros

@@ -253,7 +253,7 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
     uint32_t gate_seen = 0xFFFFFFFFu;
     for (uint32_t spin = 0; spin != 0xFFFFFFFFu; ++spin) {
         if (global_abort(c)) return make_int2(ITEM_END, 0);
-        if (p.mode == MK_MODE_COMPUTE_ONLY || p.mode == MK_MODE_ACCUMULATE) {
+        if (p.mode == MK_MODE_COMPUTE_ONLY || p.mode == MK_MODE_ACCUMULATE || p.mode == MK_MODE_CHAINED) {
             const uint32_t u = atomicAdd(&h->compute_next, 1u);
             if (u >= g.num_units) return make_int2(ITEM_END, 0);
             if (static_cast<int64_t>(u) == p.skip_unit) continue;
@@ -634,6 +634,92 @@ __device__ void finish_accumulate(const MkParams &p, const Ctx &c, int tm, int t
         st_relaxed_gpu(p.flags + lt, 0u);
         atomicAdd(&c.hdr->tiles_done, 1u);
     }
+}
+
+// ------------------------------------------------------------------ chained mode
+// The rank-ordered sum built by the compute blocks themselves: the epilogue of unit (tile, r)
+// waits for flag[tile][r-1] (rank r-1 has folded its partial in), adds its accumulator to the
+// running sum S = ((p_0 + p_1) + ...) + p_{r-1} held in rank 0's partial tile, and stores the
+// new sum, or for r = P-1 writes the output.  The fp32 additions are the ones the reduce role
+// makes, in the same order, so the result is the same bit for bit; no reduce role is needed and
+// a partial tile is read back only as the running sum, which the rank-major bands keep in L2.
+// False if the wait for the predecessor gave up (the grid is aborting).
+template <int BN>
+__device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc, int r, int tm, int tn, int warp,
+                              int lane, int etid, uint32_t epoch) {
+    const int lt = tm * p.tiles_n + tn;
+    bool ok = true;
+    if (r > 0 && etid < 32) {
+        // lane 0 acquires the predecessor's flag (one flag: no need for the whole warp)
+        const uint32_t *f = p.flags + static_cast<size_t>(lt) * p.P + (r - 1);
+        int stop = 0;
+        if (lane == 0) {
+            uint64_t t0 = 0;
+            for (uint32_t polls = 0; ld_acquire_gpu(f) != epoch; ++polls) {
+                if (*c.s_abort) { stop = 1; break; }
+                if (t0 == 0) t0 = globaltimer();
+                if ((polls & 15u) == 15u) {
+                    if (global_abort(c)) { stop = 1; break; }
+                    if (globaltimer() - t0 > c.timeout_ns || polls > (1u << 30)) {
+                        raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, static_cast<uint32_t>(lt * p.P + r - 1));
+                        stop = 1;
+                        break;
+                    }
+                }
+                __nanosleep(32);
+            }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
+    }
+    ok = bar_and(1, MK_EPI_THREADS, ok);   // orders every thread's loads of S after the acquire
+    if (!ok) return false;
+    const int lq = warp & 3;
+    const int half = (warp - MK_EPI_WARP0) >> 2;
+    const int row = lq * 32 + lane;
+    const int grow = tm * MK_BM + row;
+    const bool last = r == p.P - 1;
+    float *S = partial_tile<BN>(p, 0, lt);
+    const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 64; ++cc) {
+        const int col0 = half * (BN / 2) + cc * 32;
+        uint32_t v[32];
+        if (p.num_kb > 0) {
+            tmem_ld32(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0), v);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0u;
+        }
+        float4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            x[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                               __uint_as_float(v[4 * q + 3]));
+        float *base = S + (static_cast<size_t>(col0 >> 2) * MK_BM + row) * 4;
+        if (r > 0) {
+            float4 sv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sv[q] = ld_cg_f4(reinterpret_cast<const float4 *>(base + q * MK_BM * 4));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
+                x[q].x = sv[q].x + x[q].x; x[q].y = sv[q].y + x[q].y;
+                x[q].z = sv[q].z + x[q].z; x[q].w = sv[q].w + x[q].w;
+            }
+        }
+        if (last) {
+            if (grow < p.M) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int gcol = tn * BN + col0 + 8 * q;
+                    if (gcol < p.N) store_out8(p, grow, gcol, x[2 * q], x[2 * q + 1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) st_f4_hint(base + q * MK_BM * 4, x[q].x, x[q].y, x[q].z, x[q].w, pol);
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ split controller
@@ -1091,8 +1177,13 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
             if (!bar_and(1, MK_EPI_THREADS, ok)) break;
             tc_fence_after();
             const bool accumulate = p.mode == MK_MODE_ACCUMULATE;
+            const bool chained = p.mode == MK_MODE_CHAINED;
+            bool folded = true;
             if (accumulate)
                 accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, r, warp, lane);
+            else if (chained)
+                folded = chain_partial<BN>(p, c, tmem_base + static_cast<uint32_t>(acc * BN), r, tm, tn, warp, lane,
+                                           etid, epoch);
             else
                 store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
             tc_fence_before();
@@ -1107,9 +1198,10 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
                 if (etid == 0) atomicAdd(&c.hdr->units_done, 1u);
             } else {
                 bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
-                if (etid == 0) {
+                if (etid == 0 && folded) {
                     st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
                     atomicAdd(&c.hdr->units_done, 1u);
+                    if (chained && r == p.P - 1) atomicAdd(&c.hdr->tiles_done, 1u);
                 }
             }
         } else {
@@ -1365,11 +1457,16 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             if (!bar_and(1, MK_EPI_THREADS, ok)) break;
             tc_fence_after();
             const bool accumulate = p.mode == MK_MODE_ACCUMULATE;
+            const bool chained = p.mode == MK_MODE_CHAINED;
+            bool folded = true;
             if (exists) {
                 if (p.op == MK_IOP_AG)
                     store_output_tile<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, tm, tn, warp, lane);
                 else if (accumulate)
                     accumulate_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), lt, r, warp, lane);
+                else if (chained)
+                    folded = chain_partial<BN>(p, c, tmem_base + static_cast<uint32_t>(acc * BN), r, tm, tn, warp,
+                                               lane, etid, epoch);
                 else
                     store_partial<BN>(p, tmem_base + static_cast<uint32_t>(acc * BN), r, lt, warp, lane);
             }
@@ -1388,10 +1485,11 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                 if (etid == 0) atomicAdd(&c.hdr->units_done, 1u);
             } else {
                 bar_sync(1, MK_EPI_THREADS);   // every store of this partial tile has been issued
-                if (etid == 0) {
+                if (etid == 0 && folded) {
                     if (exists && p.op != MK_IOP_AG)
                         st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + r, epoch);
                     atomicAdd(&c.hdr->units_done, 1u);
+                    if (exists && chained && r == p.P - 1) atomicAdd(&c.hdr->tiles_done, 1u);
                 }
             }
         } else {

@@ -34,6 +34,7 @@ MK_SPLIT_ADAPTIVE = 0
 MK_SPLIT_STATIC = 1
 MK_SPLIT_UNFUSED = 2
 MK_SPLIT_ACCUMULATE = 3
+MK_SPLIT_CHAINED = 4
 
 MK_FLAG_KEEP_PARTIALS = 1
 MK_FLAG_SINGLE_SM_TILES = 2

@@ -65,7 +65,7 @@ typedef enum {
     MK_SPLIT_ADAPTIVE = 0, /* on-GPU controller publishes the reduce-role block count at run time */
     MK_SPLIT_STATIC = 1,   /* comm_sms blocks hold the communication role for the whole call */
     MK_SPLIT_UNFUSED = 2,  /* baseline: one kernel computes every per-rank tile, a second kernel reduces */
-    MK_SPLIT_ACCUMULATE = 3 /* no reduce role: compute blocks add their partial tiles into one fp32
+    MK_SPLIT_ACCUMULATE = 3, /* no reduce role: compute blocks add their partial tiles into one fp32
                                accumulator tile per output tile with L2 reductions; the last of the
                                P contributions writes the output (AllReduce and ReduceScatter only).
                                The order of the additions is not fixed: exact for integer inputs,
@@ -75,6 +75,11 @@ typedef enum {
                                mk_status_check reports MK_ERR_INVALID_ARG (zero it again).
                                A tile that did not receive all P contributions is reported
                                as MK_ERR_INTERNAL when the call ends. */
+    MK_SPLIT_CHAINED = 4    /* no reduce role: the compute block of (tile, rank r) waits for rank
+                               r-1's release, adds its partial tile to the running sum of ranks
+                               0..r-1 and stores it (rank P-1 writes the output).  The same fp32
+                               additions in the same order as the reduce role, so the same bits
+                               (AllReduce and ReduceScatter only). */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */

@@ -1,0 +1,103 @@
+"""Chained mode (MK_SPLIT_CHAINED): the compute block of (tile, rank r) folds its partial tile
+into the running sum of ranks 0..r-1 after rank r-1's release, and rank P-1 writes the output.
+
+These are the reduce role's fp32 additions in the reduce role's order, so on random inputs the
+result must equal the adaptive, static and unfused results bit for bit, besides matching the
+oracle (bit-exact on integer inputs).  A withheld compute unit makes its successor's bounded
+wait run out.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputgen as ig
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gemm_tile_level_gb300 import api, mk
+    import gpu_util as gu
+
+TILES = ("pair", "single")
+
+
+def ch_opts(tiles="pair", **kw):
+    fl = kw.pop("flags", 0) | (mk.MK_FLAG_SINGLE_SM_TILES if tiles == "single" else 0)
+    return api.make_opts(mk.MK_SPLIT_CHAINED, flags=fl, **kw)
+
+
+SHAPES = [
+    (1, 1, 8, 8),
+    (2, 128, 256, 64),
+    (3, 130, 136, 72),
+    (5, 300, 520, 24),
+    (16, 64, 256, 64),
+    (7, 384, 768, 136),
+    (8, 1100, 1032, 200),
+]
+
+
+@pytest.mark.parametrize("P,M,N,Kr", SHAPES)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_integer_bit_exact(P, M, N, Kr, out):
+    wl = ig.Workload("ch", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, out, seed=P * 5 + M)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = gu.rounded_reference(oracle.allreduce(A, B), out == "bf16")
+    code = mk.MK_BF16 if out == "bf16" else mk.MK_F32
+    for tiles in TILES:
+        for fl, band in ((0, 0), (mk.MK_FLAG_TILE_MAJOR, 0), (0, 1)):
+            C = gu.call_ar(Ad, Bd, code, opts=ch_opts(tiles, flags=fl, raster_group=band))
+            gu.assert_bit_exact(gu.host_values(C), ref)
+
+
+@pytest.mark.parametrize("P,M,N,Kr", SHAPES)
+def test_random_same_bits_as_the_reduce_role(P, M, N, Kr):
+    wl = ig.Workload("ch", "allreduce", P, M, N, Kr, ig.normal(1.0), ig.normal(1.0 / (P * Kr)), "f32", seed=6)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = oracle.allreduce(A, B)
+    for tiles in TILES:
+        fl = mk.MK_FLAG_SINGLE_SM_TILES if tiles == "single" else 0
+        want = gu.call_ar(Ad, Bd, mk.MK_F32, opts=api.make_opts(mk.MK_SPLIT_UNFUSED, flags=fl))
+        got = gu.call_ar(Ad, Bd, mk.MK_F32, opts=ch_opts(tiles))
+        gu.check_tolerance(gu.host_values(got), ref, out_bf16=False)
+        assert torch.equal(got, want)
+
+
+def test_reducescatter_and_distinct_outputs():
+    P, M, N, Kr = 4, 512, 520, 96
+    wl = ig.Workload("ch_rs", "reducescatter", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16", seed=3)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = gu.rounded_reference(oracle.allreduce(A, B), True)
+    for tiles in TILES:
+        shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts(tiles))
+        gu.assert_bit_exact(np.concatenate([gu.host_values(s) for s in shards]), ref)
+    Cs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    gu.call_ar(Ad, Bd, mk.MK_BF16, C=Cs, opts=ch_opts())
+    for c in Cs:
+        gu.assert_bit_exact(gu.host_values(c), ref)
+
+
+def test_full_size_same_bits_as_the_reduce_role():
+    wl = ig.WORKLOADS["ar_mlp_down_p8_m8192_n8192_k3584"]
+    A, B, Ad, Bd = gu.upload(wl)
+    ws = api.workspace(mk.MK_OP_ALLREDUCE, wl.P, wl.M, wl.N, wl.Kr)
+    want = gu.call_ar(Ad, Bd, mk.MK_BF16, ws=ws)
+    got = gu.call_ar(Ad, Bd, mk.MK_BF16, ws=ws, opts=ch_opts())
+    assert torch.equal(got, want)
+    rows, cols = gu.sample_indices(wl.M, wl.N, 2048)
+    rms = float(np.sqrt(np.mean(oracle.allreduce_rows(A, B, 0, 2) ** 2)))
+    gu.check_tolerance(gu.host_values(got)[rows, cols], oracle.allreduce_at(A, B, rows, cols), out_bf16=True,
+                       rms_ref=rms)
+
+
+@pytest.mark.parametrize("tiles", TILES)
+def test_missing_unit_times_out_then_recovers(tiles):
+    wl = ig.Workload("ch_fault", "allreduce", 4, 512, 512, 128, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32")
+    A, B, Ad, Bd = gu.upload(wl)
+    ws = api.workspace(mk.MK_OP_ALLREDUCE, 4, 512, 512, 128)
+    C, st = api.gemm_allreduce(Ad, Bd, mk.MK_F32, ws=ws, opts=ch_opts(tiles, timeout_ns=20_000_000, skip_unit=5))
+    assert st == mk.MK_OK
+    assert mk.mk_status_check(ws) == mk.MK_ERR_TIMEOUT
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, ws=ws, opts=ch_opts(tiles))
+    gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
