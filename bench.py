@@ -387,6 +387,16 @@ def gpu_arm(args, wl, ranks):
                           "ms_per_step": tot / n, "launches_per_step": 1,
                           "note": "MK_SPLIT_ACCUMULATE: L2 reductions into fp32 accumulators, order of additions not fixed"}
 
+        # ---------------- the chained variant (compute blocks fold in rank order; same bits) (context)
+        chained = None
+        if args.split != "chained" and not args.no_baseline:
+            n = max(3, min(args.steps, 20))
+            tot, _ = time_launches(torch, prob, split_opts(api, mk, "chained", 0), n, 2, stream)
+            chained = {"value": wl.flops / (tot / n * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "ms_per_step": tot / n, "launches_per_step": 1,
+                       "note": "MK_SPLIT_CHAINED: each rank's epilogue adds its tile to the running sum of the ranks "
+                               "before it, in rank order (the reduce role's additions, same bits)"}
+
     peaks, peak_src = load_peaks()
     kernel_ms = statistics.mean(per_launch)
     achieved = wl.flops / (kernel_ms * 1e-3) / 1e12
@@ -431,7 +441,7 @@ def gpu_arm(args, wl, ranks):
             "gpu_launches": args.steps * (2 if args.split == "unfused" else 1),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
-            "unfused_baseline": unfused, "accumulate_variant": accumulate}
+            "unfused_baseline": unfused, "accumulate_variant": accumulate, "chained_variant": chained}
     print(json.dumps(line), flush=True)
 
 
@@ -559,11 +569,13 @@ def sweep(args):
             unf = ms(split_opts(api, mk, "unfused", 0))
             prob.ws.zero_()
             acc = ms(split_opts(api, mk, "accumulate", 0))
+            chn = ms(split_opts(api, mk, "chained", 0))
             best_nr = min(static, key=static.get)
             rec = {"M": M, "adaptive_ms": adaptive, "best_static_ms": static[best_nr],
                    "best_static_comm_sms": best_nr, "adaptive_over_best_static": adaptive / static[best_nr],
                    "unfused_ms": unf, "fused_over_unfused": adaptive / unf,
                    "accumulate_ms": acc, "accumulate_over_unfused": acc / unf,
+                   "chained_ms": chn, "chained_over_unfused": chn / unf,
                    "adaptive_tflops": wl.flops / (adaptive * 1e-3) / 1e12,
                    "static_ms": {str(k): v for k, v in static.items()}}
             results.append(rec)
