@@ -558,6 +558,10 @@ def sweep(args):
             prob = Problem(wl, torch, api, mk)
             steps, warm = args.sweep_steps, 2
 
+            # enough steps per point for about 20 ms of GPU time, so that short shapes are not noise
+            t1, _ = time_launches(torch, prob, split_opts(api, mk, "static", 2), 3, warm, stream)
+            steps = max(args.sweep_steps, int(20.0 / max(t1 / 3, 1e-3)))
+
             def ms(opts):
                 tot, _ = time_launches(torch, prob, opts, steps, warm, stream)
                 return tot / steps

@@ -246,7 +246,9 @@ __device__ bool wait_claimed(const Ctx &c, uint32_t need) {
     return false;
 }
 
-__device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, bool &exhausted) {
+// `target` is the published target_nr as the caller last read it (0 = unpublished): the producer
+// loads it while it streams the current unit, so that a claim costs one atomic round trip.
+__device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, bool &exhausted, uint32_t target) {
     MkWsHeader *h = c.hdr;
     const uint32_t P = static_cast<uint32_t>(p.P);
     uint64_t gate_t0 = 0;
@@ -276,10 +278,7 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
         }
         if (!exhausted) {
             int nr = p.static_nr;
-            if (p.mode == MK_MODE_ADAPTIVE) {
-                const uint32_t pub = ld_relaxed_gpu(&h->target_nr);   // target + 1, 0 = unpublished
-                nr = pub ? static_cast<int>(pub) - 1 : p.init_nr;
-            }
+            if (p.mode == MK_MODE_ADAPTIVE) nr = target ? static_cast<int>(target) - 1 : p.init_nr;   // target + 1
             if (static_cast<int>(g.role_index) < static_cast<int>(g.role_units) - nr) {
                 const uint32_t u = atomicAdd(&h->compute_next, 1u);
                 if (u < g.num_units) {
@@ -799,7 +798,8 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
                 }
             }
         }
-        __nanosleep(static_cast<unsigned>(p.ctrl_period_ns));
+        // once every unit is computed only the end of the call is left to notice: poll faster
+        __nanosleep(u / done_per_unit < num_units ? static_cast<unsigned>(p.ctrl_period_ns) : 200u);
     }
     h->trace_count = nrec;
 }
@@ -1036,12 +1036,14 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
     const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
     uint32_t pushed = 0, ring_free_at = 0;   // ring free once the epilogue has finished ring_free_at items
     bool last_reduce = false;
+    uint32_t target = 0;                     // adaptive split: target_nr as last read
     while (!stop) {
         // Reduce items are claimed at most one ahead of the one in progress, so that the last
         // items of a call spread over the grid instead of queueing behind a few blocks.
         if (last_reduce && !wait_epilogue_done(&s.epi_done, pushed - 1, c)) break;
-        const int2 it = claim_work(p, c, g, exhausted);
+        const int2 it = claim_work(p, c, g, exhausted, target);
         last_reduce = it.x == ITEM_REDUCE;
+        if (p.mode == MK_MODE_ADAPTIVE) target = ld_relaxed_gpu(&c.hdr->target_nr);   // used by the next claim
         if (!wait_bar<false>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
         s.items[wq] = it;
         mbar_arrive(smem_u32(&s.wfull[wq]));
@@ -1288,13 +1290,15 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
     uint32_t pushed = 0, ring_free_at = 0;
     bool last_reduce = false;
+    uint32_t target = 0;   // adaptive split: target_nr as last read (see claim_work)
     while (!stop) {
         int2 it;
         if (leader) {
             // reduce items: at most one claimed ahead of the one in progress (see run1_producer)
             if (last_reduce && !wait_epilogue_done(&s.epi_done, pushed - 1, c)) break;
-            it = claim_work(p, c, g, exhausted);
+            it = claim_work(p, c, g, exhausted, target);
             last_reduce = it.x == ITEM_REDUCE;
+            if (p.mode == MK_MODE_ADAPTIVE) target = ld_relaxed_gpu(&c.hdr->target_nr);   // used by the next claim
             if (!wait_bar<true>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
             s.items[wq] = it;
             st_cluster_v2(peer_items + 8u * wq, it.x, it.y);

@@ -103,8 +103,9 @@ typedef enum {
  *                     rounded up to whole pairs; with MK_FLAG_SINGLE_SM_TILES
  *                     roles are per SM and comm_sms <= grid size - 1).
  *                     MK_SPLIT_ADAPTIVE: initial target (0 = one role unit;
- *                     the controller then follows the backlog of ready tiles).
- *                     Ignored for MK_SPLIT_UNFUSED.
+ *                     the controller then weighs early against end-of-call
+ *                     reduction).  Ignored for MK_SPLIT_UNFUSED, MK_SPLIT_ACCUMULATE
+ *                     and MK_SPLIT_CHAINED, which have no reduce role.
  *   wait_timeout_ns : limit of every device-side wait (readiness flags,
  *                     pipeline barriers, the controller's progress watchdog);
  *                     0 = 2 s.  A wait that runs out sets MK_ERR_TIMEOUT.
