@@ -29,6 +29,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr double kRasterL2Budget = 32e6;   // tile-major: bytes of A rows (all ranks) resident per band
 constexpr double kBandL2Budget = 24e6;     // rank-major: bytes of one rank's A rows resident per band
 constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-major from this M on
+constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up to this M
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
 constexpr double kTailL2Bytes = 64e6;        // partial tiles that stay in L2 until the end of a call
 constexpr double kTailL2Bandwidth = 12e12;   // bytes/s the grid streams from L2
@@ -186,7 +187,11 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     if (ws_bytes < g.total)
         return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, g.total);
 
-    const bool pair = (o.flags & MK_FLAG_SINGLE_SM_TILES) == 0;
+    // Chained mode on a short M (one band of at most two 256-row tile rows) folds the ranks of a
+    // tile while several of them are still in flight; one-SM tiles give each rank pass twice
+    // the tiles, so that fewer folds wait on a predecessor (measured: 2-3 % faster at M <= 512).
+    const bool chained_short = o.split_mode == MK_SPLIT_CHAINED && M <= kChainedOneSmMaxRows;
+    const bool pair = (o.flags & MK_FLAG_SINGLE_SM_TILES) == 0 && !chained_short;
     int resident = 0;
     cudaError_t e = mk_max_persistent_ctas(g.bn, pair, &resident);
     if (e != cudaSuccess) return fail_cuda(e, "occupancy query");

@@ -682,6 +682,13 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
 #pragma unroll 1
     for (int cc = 0; cc < BN / 64; ++cc) {
         const int col0 = half * (BN / 2) + cc * 32;
+        float *base = S + (static_cast<size_t>(col0 >> 2) * MK_BM + row) * 4;
+        // the running sum's loads go out first, so that their L2 latency overlaps the TMEM load
+        float4 sv[8];
+        if (r > 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sv[q] = ld_cg_f4(reinterpret_cast<const float4 *>(base + q * MK_BM * 4));
+        }
         uint32_t v[32];
         if (p.num_kb > 0) {
             tmem_ld32(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0), v);
@@ -694,11 +701,7 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
         for (int q = 0; q < 8; ++q)
             x[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
                                __uint_as_float(v[4 * q + 3]));
-        float *base = S + (static_cast<size_t>(col0 >> 2) * MK_BM + row) * 4;
         if (r > 0) {
-            float4 sv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sv[q] = ld_cg_f4(reinterpret_cast<const float4 *>(base + q * MK_BM * 4));
 #pragma unroll
             for (int q = 0; q < 8; ++q) {   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
                 x[q].x = sv[q].x + x[q].x; x[q].y = sv[q].y + x[q].y;

@@ -79,7 +79,8 @@ typedef enum {
                                r-1's release, adds its partial tile to the running sum of ranks
                                0..r-1 and stores it (rank P-1 writes the output).  The same fp32
                                additions in the same order as the reduce role, so the same bits
-                               (AllReduce and ReduceScatter only). */
+                               (AllReduce and ReduceScatter only).  Uses one-SM tiles for
+                               M <= 512. */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */
