@@ -2,11 +2,14 @@
 """Benchmark of the fused GEMM + AllReduce hot path on one GB300 (or N independent replicas).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mk|reference]
-                  [--workload NAME] [--split adaptive|static|unfused] [--comm-sms n]
+                  [--workload NAME] [--split chained|adaptive|static|accumulate|unfused] [--comm-sms n]
   python bench.py --sweep        # SM-split sweep: adaptive vs every static split, per M
 
 A step is one mk_gemm_allreduce (or mk_gemm_reducescatter) call over one batch of seeded
-synthetic inputs already resident in HBM.  Prints ONE JSON line (rank 0).
+synthetic inputs already resident in HBM.  Prints ONE JSON line (rank 0).  The default split is
+the chained one (compute blocks fold each rank's partial tile into the rank-ordered running
+sum, the same bits as the reduce role); the line also carries, on the same inputs, the
+controller-driven role split, the unfused two-kernel baseline and the accumulate variant.
 
 Default workload: the row-parallel MLP down-projection GEMM + AllReduce, P=8 logical ranks,
 M=N=8192, K_per_rank=3584 (the large AllReduce shape the tensor-peak target refers to).  Its
@@ -387,6 +390,15 @@ def gpu_arm(args, wl, ranks):
                           "ms_per_step": tot / n, "launches_per_step": 1,
                           "note": "MK_SPLIT_ACCUMULATE: L2 reductions into fp32 accumulators, order of additions not fixed"}
 
+        # ---------------- the role split with the on-GPU controller (same bits) (context)
+        adaptive = None
+        if args.split != "adaptive" and not args.no_baseline:
+            n = max(3, min(args.steps, 20))
+            tot, _ = time_launches(torch, prob, split_opts(api, mk, "adaptive", 0), n, 2, stream)
+            adaptive = {"value": wl.flops / (tot / n * 1e-3) / 1e12, "unit": "TFLOP/s",
+                        "ms_per_step": tot / n, "launches_per_step": 1,
+                        "note": "MK_SPLIT_ADAPTIVE: compute and reduce roles, SM split set by the on-GPU controller"}
+
         # ---------------- the chained variant (compute blocks fold in rank order; same bits) (context)
         chained = None
         if args.split != "chained" and not args.no_baseline:
@@ -441,7 +453,8 @@ def gpu_arm(args, wl, ranks):
             "gpu_launches": args.steps * (2 if args.split == "unfused" else 1),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
-            "unfused_baseline": unfused, "accumulate_variant": accumulate, "chained_variant": chained}
+            "unfused_baseline": unfused, "adaptive_split": adaptive, "accumulate_variant": accumulate,
+            "chained_variant": chained}
     print(json.dumps(line), flush=True)
 
 
@@ -598,7 +611,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mk", "reference"], default="mk")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--split", choices=["adaptive", "static", "unfused", "accumulate", "chained"], default="adaptive")
+    ap.add_argument("--split", choices=["adaptive", "static", "unfused", "accumulate", "chained"], default="chained",
+                    help="chained (default): compute blocks fold each rank's tile into the rank-ordered running "
+                         "sum; adaptive / static: compute and reduce roles with the controller's or a fixed SM "
+                         "split (the same bits); accumulate: unordered L2 reductions; unfused: two kernels")
     ap.add_argument("--comm-sms", type=int, default=0)
     ap.add_argument("--tiles", choices=["pair", "single"], default="pair",
                     help="SM-pair 256 x BN compute tiles (default) or one-SM 128 x BN tiles")
