@@ -13,16 +13,24 @@
 // Two compute-tile shapes share everything but the MMA issue:
 //   mk_pair_kernel<BN>  (default): a cluster of two CTAs on two SMs computes one 256 x BN tile
 //       with tcgen05.mma.cta_group::2 (M=256); each CTA stages only its 128 rows of A and its
-//       BN/2 columns of B, so a 6-stage TMA ring fits and L2->SM bytes per FLOP drop by a third.
+//       BN/2 columns of B, so a 7-stage TMA ring fits and L2->SM bytes per FLOP drop by a third.
 //   mk_persistent_kernel<BN>: one CTA computes a 128 x BN tile with cta_group::1.
 // Warp roles in a block (352 threads):
 //   warp 0   : work scheduler (pair: the even CTA claims for both) and TMA producer
 //   warp 1   : one thread issues tcgen05.mma into one of two TMEM accumulators (pair: even CTA)
 //   warps 2-9: tcgen05.ld the accumulator, store the fp32 partial tile of rank r into rank r's
 //              workspace partition with coalesced 512-byte warp stores, release flag[tile][r];
-//              or, for a reduce item, acquire flag[tile][0..P-1], stream the P partials with
-//              16-byte L2-only loads, sum them in rank order 0..P-1 and write C or the shard
+//              or, for a reduce item, acquire flag[tile][0..P-1], stream the P partials through
+//              the idle TMA ring with bulk copies, sum them in rank order 0..P-1 and write C or
+//              the shard
 //   warp 10  : the split controller (block 0, adaptive mode)
+//
+// Two more ways to form the sum use the compute blocks alone (no reduce role):
+//   chained    : the epilogue of (tile, r) acquires flag[tile][r-1], adds its accumulator to the
+//                running sum of ranks 0..r-1 and stores it (rank P-1 writes the output): the
+//                reduce role's additions in its order, so the same bits;
+//   accumulate : the epilogue adds its accumulator into one fp32 tile with L2 reductions, and
+//                the last of the P contributions writes the output (no fixed order).
 //
 // Failure handling: every wait is bounded.  A wait for another block's progress (readiness
 // flags, the work gate, the controller watchdog) gives up after timeout_ns and raises
