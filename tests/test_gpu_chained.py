@@ -101,3 +101,23 @@ def test_missing_unit_times_out_then_recovers(tiles):
     assert mk.mk_status_check(ws) == mk.MK_ERR_TIMEOUT
     C = gu.call_ar(Ad, Bd, mk.MK_F32, ws=ws, opts=ch_opts(tiles))
     gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
+
+
+def test_reducescatter_full_size_same_bits_and_sampled():
+    wl = ig.WORKLOADS["rs_p8_m16384_n8192_k1024"]
+    A, B, Ad, Bd = gu.upload(wl)
+    want = torch.cat(gu.call_rs(Ad, Bd, mk.MK_BF16), dim=0)          # adaptive role split
+    got = torch.cat(gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts()), dim=0)
+    assert torch.equal(got, want)
+    rows, cols = gu.sample_indices(wl.M, wl.N, 2048)
+    rms = float(np.sqrt(np.mean(oracle.allreduce_rows(A, B, 0, 2) ** 2)))
+    gu.check_tolerance(gu.host_values(got)[rows, cols], oracle.allreduce_at(A, B, rows, cols), out_bf16=True,
+                       rms_ref=rms)
+
+
+def test_mid_workload_full_oracle_and_same_bits():
+    wl = ig.WORKLOADS["ar_p8_m2048_n4096_k512"]
+    A, B, Ad, Bd = gu.upload(wl)
+    got = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=ch_opts())
+    gu.check_tolerance(gu.host_values(got), oracle.allreduce(A, B), out_bf16=True)
+    assert torch.equal(got, gu.call_ar(Ad, Bd, mk.MK_BF16))
