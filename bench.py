@@ -556,6 +556,70 @@ def e2e_leg(torch, prob, opts, stream, steps, ranks):
             "serial": {"value": ranks.world * wl.flops / (serial_ms * 1e-3) / 1e12, "ms_per_step": serial_ms}}
 
 
+# ------------------------------------------------------------------ AllGather + GEMM
+def allgather_arm(args):
+    """`--op allgather`: the fused AllGather + GEMM (communication pairs gather 128-row chunks of
+    the row-sharded A into every rank's buffer, compute pairs multiply as chunks arrive) against
+    its unfused form (a gather kernel, then the GEMM kernel), P logical ranks on one GPU.  The
+    default shape is a column-parallel MLP up-projection: 8192 tokens, hidden 4096, 3584 output
+    columns per rank."""
+    import torch
+    from gemm_tile_level_gb300 import api, mk
+
+    P, M, N, K = (int(x) for x in args.ag_shape.split(","))
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    A = [np.empty((M // P, K), np.uint16) for _ in range(P)]
+    B = [np.empty((K, N), np.uint16) for _ in range(P)]
+    for r in range(P):
+        ig.fill_bf16(A[r].reshape(-1), ig.normal(1.0), 0, r, ig.TID_A)
+        ig.fill_bf16(B[r].reshape(-1), ig.normal(1.0 / K), 0, r, ig.TID_B)
+    flops = 2.0 * P * M * N * K
+    with torch.cuda.stream(stream):
+        Ad = [api.bf16_device(a) for a in A]
+        Bd = [api.bf16_device(b) for b in B]
+        C = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        G = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
+
+        def timed(mode, steps):
+            o = api.make_opts(mode)
+            for _ in range(args.warmup):
+                mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(steps):
+                mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            mk.check(mk.mk_status_check(ws, stream))
+            return e0.elapsed_time(e1) / steps
+
+        clocks = ClockSampler(0)
+        clocks.start()
+        fused_ms = timed(mk.MK_SPLIT_ADAPTIVE, args.steps)
+        clocks.stop()
+        unfused_ms = timed(mk.MK_SPLIT_UNFUSED, max(3, min(args.steps, 50)))
+    peaks, peak_src = load_peaks()
+    value = flops / (fused_ms * 1e-3) / 1e12
+    clk = clocks.summary()
+    line = {"metric": "fused AllGather+GEMM TFLOP/s on 1 GB300", "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": fused_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"ag_p{P}_m{M}_n{N}_k{K}", "op": "allgather_gemm", "P": P, "M": M, "N": N, "K": K,
+                       "gathered_copies": True, "out_dtype": "bf16"},
+            "roofline": {"bound": "tensor", "achieved": value, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": value / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json, burst)"},
+            "gpu_launches": args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "unfused_baseline": {"value": flops / (unfused_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                 "ms_per_step": unfused_ms, "launches_per_step": 2}}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ SM-split sweep
 def sweep(args):
     import torch
@@ -633,6 +697,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-s", type=float, default=8.0)
+    ap.add_argument("--op", choices=["rowparallel", "allgather"], default="rowparallel",
+                    help="allgather: time the fused AllGather + GEMM against its unfused form instead")
+    ap.add_argument("--ag-shape", default="8,8192,3584,4096", help="P,M,N,K of --op allgather")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-m", type=int, nargs="*")
     ap.add_argument("--sweep-steps", type=int, default=10)
@@ -647,6 +714,9 @@ def main():
     _RASTER_GROUP = args.raster_group
     if args.sweep:
         sweep(args)
+        return
+    if args.op == "allgather":
+        allgather_arm(args)
         return
     wl = workload_by_name(args.workload)
     if args.shape:
