@@ -583,7 +583,7 @@ def allgather_arm(args):
         ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
 
         def timed(mode, steps):
-            o = api.make_opts(mode)
+            o = api.make_opts(mode, flags=_EXTRA_FLAGS)
             for _ in range(args.warmup):
                 mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
