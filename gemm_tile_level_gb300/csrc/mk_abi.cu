@@ -31,6 +31,7 @@ constexpr double kBandL2Budget = 24e6;     // rank-major: bytes of one rank's A 
 constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-major from this M on
 constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up to this M
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
+constexpr int64_t kAgBandRows = 4;             // AllGather + GEMM: 256-row tile rows per rank-major band
 constexpr double kTailL2Bytes = 64e6;        // partial tiles that stay in L2 until the end of a call
 constexpr double kTailL2Bandwidth = 12e12;   // bytes/s the grid streams from L2
 constexpr double kHbmEfficiency = 0.8;       // streaming fraction of the nominal HBM bandwidth
@@ -318,10 +319,12 @@ size_t ag_workspace_bytes(const Geometry &g) {
 }
 
 // First split of AllGather + GEMM (roles are fixed for the call): SMs for the copies in proportion
-// to their share of the work, at the per-SM rates measured on GB300 while the GEMM runs: about
-// 60 GB/s of bulk copies (read once, written P times) and 11 TFLOP/s of bf16 MMA.
+// to their share of the work, at per-SM rates measured on GB300 while the GEMM runs: about
+// 30 GB/s of bulk copies (read once, written P times) against 11 TFLOP/s of bf16 MMA.  The copy
+// rate is taken low on purpose: in rank-major order the first band's rows are all needed at
+// once, so the copies should run well ahead of the compute.
 int initial_copy_pairs(int role_units, int P, int64_t M, int64_t N, int64_t K) {
-    const double copy = static_cast<double>(M) * K * 2.0 * (P + 1) / 60e9;
+    const double copy = static_cast<double>(M) * K * 2.0 * (P + 1) / 30e9;
     const double gemm = static_cast<double>(P) * 2.0 * M * N * K / 11e12;
     int nr = static_cast<int>(role_units * copy / (copy + gemm) + 0.5);
     if (nr < 1) nr = 1;
@@ -427,11 +430,19 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     int nr = o.comm_sms > 0 ? (o.comm_sms + 1) / 2 : initial_copy_pairs(role_units, P, M, N, K);
     if (nr > role_units - 1) nr = role_units - 1;
     p.static_nr = p.init_nr = nr < 1 ? 1 : nr;
-    p.rank_major = 0;
+    // Rank-major bands by default, as for the row-parallel ops: each rank multiplies its own
+    // gathered copy of A with its own B, and computing a band rank by rank streams each B once
+    // per band instead of once per tile row (measured 12 % faster, fused and unfused alike).
+    p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : 1;
     // each rank multiplies its own gathered copy of A (P copies live at once); without gathered
     // copies every rank reads the same shards
-    p.raster_group = o.raster_group > 0 ? o.raster_group
-                                        : auto_raster_group(true, gather ? P : 1, K, g.pair_tiles_m, false);
+    if (o.raster_group > 0)
+        p.raster_group = o.raster_group;
+    else if (p.rank_major)
+        p.raster_group = static_cast<int32_t>(g.pair_tiles_m < kAgBandRows ? (g.pair_tiles_m > 0 ? g.pair_tiles_m : 1)
+                                                                            : kAgBandRows);
+    else
+        p.raster_group = auto_raster_group(true, gather ? P : 1, K, g.pair_tiles_m, false);
     p.discard = 0;
     p.ctrl_period_ns = kCtrlPeriodNs;
     p.ctrl_tail_ns = 0;   // unused: AllGather + GEMM fixes the roles for the call
