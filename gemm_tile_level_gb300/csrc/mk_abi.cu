@@ -32,6 +32,25 @@ constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-majo
 constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up to this M
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
 constexpr int64_t kAgBandRows = 4;             // AllGather + GEMM: 256-row tile rows per rank-major band
+// Pause between an epilogue's 32-column store chunks: an eighth of one unit's MMA time at about
+// 0.33 us per 64-deep k-block, at most 1 us (4 chunks per warp then take at most half a unit).
+int unit_pace_ns(int64_t K) {
+    const double unit_ns = static_cast<double>((K + MK_BK - 1) / MK_BK) * 330.0;
+    const double pace = unit_ns / 8.0;
+    return static_cast<int>(pace > 1000.0 ? 1000.0 : pace);
+}
+
+// The unfused GEMM launch and the role split (static or adaptive) are always paced. Chained and
+// accumulate modes, whose epilogues also load or reduce in L2 and hold up the next rank's fold,
+// are paced only when units are long (K_r >= 2048): pacing them measured faster at K_r = 3584
+// and slower at K_r = 1024.
+int epilogue_pace_ns(const mk_opts &o, int64_t Kr) {
+    if (o.flags & MK_FLAG_NO_EPILOGUE_PACING) return 0;
+    const int64_t kb = (Kr + MK_BK - 1) / MK_BK;
+    if ((o.split_mode == MK_SPLIT_CHAINED || o.split_mode == MK_SPLIT_ACCUMULATE) && kb < 32) return 0;
+    return unit_pace_ns(Kr);
+}
+
 constexpr double kTailL2Bytes = 64e6;        // partial tiles that stay in L2 until the end of a call
 constexpr double kTailL2Bandwidth = 12e12;   // bytes/s the grid streams from L2
 constexpr double kHbmEfficiency = 0.8;       // streaming fraction of the nominal HBM bandwidth
@@ -280,6 +299,7 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
     p.ctrl_period_ns = kCtrlPeriodNs;
+    p.epi_pace_ns = epilogue_pace_ns(o, Kr);
     p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P);
     {
         // SM time of one reduce item when the whole grid reduces at the end of the call: the
@@ -445,6 +465,8 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
         p.raster_group = auto_raster_group(true, gather ? P : 1, K, g.pair_tiles_m, false);
     p.discard = 0;
     p.ctrl_period_ns = kCtrlPeriodNs;
+    // paced like the row-parallel role split (3.5 % faster fused at M = 8192, N = 3584, K = 4096)
+    p.epi_pace_ns = (o.flags & MK_FLAG_NO_EPILOGUE_PACING) ? 0 : unit_pace_ns(K);
     p.ctrl_tail_ns = 0;   // unused: AllGather + GEMM fixes the roles for the call
     p.red_split = 1;
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;

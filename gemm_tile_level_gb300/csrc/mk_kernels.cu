@@ -540,6 +540,13 @@ __device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int s
     if (etid == 0 && (ok || !exists)) atomicAdd(&c.hdr->tiles_done, 1u);
 }
 
+// Between the 32-column chunks of an epilogue's global stores: a pause, so that the 8 warps'
+// stores do not arrive in one burst that holds up the TMA loads feeding the next unit (measured:
+// up to 9 % faster GEMM at K_r = 1024).  The host sizes it to fit well inside one unit's MMA time.
+__device__ __forceinline__ void epilogue_pace(const MkParams &p) {
+    if (p.epi_pace_ns > 0) __nanosleep(static_cast<unsigned>(p.epi_pace_ns));
+}
+
 // The epilogue group drains TMEM accumulator `acc` (128 lanes x BN columns of fp32) into the
 // partial tile (r, lt) with 512-byte coalesced warp stores.
 template <int BN>
@@ -570,6 +577,7 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
             st_f4_hint(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
                        __uint_as_float(v[4 * q + 3]), pol);
         }
+        epilogue_pace(p);
     }
 }
 
@@ -605,6 +613,7 @@ __device__ __forceinline__ void accumulate_partial(const MkParams &p, uint32_t t
             red_add_f4_hint(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
                             __uint_as_float(v[4 * q + 3]), pol);
         }
+        epilogue_pace(p);
     }
 }
 
@@ -728,6 +737,7 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
 #pragma unroll
             for (int q = 0; q < 8; ++q) st_f4_hint(base + q * MK_BM * 4, x[q].x, x[q].y, x[q].z, x[q].w, pol);
         }
+        epilogue_pace(p);
     }
     return true;
 }

@@ -87,6 +87,9 @@ typedef enum {
 #define MK_FLAG_KEEP_PARTIALS 1u   /* do not discard consumed partial tiles from L2 (default: discard) */
 #define MK_FLAG_SINGLE_SM_TILES 2u /* one SM per 128 x 256 compute tile instead of an SM pair per 256 x 256 */
 #define MK_FLAG_NO_L2_HINTS 4u     /* load operands without L2 eviction-priority hints */
+#define MK_FLAG_NO_EPILOGUE_PACING 64u /* store each tile's epilogue in one burst (by default the
+                                          stores of a tile are spread over part of the next unit's
+                                          MMA time, so that they do not hold up its TMA loads) */
 #define MK_FLAG_TILE_MAJOR 16u    /* compute the P ranks of each tile back to back */
 #define MK_FLAG_RANK_MAJOR 32u    /* compute bands of tile rows rank by rank (see raster_group); without
                                      either flag the order is rank-major for M >= 1024, else tile-major */
