@@ -55,11 +55,12 @@ def workload_by_name(name: str) -> ig.Workload:
     raise SystemExit(f"unknown workload {name}; choose from {list(ig.WORKLOADS)}")
 
 
-def algorithmic_bytes(wl: ig.Workload) -> int:
-    """A and B once, every rank's fp32 partial tile written and read once, the output once."""
+def algorithmic_bytes(wl: ig.Workload, partial_bytes: int = 4) -> int:
+    """A and B once, every rank's partial tile (fp32, or bf16 with --bf16-partials) written and
+    read once, the output once."""
     a = wl.P * wl.M * wl.Kr * 2
     b = wl.P * wl.Kr * wl.N * 2
-    partial = wl.P * wl.M * wl.N * 4
+    partial = wl.P * wl.M * wl.N * partial_bytes
     out = wl.M * wl.N * (2 if wl.out_dtype == "bf16" else 4)
     return a + b + 2 * partial + out
 
@@ -267,8 +268,13 @@ _REDUCE_SPLIT = 0  # --reduce-split (0 = chosen by the library)
 _RASTER_GROUP = 0  # --raster-group (0 = chosen by the library)
 
 
+BF16_PARTIALS_FLAG = 128   # MK_FLAG_BF16_PARTIALS (--bf16-partials)
+
+
 def split_opts(api, mk, split: str, comm_sms: int):
     kw = dict(flags=_EXTRA_FLAGS, reduce_split=_REDUCE_SPLIT, raster_group=_RASTER_GROUP)
+    if split in ("accumulate", "chained"):
+        kw["flags"] &= ~BF16_PARTIALS_FLAG    # these splits store no partial tiles
     if split == "adaptive":
         return api.make_opts(mk.MK_SPLIT_ADAPTIVE, comm_sms=comm_sms, **kw)
     if split == "static":
@@ -412,7 +418,8 @@ def gpu_arm(args, wl, ranks):
     peaks, peak_src = load_peaks()
     kernel_ms = statistics.mean(per_launch)
     achieved = wl.flops / (kernel_ms * 1e-3) / 1e12
-    bytes_alg = algorithmic_bytes(wl)
+    bf16_partials = bool(_EXTRA_FLAGS & BF16_PARTIALS_FLAG) and args.split in ("adaptive", "static", "unfused")
+    bytes_alg = algorithmic_bytes(wl, 2 if bf16_partials else 4)
     t_tensor = wl.flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
@@ -446,6 +453,7 @@ def gpu_arm(args, wl, ranks):
             "config": {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
                        "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype, "split": args.split,
                        "accumulate": "fp32", "seed": wl.seed, "tiles": args.tiles,
+                       "partial_tiles": "bf16" if bf16_partials else "fp32",
                        "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
                        "parallelism": f"{wl.P} logical ranks on one GPU" + (
                            f"; {ranks.world} replicas" if ranks.world > 1 else "")},
@@ -583,7 +591,7 @@ def allgather_arm(args):
         ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
 
         def timed(mode, steps):
-            o = api.make_opts(mode, flags=_EXTRA_FLAGS)
+            o = api.make_opts(mode, flags=_EXTRA_FLAGS & ~BF16_PARTIALS_FLAG)
             for _ in range(args.warmup):
                 mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -690,6 +698,8 @@ def main():
                     help="compute the P ranks of each tile back to back instead of band by band")
     ap.add_argument("--reduce-split", type=int, default=0,
                     help="column slices per output tile's reduction (0 = the library's choice)")
+    ap.add_argument("--bf16-partials", action="store_true",
+                    help="adaptive / static / unfused splits: store partial tiles as bf16 (MK_FLAG_BF16_PARTIALS)")
     ap.add_argument("--shape", default="", help="P,M,N,K_per_rank override (same distributions); "
                     "for small profiling cases")
     ap.add_argument("--no-e2e", action="store_true")
@@ -709,7 +719,7 @@ def main():
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     global _EXTRA_FLAGS, _REDUCE_SPLIT, _RASTER_GROUP
     _EXTRA_FLAGS = (2 if args.tiles == "single" else 0) | (8 if args.no_cooperative else 0) | \
-        (16 if args.tile_major else 0)
+        (16 if args.tile_major else 0) | (BF16_PARTIALS_FLAG if args.bf16_partials else 0)
     _REDUCE_SPLIT = args.reduce_split
     _RASTER_GROUP = args.raster_group
     if args.sweep:

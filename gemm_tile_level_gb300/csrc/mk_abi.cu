@@ -87,8 +87,8 @@ constexpr int kCtrlPeriodNs = 1000;
 // that gives every role unit a reduce item (each item restarts the staged pipeline, so finer
 // slices only pay while some units would otherwise get none); never more slices than the staged
 // reducer has chunks in a tile (CH = 8 KiB per rank for P <= 8, else 4 KiB).
-int choose_reduce_split(int requested, int64_t items, int role_units, int bn, int P) {
-    const int nch = MK_BM * bn * 4 / (P <= 8 ? 8192 : 4096);
+int choose_reduce_split(int requested, int64_t items, int role_units, int bn, int P, int partial_esize) {
+    const int nch = MK_BM * bn * partial_esize / (P <= 8 ? 8192 : 4096);
     int s = requested;
     if (s <= 0) {
         s = 1;
@@ -169,6 +169,9 @@ mk_status check_opts(const mk_opts *o) {
         return fail(MK_ERR_INVALID_ARG, "reduce_split %d outside [0, 64]", o->reduce_split);
     if (o->trace_bytes && !o->trace) return fail(MK_ERR_INVALID_ARG, "trace_bytes without trace buffer");
     if (o->trace && !aligned16(o->trace)) return fail(MK_ERR_ALIGNMENT, "trace buffer not 16-byte aligned");
+    if ((o->flags & MK_FLAG_BF16_PARTIALS) &&
+        (o->split_mode == MK_SPLIT_ACCUMULATE || o->split_mode == MK_SPLIT_CHAINED))
+        return fail(MK_ERR_INVALID_ARG, "MK_FLAG_BF16_PARTIALS needs partial tiles (adaptive, static or unfused split)");
     return MK_OK;
 }
 
@@ -300,13 +303,16 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.discard = (o.flags & MK_FLAG_KEEP_PARTIALS) ? 0 : 1;
     p.ctrl_period_ns = kCtrlPeriodNs;
     p.epi_pace_ns = epilogue_pace_ns(o, Kr);
-    p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P);
+    p.partial_bf16 = (o.flags & MK_FLAG_BF16_PARTIALS) ? 1 : 0;
+    const int esize = p.partial_bf16 ? 2 : 4;
+    p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P,
+                                      esize);
     {
         // SM time of one reduce item when the whole grid reduces at the end of the call: the
         // item's partial bytes at the grid's share of memory bandwidth (L2 when every partial
         // tile of the call fits there, else HBM)
-        const double item_bytes = static_cast<double>(MK_BM) * g.bn * 4.0 * P / p.red_split;
-        const double partials = static_cast<double>(g.num_tiles) * MK_BM * g.bn * 4.0 * P;
+        const double item_bytes = static_cast<double>(MK_BM) * g.bn * esize * P / p.red_split;
+        const double partials = static_cast<double>(g.num_tiles) * MK_BM * g.bn * esize * P;
         const double bw = partials <= kTailL2Bytes ? kTailL2Bandwidth : device_hbm_bandwidth();
         p.ctrl_tail_ns = static_cast<int32_t>(item_bytes * S / bw * 1e9);
     }
@@ -314,7 +320,7 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
 
     if (o.split_mode == MK_SPLIT_UNFUSED) {
         p.mode = MK_MODE_COMPUTE_ONLY;
-        p.red_split = choose_reduce_split(o.reduce_split, g.num_tiles, S, g.bn, P);
+        p.red_split = choose_reduce_split(o.reduce_split, g.num_tiles, S, g.bn, P, esize);
         e = mk_launch_persistent(p, g.bn, pair, S, s);
         if (e != cudaSuccess) return fail_cuda(e, "launch of the per-rank GEMM kernel");
         e = mk_launch_reduce(p, g.bn, S, s);
@@ -368,6 +374,8 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     if (o.split_mode == MK_SPLIT_ACCUMULATE || o.split_mode == MK_SPLIT_CHAINED)
         return fail(MK_ERR_INVALID_ARG, "MK_SPLIT_ACCUMULATE and MK_SPLIT_CHAINED apply to GEMM + AllReduce and "
                     "GEMM + ReduceScatter");
+    if (o.flags & MK_FLAG_BF16_PARTIALS)
+        return fail(MK_ERR_INVALID_ARG, "MK_FLAG_BF16_PARTIALS applies to GEMM + AllReduce and GEMM + ReduceScatter");
     if (N % 8 || K % 8)
         return fail(MK_ERR_UNSUPPORTED_SHAPE, "N=%lld and K=%lld must be multiples of 8", (long long)N, (long long)K);
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "dimension above 2^31-1");

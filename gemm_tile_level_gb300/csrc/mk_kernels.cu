@@ -348,19 +348,32 @@ __device__ __forceinline__ void store_out4(const MkParams &p, int grow, int gcol
 }
 
 // Partial tile (rank r, tile (tm, tn)) lives at ((r * num_tiles) + tm * tiles_n + tn) tiles into
-// the partial region; inside a tile the layout is [BN/4 column groups][128 rows][4 floats].
+// the partial region.  Inside a tile the layout is 16-byte column groups, [group][128 rows]:
+// four floats per group for fp32 partials, eight bf16 for bf16 partials (MK_FLAG_BF16_PARTIALS).
+template <int BN>
+__device__ __forceinline__ uint32_t partial_tile_bytes(const MkParams &p) {
+    return MK_BM * BN * (p.partial_bf16 ? 2u : 4u);
+}
+
+template <int BN>
+__device__ __forceinline__ char *partial_tile_at(const MkParams &p, int r, int lt) {
+    return reinterpret_cast<char *>(p.partials) +
+           (static_cast<size_t>(r) * p.num_tiles + lt) * partial_tile_bytes<BN>(p);
+}
+
+// fp32 tiles (chained running sums, accumulate mode, which never store bf16 partials)
 template <int BN>
 __device__ __forceinline__ float *partial_tile(const MkParams &p, int r, int lt) {
     return p.partials + (static_cast<size_t>(r) * p.num_tiles + lt) * (MK_BM * BN);
 }
 
-// Byte range [*b0, *b1) of a partial tile that reduce slice `sub` of `nsub` covers: whole chunks
-// of the staged reduction (CH bytes per rank, see reduce_tile_staged).
+// Chunks [c0, c1) of a partial tile that reduce slice `sub` of `nsub` covers: whole chunks of the
+// staged reduction (CH bytes per rank, see reduce_tile_staged).
 template <int BN>
 __device__ __forceinline__ void slice_chunks(const MkParams &p, int sub, int nsub, uint32_t &c0, uint32_t &c1,
                                              uint32_t &ch_bytes) {
     ch_bytes = p.P <= 8 ? 8192u : 4096u;
-    const uint32_t nch = MK_BM * BN * 4 / ch_bytes;
+    const uint32_t nch = partial_tile_bytes<BN>(p) / ch_bytes;
     c0 = static_cast<uint32_t>(sub) * nch / static_cast<uint32_t>(nsub);
     c1 = static_cast<uint32_t>(sub + 1) * nch / static_cast<uint32_t>(nsub);
 }
@@ -373,7 +386,7 @@ __device__ __forceinline__ void discard_tile(const MkParams &p, int lt, int sub,
     slice_chunks<BN>(p, sub, nsub, c0, c1, chb);
     const int l0 = static_cast<int>(c0 * chb / 128), l1 = static_cast<int>(c1 * chb / 128);
     for (int r = 0; r < p.P; ++r) {
-        const char *base = reinterpret_cast<const char *>(partial_tile<BN>(p, r, lt));
+        const char *base = partial_tile_at<BN>(p, r, lt);
         for (int l = l0 + tid; l < l1; l += nthreads) discard_l2_line(base + static_cast<size_t>(l) * 128);
     }
 }
@@ -444,6 +457,14 @@ __device__ __forceinline__ void store_out8(const MkParams &p, int grow, int gcol
     }
 }
 
+// Eight packed bf16 (element 0 in the low half of word 0) to fp32, exactly.
+__device__ __forceinline__ void widen_bf16x8(uint4 w, float4 &lo, float4 &hi) {
+    lo = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xFFFF0000u));
+    hi = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u), __uint_as_float(w.w << 16),
+                     __uint_as_float(w.w & 0xFFFF0000u));
+}
+
 // Sum the P partial tiles of tile (tm, tn) in rank order r = 0..P-1, over column slice `sub` of
 // `nsub` (a reduce item covers one slice, so that a few large tiles still spread over many SMs).
 // The tiles are streamed in chunks of CH bytes per rank (chunk c = column groups
@@ -460,10 +481,9 @@ __device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int 
     slice_chunks<BN>(p, sub, nsub, c0, c1, CH);
     const uint32_t set_bytes = CH * P;
     const uint32_t NB = min(3u, st.ring_bytes / set_bytes);
-    constexpr uint32_t TILE_BYTES = MK_BM * BN * 4;
     const uint32_t nch = c1 - c0;   // chunks of this slice
-    const char *src0 = reinterpret_cast<const char *>(partial_tile<BN>(p, 0, lt)) + static_cast<size_t>(c0) * CH;
-    const size_t rank_stride = static_cast<size_t>(p.num_tiles) * TILE_BYTES;
+    const char *src0 = partial_tile_at<BN>(p, 0, lt) + static_cast<size_t>(c0) * CH;
+    const size_t rank_stride = static_cast<size_t>(p.num_tiles) * partial_tile_bytes<BN>(p);
     const uint64_t pol = policy_evict_first();
     auto issue = [&](uint32_t ch, uint32_t seq) {
         const uint32_t b = seq % NB;
@@ -484,7 +504,25 @@ __device__ void reduce_tile_staged(const MkParams &p, const Ctx &c, int tm, int 
         const uint32_t b = seq % NB;
         wait_bar<false>(smem_u32(&st.rfull[b]), (seq / NB) & 1u, c, SITE_STAGE_FULL, ch);
         const uint8_t *buf = st.ring + b * set_bytes;
-        if (groups_per_chunk == 4) {
+        if (p.partial_bf16) {
+            // eight bf16 columns per 16-byte group, widened exactly to fp32 and summed in rank order
+            const int ng = groups_per_chunk == 4 ? 2 : 1;
+            const int g_local = groups_per_chunk == 4 ? 2 * half : half;
+#pragma unroll 1
+            for (int gi = 0; gi < ng; ++gi) {
+                const uint32_t off = (static_cast<uint32_t>(g_local + gi) * MK_BM + row) * 16;
+                float4 lo, hi;
+                widen_bf16x8(*reinterpret_cast<const uint4 *>(buf + off), lo, hi);
+                for (uint32_t r = 1; r < P; ++r) {
+                    float4 xl, xh;
+                    widen_bf16x8(*reinterpret_cast<const uint4 *>(buf + r * CH + off), xl, xh);
+                    lo.x += xl.x; lo.y += xl.y; lo.z += xl.z; lo.w += xl.w;
+                    hi.x += xh.x; hi.y += xh.y; hi.z += xh.z; hi.w += xh.w;
+                }
+                const int gcol = tn * BN + static_cast<int>((c0 + ch) * groups_per_chunk + g_local + gi) * 8;
+                if (grow < p.M && gcol < p.N) store_out8(p, grow, gcol, lo, hi);
+            }
+        } else if (groups_per_chunk == 4) {
             const int g_local = 2 * half;   // this thread's two column groups in the chunk
             const uint32_t off0 = (static_cast<uint32_t>(g_local) * MK_BM + row) * 16;
             const uint32_t off1 = off0 + MK_BM * 16;
@@ -555,7 +593,7 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
     const int lq = warp & 3;                          // the TMEM lane quarter this warp can access
     const int half = (warp - MK_EPI_WARP0) >> 2;      // which half of the tile's columns
     const int row = lq * 32 + lane;
-    float *tile = partial_tile<BN>(p, r, lt);
+    char *tile = partial_tile_at<BN>(p, r, lt);
     // partial tiles should live in L2 until the reduce role has read them (then they are
     // discarded); in rank-major order only the last rank's tiles are read soon after they are
     // written, the others would only crowd out the band's A rows
@@ -571,11 +609,22 @@ __device__ __forceinline__ void store_partial(const MkParams &p, uint32_t tmem_a
 #pragma unroll
             for (int q = 0; q < 32; ++q) v[q] = 0u;
         }
+        if (p.partial_bf16) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float *dst = tile + (static_cast<size_t>((col0 >> 2) + q) * MK_BM + row) * 4;
-            st_f4_hint(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                       __uint_as_float(v[4 * q + 3]), pol);
+            for (int q = 0; q < 4; ++q) {
+                char *dst = tile + (static_cast<size_t>((col0 >> 3) + q) * MK_BM + row) * 16;
+                st_u4_hint(dst, pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])), pol);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                char *dst = tile + (static_cast<size_t>((col0 >> 2) + q) * MK_BM + row) * 16;
+                st_f4_hint(dst, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]), pol);
+            }
         }
         epilogue_pace(p);
     }

@@ -404,6 +404,12 @@ __device__ __forceinline__ void st_f4_hint(void *p, float a, float b, float c, f
                  : "memory");
 }
 
+__device__ __forceinline__ void st_u4_hint(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_u2(void *p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }

@@ -43,6 +43,7 @@ MK_FLAG_NO_COOPERATIVE = 8
 MK_FLAG_TILE_MAJOR = 16
 MK_FLAG_RANK_MAJOR = 32
 MK_FLAG_NO_EPILOGUE_PACING = 64
+MK_FLAG_BF16_PARTIALS = 128
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",

@@ -90,6 +90,15 @@ typedef enum {
 #define MK_FLAG_NO_EPILOGUE_PACING 64u /* store each tile's epilogue in one burst (by default the
                                           stores of a tile are spread over part of the next unit's
                                           MMA time, so that they do not hold up its TMA loads) */
+#define MK_FLAG_BF16_PARTIALS 128u /* adaptive, static and unfused splits: store each per-rank partial
+                                      tile as bf16 (round to nearest even from the fp32 accumulator)
+                                      instead of fp32, halving the partial-tile bytes; the reduction
+                                      still adds in fp32 in rank order.  The result is then
+                                      RNE_out(sum_r RNE_bf16(P_r)): exact on integer inputs whose
+                                      per-rank partials are exact in bf16, otherwise within one bf16
+                                      rounding per partial.  MK_ERR_INVALID_ARG with the accumulate
+                                      and chained splits and with mk_allgather_gemm (no partial
+                                      tiles). */
 #define MK_FLAG_TILE_MAJOR 16u    /* compute the P ranks of each tile back to back */
 #define MK_FLAG_RANK_MAJOR 32u    /* compute bands of tile rows rank by rank (see raster_group); without
                                      either flag the order is rank-major for M >= 1024, else tile-major */

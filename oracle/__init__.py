@@ -10,6 +10,8 @@ tensor-parallel rows):
   * GEMM + ReduceScatter: rank s receives rows [s M/P, (s+1) M/P) of that same C.
   * AllGather + GEMM:     rank r receives [A_0; ...; A_{P-1}] B_r (row shards of A gathered,
                           B column-sharded).
+Partial tiles stored at half width (bf16) are a variant of the boundary without a counterpart on
+those pages: ``allreduce_bf16_partials`` defines it.
 Parity pins: every function here is pinned by tests/test_oracle_pins.py against exact
 arithmetic, closed forms, invariants or numpy's fp64 matmul.
 """
@@ -120,6 +122,31 @@ def allreduce_at(A, B, rows, cols) -> np.ndarray:
     if rows.size:
         _load().mko_rank_sum_at(P, N, Kr, _ptr_array(A), _ptr_array(B), rows.size,
                                 rows.ctypes.data, cols.ctypes.data, out.ctypes.data)
+    return out
+
+
+def allreduce_bf16_partials(A, B) -> np.ndarray:
+    """The bf16-partial-tile form of GEMM + AllReduce: sum_r RNE_bf16(A_r B_r), summed in fp64 in
+    rank order.  Each per-rank partial product is rounded to bf16 (round to nearest even) before
+    the ranks are added, which is what storing partial tiles at half width computes.  The partial
+    is rounded from its fp64 value here; a kernel that rounds its fp32 accumulator lands on the
+    other side of a rounding midpoint only where the two differ across it.
+    Parity pinned (ties-to-even closed form, reduction to ``allreduce`` when every partial is
+    exact in bf16, exact-rational brute force)."""
+    A = [_bits(a) for a in A]
+    B = [_bits(b) for b in B]
+    P, M, N, Kr = _check_ranks(A, B)
+    out = np.zeros((M, N), np.float64)
+    for a, b in zip(A, B):
+        out += bf16_to_f64(round_bf16(gemm(a, b)))
+    return out
+
+
+def allreduce_bf16_partials_at(A, B, rows, cols) -> np.ndarray:
+    """``allreduce_bf16_partials`` at the sampled elements (rows[s], cols[s]) only."""
+    out = np.zeros(np.asarray(rows).shape, np.float64)
+    for a, b in zip(A, B):
+        out += bf16_to_f64(round_bf16(allreduce_at([a], [b], rows, cols)))
     return out
 
 

@@ -125,6 +125,17 @@ def test_argument_checks_return_before_any_launch(mk):
         o.reduce_split = bad
         assert call_ar(mk, opts=o) == mk.MK_ERR_INVALID_ARG and "reduce_split" in mk.mk_last_error()
     assert call_ar(mk, N=100) == mk.MK_ERR_UNSUPPORTED_SHAPE and "multiples of 8" in mk.mk_last_error()
+    # bf16 partial tiles need a split that stores partial tiles
+    for mode in (mk.MK_SPLIT_ACCUMULATE, mk.MK_SPLIT_CHAINED):
+        o = mk.mk_opts_default()
+        o.split_mode = mode
+        o.flags = mk.MK_FLAG_BF16_PARTIALS
+        assert call_ar(mk, opts=o) == mk.MK_ERR_INVALID_ARG and "BF16_PARTIALS" in mk.mk_last_error()
+    o = mk.mk_opts_default()
+    o.flags = mk.MK_FLAG_BF16_PARTIALS
+    st = mk.mk_allgather_gemm(2, 256, 128, 64, [FAKE] * 2, [FAKE] * 2, [FAKE] * 2, [FAKE] * 2, mk.MK_BF16, FAKE,
+                              ws_bytes=1 << 30, opts=o, stream=0)
+    assert st == mk.MK_ERR_INVALID_ARG and "BF16_PARTIALS" in mk.mk_last_error()
     # ReduceScatter needs M divisible by P
     st = mk.mk_gemm_reducescatter(3, 128, 128, 64, [FAKE] * 3, [FAKE] * 3, [FAKE] * 3, 0, FAKE,
                                   ws_bytes=1 << 30, stream=0)

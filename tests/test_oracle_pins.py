@@ -234,6 +234,70 @@ def test_allgather_gemm_matches_numpy_blocks():
         assert np.array_equal(Cs[r], full[:, r * Np:(r + 1) * Np])
 
 
+# ---------------------------------------------------------------- bf16 partial tiles
+def test_bf16_partials_ties_to_even_closed_form():
+    # A_r = 1 and B_r[:, j] holding s ones (zeros below) make every partial equal to s.  Between
+    # 256 and 512 bf16 steps by 2, so odd s is a tie: 257 -> 256, 259 -> 260, 261 -> 260,
+    # 263 -> 264 (even significand); 255 and 256 are exact.  Rounding happens per rank.
+    P, M, Kr = 3, 2, 264
+    s = [[255, 256, 257, 259, 261, 263],
+         [257, 257, 259, 263, 255, 256],
+         [263, 261, 255, 257, 259, 257]]
+    rounded = {255: 255, 256: 256, 257: 256, 259: 260, 261: 260, 263: 264}
+    N = len(s[0])
+    one = f32_to_bf16_exact(1.0)
+    A = [np.full((M, Kr), one, np.uint16) for _ in range(P)]
+    B = []
+    for r in range(P):
+        b = np.zeros((Kr, N), np.float32)
+        for j in range(N):
+            b[:s[r][j], j] = 1.0
+        B.append(f32_to_bf16_exact(b))
+    want = np.array([sum(rounded[s[r][j]] for r in range(P)) for j in range(N)], np.float64)
+    got = oracle.allreduce_bf16_partials(A, B)
+    assert np.array_equal(got, np.tile(want, (M, 1)))
+    # the plain sum is not rounded per rank (column 2: 257 + 259 + 255 = 771, not 256 + 260 + 255)
+    assert np.array_equal(oracle.allreduce(A, B)[0], np.array([sum(s[r][j] for r in range(P)) for j in range(N)]))
+
+
+@pytest.mark.parametrize("Kr", [16, 64])
+def test_bf16_partials_equal_the_plain_sum_when_partials_are_exact(Kr):
+    # integer entries in {-2..2}: |partial| <= 4 K_r <= 256, every such integer is a bf16 value
+    A, B = rand_case(5, 23, 31, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, seed=Kr)
+    assert np.array_equal(oracle.allreduce_bf16_partials(A, B), oracle.allreduce(A, B))
+
+
+def test_bf16_partials_sampled_elements_equal_full_result():
+    A, B = rand_case(4, 30, 40, 48, ig.normal(1.0), ig.normal(1.0), seed=12)
+    C = oracle.allreduce_bf16_partials(A, B)
+    rng = np.random.default_rng(3)
+    rows, cols = rng.integers(0, 30, 200), rng.integers(0, 40, 200)
+    assert np.array_equal(oracle.allreduce_bf16_partials_at(A, B, rows, cols), C[rows, cols])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bf16_partials_bruteforce_exact_rationals(seed):
+    rng = np.random.default_rng(50 + seed)
+    P, M, N, Kr = int(rng.integers(1, 4)), int(rng.integers(1, 7)), int(rng.integers(1, 7)), \
+        int(rng.integers(1, 17))
+    A, B = rand_case(P, M, N, Kr, ig.normal(1.0), ig.UNIFORM_PM1, seed=200 + seed)
+    C = oracle.allreduce_bf16_partials(A, B)
+    for i in range(M):
+        for j in range(N):
+            total, absq = Fraction(0), Fraction(0)
+            for r in range(P):
+                terms = [exact_value(A[r][i, k]) * exact_value(B[r][k, j]) for k in range(Kr)]
+                p = sum(terms, Fraction(0))
+                bound = Fraction(gamma(Kr)) * sum((abs(t) for t in terms), Fraction(0))
+                q = exact_round_bf16(p)
+                # a partial within the fp64 error of a rounding midpoint may round either way
+                assert q == exact_round_bf16(p - bound) == exact_round_bf16(p + bound), "midpoint case"
+                qv = exact_value(q)
+                total += qv
+                absq += abs(qv)
+            assert abs(Fraction(C[i, j]) - total) <= Fraction(gamma(P)) * absq
+
+
 # ---------------------------------------------------------------- output rounding
 def test_round_bf16_hand_cases():
     cases = {
