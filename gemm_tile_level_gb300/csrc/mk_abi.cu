@@ -30,6 +30,10 @@ constexpr double kRasterL2Budget = 32e6;   // tile-major: bytes of A rows (all r
 constexpr double kBandL2Budget = 24e6;     // rank-major: bytes of one rank's A rows resident per band
 constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-major from this M on
 constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up to this M
+#ifndef MK_CHAIN_OWNER_MAX_ROWS
+#define MK_CHAIN_OWNER_MAX_ROWS 256
+#endif
+constexpr int64_t kChainedOwnerMaxRows = MK_CHAIN_OWNER_MAX_ROWS; // chained mode: tile owners up to this M
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
 constexpr int64_t kAgBandRows = 4;             // AllGather + GEMM: 256-row tile rows per rank-major band
 // Pause between an epilogue's 32-column store chunks: an eighth of one unit's MMA time at about
@@ -108,9 +112,9 @@ struct Geometry {
     size_t flags_off, partials_off, total;
 };
 
-bool make_geometry(int P, int64_t M, int64_t N, int64_t Kr, Geometry *g) {
+bool make_geometry(int P, int64_t M, int64_t N, int64_t Kr, Geometry *g, int bn = 0) {
     if (P < 1 || P > MK_MAX_P || M < 0 || N < 0 || Kr < 0) return false;
-    g->bn = choose_bn(N);
+    g->bn = bn > 0 ? bn : choose_bn(N);
     g->tiles_m = (M + MK_BM - 1) / MK_BM;
     g->tiles_n = (N + g->bn - 1) / g->bn;
     g->num_tiles = g->tiles_m * g->tiles_n;
@@ -213,8 +217,19 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     // Chained mode on a short M (one band of at most two 256-row tile rows) folds the ranks of a
     // tile while several of them are still in flight; one-SM tiles give each rank pass twice
     // the tiles, so that fewer folds wait on a predecessor (measured: 2-3 % faster at M <= 512).
-    const bool chained_short = o.split_mode == MK_SPLIT_CHAINED && M <= kChainedOneSmMaxRows;
+    //
+    // With a single 256-row band (M <= 256) every rank of a tile is in flight at once, the P folds
+    // of a tile follow one another through L2 and their latency sets the call time.  There one SM
+    // pair owns each 256 x 128 tile instead: it computes the tile's P ranks one after the other
+    // and its epilogue keeps the running sum in TMEM (the same additions in the same order), so no
+    // fold waits on another block (measured at P=8, N=8192, K_r=1024: 56 us against 60 us for the
+    // chain; at M = 512 and up the chain is faster, 81 against 100 us).  A caller that fixes the
+    // tile kind or the unit order, or withholds a unit, gets the rank-ordered chain.
+    const bool chain_owner = o.split_mode == MK_SPLIT_CHAINED && M <= kChainedOwnerMaxRows && o.debug_skip_unit < 0 &&
+                             (o.flags & (MK_FLAG_SINGLE_SM_TILES | MK_FLAG_RANK_MAJOR | MK_FLAG_TILE_MAJOR)) == 0;
+    const bool chained_short = o.split_mode == MK_SPLIT_CHAINED && M <= kChainedOneSmMaxRows && !chain_owner;
     const bool pair = (o.flags & MK_FLAG_SINGLE_SM_TILES) == 0 && !chained_short;
+    if (chain_owner) make_geometry(P, M, N, Kr, &g, 128);   // the workspace check above used the default tiles
     int resident = 0;
     cudaError_t e = mk_max_persistent_ctas(g.bn, pair, &resident);
     if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
@@ -297,6 +312,9 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
             if (!p.rank_major) band = auto_raster_group(pair, P, Kr, order_rows, false);
             p.raster_group = static_cast<int32_t>(band < 1 ? 1 : band > order_rows ? order_rows : band);
         }
+        // tile owners walk the tiles column by column, so that the owners of one column's tiles
+        // read each B_r column block at about the same time
+        if (chain_owner && o.raster_group <= 0) p.raster_group = static_cast<int32_t>(g.pair_tiles_m);
     }
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
@@ -304,6 +322,7 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.ctrl_period_ns = kCtrlPeriodNs;
     p.epi_pace_ns = epilogue_pace_ns(o, Kr);
     p.partial_bf16 = (o.flags & MK_FLAG_BF16_PARTIALS) ? 1 : 0;
+    p.chain_owner = chain_owner ? 1 : 0;
     const int esize = p.partial_bf16 ? 2 : 4;
     p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P,
                                       esize);

@@ -90,6 +90,8 @@ struct MkParams {
     int32_t ctrl_tail_ns;        // adaptive split: grid time per reduce item at the end of the call
     int32_t epi_pace_ns;         // pause between an epilogue's 32-column store chunks (0 = none)
     int32_t partial_bf16;        // role split / unfused: partial tiles stored as bf16 (RNE), summed in fp32
+    int32_t chain_owner;         // chained mode, short M: one SM pair computes all P ranks of a tile in
+                                 // rank order and keeps the running sum in registers (BN = 128 only)
 };
 
 // Implemented in mk_abi.cu: set the host thread's mk_last_error() text; bytes of the readiness

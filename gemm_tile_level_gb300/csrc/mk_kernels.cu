@@ -80,7 +80,10 @@ struct Cfg2 {
     static constexpr int B_BOXES = BN / 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BOXES * B_BOX_BYTES;
     static constexpr int STAGES = (BN == 256) ? 7 : 8;
-    static constexpr int TMEM_COLS = ACC * BN;
+    // all of TMEM: two accumulators, and with BN = 128 a third region for a tile owner's
+    // running sum (chained mode on a short M)
+    static constexpr int TMEM_COLS = 512;
+    static_assert(ACC * BN <= 512 && (BN == 256 || (ACC + 1) * BN <= 512), "TMEM columns");
     static constexpr int TILE_FLOATS = MK_BM * BN;
     static constexpr uint32_t IDESC = idesc_bf16_f32(2 * MK_BM, BN);
 };
@@ -1365,7 +1368,8 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     using T = Cfg2<BN>;
     const bool leader = crank == 0;
     const bool ag = p.op == MK_IOP_AG;
-    const ClaimGeom g{static_cast<uint32_t>(p.num_pair_units),
+    // tile owners (chained mode, short M) claim whole tiles and load the tile's P ranks in turn
+    const ClaimGeom g{static_cast<uint32_t>(p.chain_owner ? p.num_pair_tiles : p.num_pair_units),
                       static_cast<uint32_t>(ag ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), blockIdx.x >> 1,
                       gridDim.x >> 1, 2u, ag ? 1u : static_cast<uint32_t>(p.red_split), p.pair_tiles_m};
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
@@ -1407,41 +1411,49 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
         const int u = it.y;
-        int pt, r, sm, tn;
-        unit_tile(p, p.pair_tiles_m, u, pt, r);
-        raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
-        const int tm = 2 * sm + static_cast<int>(crank);
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
-        const CUtensorMap *amap = &p.tmA[r];
-        int ay = tm * MK_BM;
-        if (p.op == MK_IOP_AG) {
-            if (p.ag_gather) {
-                // a failed wait has raised the abort: the loads still go ahead so the pipeline drains
-                if (p.ag_wait && tm < p.tiles_m) (void)wait_chunk_ready(p, c, tm, s.epoch);
+        const int nranks = p.chain_owner ? p.P : 1;
+        for (int rr = 0; rr < nranks && !stop; ++rr) {
+            int pt, r, sm, tn;
+            if (p.chain_owner) {
+                pt = u;
+                r = rr;
             } else {
-                const int sh = min(p.P - 1, tm * MK_BM / p.rows_per_shard);   // rows_per_shard % 128 == 0
-                amap = &p.tmA[sh];
-                ay = tm * MK_BM - sh * p.rows_per_shard;
+                unit_tile(p, p.pair_tiles_m, u, pt, r);
             }
-        }
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
-                stop = true;
-                break;
+            raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+            const int tm = 2 * sm + static_cast<int>(crank);
+            const CUtensorMap *amap = &p.tmA[r];
+            int ay = tm * MK_BM;
+            if (p.op == MK_IOP_AG) {
+                if (p.ag_gather) {
+                    // a failed wait has raised the abort: the loads still go ahead so the pipeline drains
+                    if (p.ag_wait && tm < p.tiles_m) (void)wait_chunk_ready(p, c, tm, s.epoch);
+                } else {
+                    const int sh = min(p.P - 1, tm * MK_BM / p.rows_per_shard);   // rows_per_shard % 128 == 0
+                    amap = &p.tmA[sh];
+                    ay = tm * MK_BM - sh * p.rows_per_shard;
+                }
             }
-            const uint32_t fb = full0 + 8u * stage;
-            const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
-            const uint32_t sb = sa + T::A_BYTES;
-            mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
-            tma_load_2d_pair_hint(sa, amap, fb, kb * MK_BK, ay, pol_a);
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
+                    stop = true;
+                    break;
+                }
+                const uint32_t fb = full0 + 8u * stage;
+                const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
+                const uint32_t sb = sa + T::A_BYTES;
+                mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
+                tma_load_2d_pair_hint(sa, amap, fb, kb * MK_BK, ay, pol_a);
 #pragma unroll
-            for (int j = 0; j < T::B_BOXES; ++j)
-                tma_load_2d_pair_hint(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
-                                      tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK, pol_b);
-            ++s.issued;
-            if (++stage == T::STAGES) {
-                stage = 0;
-                phase ^= 1u;
+                for (int j = 0; j < T::B_BOXES; ++j)
+                    tma_load_2d_pair_hint(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
+                                          tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK, pol_b);
+                ++s.issued;
+                if (++stage == T::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     }
@@ -1469,44 +1481,139 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
         }
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
-        if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
-        tc_fence_after();
-        const long long t0 = clock64();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        // one unit, or a tile owner's P units (one per rank, each in its own accumulator)
+        const int nranks = p.chain_owner ? p.P : 1;
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!wait_bar<false>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
+        for (int rr = 0; rr < nranks && ok; ++rr) {
+            if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
-            const uint32_t sb = sa + T::A_BYTES;
-            // Per-CTA halves at identical offsets in both CTAs: A 128 rows (K-major), B BN/2
-            // columns (MN-major, 64-column boxes 8 KiB apart).
-            const uint64_t ad = sw128_desc(sa, 16, 1024);
-            const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
+            const long long t0 = clock64();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!wait_bar<false>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(stages + stage * T::STAGE_BYTES);
+                const uint32_t sb = sa + T::A_BYTES;
+                // Per-CTA halves at identical offsets in both CTAs: A 128 rows (K-major), B BN/2
+                // columns (MN-major, 64-column boxes 8 KiB apart).
+                const uint64_t ad = sw128_desc(sa, 16, 1024);
+                const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
 #pragma unroll
-            for (int kk = 0; kk < MK_BK / 16; ++kk)
-                umma_bf16_pair(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
-                               T::IDESC, static_cast<uint32_t>((kb | kk) != 0));
-            umma_commit_pair(smem_u32(&s.empty[stage]), 0x3);
-            if (++stage == T::STAGES) {
-                stage = 0;
-                phase ^= 1u;
+                for (int kk = 0; kk < MK_BK / 16; ++kk)
+                    umma_bf16_pair(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
+                                   T::IDESC, static_cast<uint32_t>((kb | kk) != 0));
+                umma_commit_pair(smem_u32(&s.empty[stage]), 0x3);
+                if (++stage == T::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
+            if (!ok) break;
+            umma_commit_pair(smem_u32(&s.tfull[acc]), 0x3);
+            if (++acc == ACC) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+            atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
+                      static_cast<unsigned long long>(clock64() - t0));
         }
         if (!ok) break;
-        umma_commit_pair(smem_u32(&s.tfull[acc]), 0x3);
-        if (++acc == ACC) {
-            acc = 0;
-            aphase ^= 1u;
-        }
-        atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
-                  static_cast<unsigned long long>(clock64() - t0));
     }
     umma_commit_pair(smem_u32(&s.drain), 0x1);
     wait_bar<false>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
+}
+
+// Tile owner (chained mode on a short M): the pair computed the P ranks of one 256 x 128 tile
+// into alternating accumulators; the epilogue folds them, in rank order, into a running sum
+// S = ((p_0 + p_1) + ...) + p_r kept in TMEM next to the accumulators (each thread its row's 64
+// columns of the CTA's 128-row half), then writes the output once.  These are the reduce role's fp32
+// additions in its order, so the bits are the same; nothing is stored before the output and no
+// wait depends on another block.  False if a wait gave up (the grid is aborting).
+template <int BN>
+__device__ bool owner_tile(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base, int pt,
+                           uint32_t crank, int warp, int lane, int etid, int &acc, uint32_t &aphase,
+                           uint32_t tempty0) {
+    if constexpr (BN != 128) {
+        // the host picks tile owners with 128-column tiles only
+        if (etid == 0) raise_error(c, MK_ERR_INTERNAL, SITE_ACC_FULL, static_cast<uint32_t>(pt));
+        return false;
+    } else {
+        int sm, tn;
+        raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+        const int tm = 2 * sm + static_cast<int>(crank);
+        const bool exists = tm < p.tiles_m;
+        const int lq = warp & 3;
+        const int half = (warp - MK_EPI_WARP0) >> 2;
+        const int row = lq * 32 + lane;
+        const int grow = tm * MK_BM + row;
+        const uint32_t lanes = static_cast<uint32_t>(lq * 32) << 16;
+        // the running sum lives in the TMEM columns after the two accumulators, in the same layout
+        const uint32_t t_sum = tmem_base + static_cast<uint32_t>(ACC * BN) + lanes + static_cast<uint32_t>(half * 64);
+#pragma unroll 1
+        for (int r = 0; r < p.P; ++r) {
+            bool ok = true;
+            if (lane == 0) ok = wait_bar<false>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, pt);
+            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+            if (!bar_and(1, MK_EPI_THREADS, ok)) return false;
+            tc_fence_after();
+            if (exists) {
+                const uint32_t t_acc = tmem_base + static_cast<uint32_t>(acc * BN) + lanes + static_cast<uint32_t>(half * 64);
+                const bool last = r == p.P - 1;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {   // 16 of the thread's 64 columns at a time
+                    uint32_t v[16], sv[16];
+                    if (p.num_kb > 0) {
+                        tmem_ld16(t_acc + static_cast<uint32_t>(16 * h), v);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) v[q] = 0u;
+                    }
+                    if (r > 0) {
+                        tmem_ld16(t_sum + static_cast<uint32_t>(16 * h), sv);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
+                            v[q] = __float_as_uint(__uint_as_float(sv[q]) + __uint_as_float(v[q]));
+                    }
+                    if (!last) {
+                        tmem_st16(t_sum + static_cast<uint32_t>(16 * h), v);
+                    } else if (grow < p.M) {
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            const int gcol = tn * BN + half * 64 + 16 * h + 8 * g;
+                            if (gcol < p.N)
+                                store_out8(p, grow, gcol,
+                                           make_float4(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]),
+                                                       __uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3])),
+                                           make_float4(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]),
+                                                       __uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7])));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (crank == 0) mbar_arrive(smem_u32(&s.tempty[acc]));
+                else mbar_arrive_remote(tempty0 + 8u * acc);
+            }
+            if (++acc == ACC) {
+                acc = 0;
+                aphase ^= 1u;
+            }
+        }
+        bar_sync(1, MK_EPI_THREADS);
+        if (etid == 0) {
+            atomicAdd(&c.hdr->units_done, static_cast<uint32_t>(p.P));
+            if (exists) atomicAdd(&c.hdr->tiles_done, 1u);
+        }
+        return true;
+    }
 }
 
 template <int BN>
@@ -1536,7 +1643,9 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             wphase ^= 1u;
         }
         if (it.x == ITEM_END) break;
-        if (it.x == ITEM_COMPUTE) {
+        if (it.x == ITEM_COMPUTE && p.chain_owner) {
+            if (!owner_tile<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0)) break;
+        } else if (it.x == ITEM_COMPUTE) {
             const int u = it.y;
             int pt, r, sm, tn;
             unit_tile(p, p.pair_tiles_m, u, pt, r);

@@ -183,6 +183,18 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base lane + i), and the
 // wait is folded into the same statement so the registers are valid on return.
+// Store 16 consecutive fp32 columns into the warp's 32 TMEM lanes (one row per thread), and
+// wait until the stores are done (so that a later tcgen05.ld of those columns sees them).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 // 16 consecutive fp32 columns of the warp's 32 TMEM lanes (one per thread), then wait.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile(

@@ -1,5 +1,8 @@
 """Chained mode (MK_SPLIT_CHAINED): the compute block of (tile, rank r) folds its partial tile
 into the running sum of ranks 0..r-1 after rank r-1's release, and rank P-1 writes the output.
+On a short M (M <= 256, the default tile kind and order) one SM pair instead owns each tile,
+computes its P ranks in turn and keeps the running sum in TMEM; a tile-kind or unit-order flag
+selects the rank-ordered chain there too, so both paths are run below.
 
 These are the reduce role's fp32 additions in the reduce role's order, so on random inputs the
 result must equal the adaptive, static and unfused results bit for bit, besides matching the
@@ -46,7 +49,8 @@ def test_integer_bit_exact(P, M, N, Kr, out):
     ref = gu.rounded_reference(oracle.allreduce(A, B), out == "bf16")
     code = mk.MK_BF16 if out == "bf16" else mk.MK_F32
     for tiles in TILES:
-        for fl, band in ((0, 0), (mk.MK_FLAG_TILE_MAJOR, 0), (0, 1)):
+        # (0, 0): tile owners when M <= 256 with pair tiles; the order flags force the chain
+        for fl, band in ((0, 0), (mk.MK_FLAG_TILE_MAJOR, 0), (mk.MK_FLAG_RANK_MAJOR, 0), (0, 1)):
             C = gu.call_ar(Ad, Bd, code, opts=ch_opts(tiles, flags=fl, raster_group=band))
             gu.assert_bit_exact(gu.host_values(C), ref)
 
@@ -59,23 +63,53 @@ def test_random_same_bits_as_the_reduce_role(P, M, N, Kr):
     for tiles in TILES:
         fl = mk.MK_FLAG_SINGLE_SM_TILES if tiles == "single" else 0
         want = gu.call_ar(Ad, Bd, mk.MK_F32, opts=api.make_opts(mk.MK_SPLIT_UNFUSED, flags=fl))
-        got = gu.call_ar(Ad, Bd, mk.MK_F32, opts=ch_opts(tiles))
-        gu.check_tolerance(gu.host_values(got), ref, out_bf16=False)
-        assert torch.equal(got, want)
+        for order in (0, mk.MK_FLAG_RANK_MAJOR):
+            got = gu.call_ar(Ad, Bd, mk.MK_F32, opts=ch_opts(tiles, flags=order))
+            gu.check_tolerance(gu.host_values(got), ref, out_bf16=False)
+            assert torch.equal(got, want)
 
 
-def test_reducescatter_and_distinct_outputs():
-    P, M, N, Kr = 4, 512, 520, 96
+@pytest.mark.parametrize("P,M,N", [(3, 200, 136), (8, 256, 8192), (2, 1024, 512)])
+def test_zero_k_gives_zeros(P, M, N):
+    Ad = [torch.empty((M, 0), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Bd = [torch.empty((0, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    for tiles in TILES:
+        for order in (0, mk.MK_FLAG_RANK_MAJOR):
+            C = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+            gu.call_ar(Ad, Bd, mk.MK_F32, C=C, opts=ch_opts(tiles, flags=order))
+            assert not C.any()
+
+
+@pytest.mark.parametrize("M", [256, 512])
+def test_short_m_sweep_shape_both_paths_same_bits(M):
+    """The sweep's short shapes (P=8, N=8192, K_r=1024): tile owners and the rank-ordered chain
+    against the unfused baseline, bit for bit, and against the oracle on sampled elements."""
+    wl = ig.sweep_workload(M)
+    A, B, Ad, Bd = gu.upload(wl)
+    want = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=api.make_opts(mk.MK_SPLIT_UNFUSED))
+    for fl in (0, mk.MK_FLAG_RANK_MAJOR, mk.MK_FLAG_SINGLE_SM_TILES):
+        assert torch.equal(gu.call_ar(Ad, Bd, mk.MK_BF16, opts=ch_opts(flags=fl)), want)
+    rows, cols = gu.sample_indices(wl.M, wl.N, 1024)
+    rms = float(np.sqrt(np.mean(oracle.allreduce_rows(A, B, 0, 2) ** 2)))
+    gu.check_tolerance(gu.host_values(want)[rows, cols], oracle.allreduce_at(A, B, rows, cols), out_bf16=True,
+                       rms_ref=rms)
+
+
+@pytest.mark.parametrize("M", [512, 256])   # the rank-ordered chain; tile owners
+def test_reducescatter_and_distinct_outputs(M):
+    P, N, Kr = 4, 520, 96
     wl = ig.Workload("ch_rs", "reducescatter", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16", seed=3)
     A, B, Ad, Bd = gu.upload(wl)
     ref = gu.rounded_reference(oracle.allreduce(A, B), True)
     for tiles in TILES:
-        shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts(tiles))
-        gu.assert_bit_exact(np.concatenate([gu.host_values(s) for s in shards]), ref)
-    Cs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-    gu.call_ar(Ad, Bd, mk.MK_BF16, C=Cs, opts=ch_opts())
-    for c in Cs:
-        gu.assert_bit_exact(gu.host_values(c), ref)
+        for order in (0, mk.MK_FLAG_RANK_MAJOR):
+            shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts(tiles, flags=order))
+            gu.assert_bit_exact(np.concatenate([gu.host_values(s) for s in shards]), ref)
+    for order in (0, mk.MK_FLAG_RANK_MAJOR):
+        Cs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        gu.call_ar(Ad, Bd, mk.MK_BF16, C=Cs, opts=ch_opts(flags=order))
+        for c in Cs:
+            gu.assert_bit_exact(gu.host_values(c), ref)
 
 
 def test_full_size_same_bits_as_the_reduce_role():
