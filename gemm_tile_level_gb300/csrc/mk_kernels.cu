@@ -748,65 +748,46 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
     const bool last = r == p.P - 1;
     float *S = partial_tile<BN>(p, 0, lt);
     const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
-    // The running sum is read one 32-column chunk ahead: the loads of chunk cc + 1 go out before
-    // chunk cc is added and stored, so the chunks' L2 round trips overlap instead of following
-    // one another.
-    float4 sv[8], sn[8];
-    if (r > 0) {
-        const float *b0 = S + (static_cast<size_t>((half * (BN / 2)) >> 2) * MK_BM + row) * 4;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) sv[q] = ld_cg_f4(reinterpret_cast<const float4 *>(b0 + q * MK_BM * 4));
-    }
 #pragma unroll 1
     for (int cc = 0; cc < BN / 64; ++cc) {
         const int col0 = half * (BN / 2) + cc * 32;
         float *base = S + (static_cast<size_t>(col0 >> 2) * MK_BM + row) * 4;
-        if (r > 0 && cc + 1 < BN / 64) {
-            const float *bn = base + static_cast<size_t>(8) * MK_BM * 4;   // chunk cc + 1: 32 columns on
+        // the running sum's loads go out first, so that their L2 latency overlaps the TMEM load
+        float4 sv[8];
+        if (r > 0) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sn[q] = ld_cg_f4(reinterpret_cast<const float4 *>(bn + q * MK_BM * 4));
+            for (int q = 0; q < 8; ++q) sv[q] = ld_cg_f4(reinterpret_cast<const float4 *>(base + q * MK_BM * 4));
         }
-        // two 16-column halves, so that the accumulator values, this chunk's running sum and the
-        // next chunk's loads in flight fit in registers together
+        uint32_t v[32];
+        if (p.num_kb > 0) {
+            tmem_ld32(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0), v);
+        } else {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v[16];
-            if (p.num_kb > 0) {
-                tmem_ld16(tmem_acc + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(col0 + 16 * hh), v);
-            } else {
+            for (int q = 0; q < 32; ++q) v[q] = 0u;
+        }
+        float4 x[8];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) v[q] = 0u;
-            }
-            float4 x[4];
+        for (int q = 0; q < 8; ++q)
+            x[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                               __uint_as_float(v[4 * q + 3]));
+        if (r > 0) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                x[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-            if (r > 0) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
-                    const float4 s4 = sv[4 * hh + q];
-                    x[q].x = s4.x + x[q].x; x[q].y = s4.y + x[q].y;
-                    x[q].z = s4.z + x[q].z; x[q].w = s4.w + x[q].w;
-                }
-            }
-            if (last) {
-                if (grow < p.M) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int gcol = tn * BN + col0 + 16 * hh + 8 * q;
-                        if (gcol < p.N) store_out8(p, grow, gcol, x[2 * q], x[2 * q + 1]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_f4_hint(base + (4 * hh + q) * MK_BM * 4, x[q].x, x[q].y, x[q].z, x[q].w, pol);
+            for (int q = 0; q < 8; ++q) {   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
+                x[q].x = sv[q].x + x[q].x; x[q].y = sv[q].y + x[q].y;
+                x[q].z = sv[q].z + x[q].z; x[q].w = sv[q].w + x[q].w;
             }
         }
-        if (r > 0 && cc + 1 < BN / 64) {
+        if (last) {
+            if (grow < p.M) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sv[q] = sn[q];
+                for (int q = 0; q < 4; ++q) {
+                    const int gcol = tn * BN + col0 + 8 * q;
+                    if (gcol < p.N) store_out8(p, grow, gcol, x[2 * q], x[2 * q + 1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) st_f4_hint(base + q * MK_BM * 4, x[q].x, x[q].y, x[q].z, x[q].w, pol);
         }
         epilogue_pace(p);
     }
@@ -1369,7 +1350,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     const bool leader = crank == 0;
     const bool ag = p.op == MK_IOP_AG;
     // tile owners (chained mode, short M) claim whole tiles and load the tile's P ranks in turn
-    const ClaimGeom g{static_cast<uint32_t>(p.chain_owner ? p.num_pair_tiles : p.num_pair_units),
+    const ClaimGeom g{static_cast<uint32_t>((BN == 128 && p.chain_owner) ? p.num_pair_tiles : p.num_pair_units),
                       static_cast<uint32_t>(ag ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), blockIdx.x >> 1,
                       gridDim.x >> 1, 2u, ag ? 1u : static_cast<uint32_t>(p.red_split), p.pair_tiles_m};
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
@@ -1412,10 +1393,12 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (it.x != ITEM_COMPUTE) continue;
         const int u = it.y;
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
-        const int nranks = p.chain_owner ? p.P : 1;
+        // tile owners exist only with 128-column tiles: the 256-column kernel keeps one unit per item
+        const bool owner = BN == 128 && p.chain_owner;
+        const int nranks = owner ? p.P : 1;
         for (int rr = 0; rr < nranks && !stop; ++rr) {
             int pt, r, sm, tn;
-            if (p.chain_owner) {
+            if (owner) {
                 pt = u;
                 r = rr;
             } else {
@@ -1481,8 +1464,9 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
         }
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
-        // one unit, or a tile owner's P units (one per rank, each in its own accumulator)
-        const int nranks = p.chain_owner ? p.P : 1;
+        // one unit, or a tile owner's P units (one per rank, each in its own accumulator; tile
+        // owners exist only with 128-column tiles)
+        const int nranks = (BN == 128 && p.chain_owner) ? p.P : 1;
         bool ok = true;
         for (int rr = 0; rr < nranks && ok; ++rr) {
             if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) {
@@ -1643,7 +1627,7 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             wphase ^= 1u;
         }
         if (it.x == ITEM_END) break;
-        if (it.x == ITEM_COMPUTE && p.chain_owner) {
+        if (BN == 128 && it.x == ITEM_COMPUTE && p.chain_owner) {
             if (!owner_tile<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0)) break;
         } else if (it.x == ITEM_COMPUTE) {
             const int u = it.y;
