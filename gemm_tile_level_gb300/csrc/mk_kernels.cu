@@ -329,6 +329,25 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
     return make_int2(ITEM_END, 0);
 }
 
+// Compute-only, accumulate and chained calls claim a compute unit with one atomic.  Their
+// producer issues the claim of the next unit before it loads the current one, so that the
+// atomic's round trip overlaps those loads instead of falling between the last load of one unit
+// and the first load of the next (only STAGES k-slices are buffered ahead of the MMA).
+constexpr uint32_t NO_CLAIM = 0xFFFFFFFFu;
+
+__device__ __forceinline__ bool claims_ahead(const MkParams &p) {
+    return p.op != MK_IOP_AG &&
+           (p.mode == MK_MODE_COMPUTE_ONLY || p.mode == MK_MODE_ACCUMULATE || p.mode == MK_MODE_CHAINED);
+}
+
+// The work item for unit `u`, claimed ahead (see claims_ahead).
+__device__ int2 item_claimed_ahead(const MkParams &p, const Ctx &c, const ClaimGeom &g, uint32_t u, bool &exhausted,
+                                   uint32_t target) {
+    if (global_abort(c) || u >= g.num_units) return make_int2(ITEM_END, 0);
+    if (static_cast<int64_t>(u) == p.skip_unit) return claim_work(p, c, g, exhausted, target);
+    return make_int2(ITEM_COMPUTE, static_cast<int>(u));
+}
+
 // ------------------------------------------------------------------ reduction of one tile
 __device__ __forceinline__ void store_out4(const MkParams &p, int grow, int gcol, float4 v) {
     if (p.op == MK_IOP_RS) {
@@ -1110,11 +1129,15 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
     uint32_t pushed = 0, ring_free_at = 0;   // ring free once the epilogue has finished ring_free_at items
     bool last_reduce = false;
     uint32_t target = 0;                     // adaptive split: target_nr as last read
+    const bool ahead_mode = claims_ahead(p);
+    uint32_t ahead = NO_CLAIM;               // compute unit claimed ahead, not yet queued
     while (!stop) {
         // Reduce items are claimed at most one ahead of the one in progress, so that the last
         // items of a call spread over the grid instead of queueing behind a few blocks.
         if (last_reduce && !wait_epilogue_done(&s.epi_done, pushed - 1, c)) break;
-        const int2 it = claim_work(p, c, g, exhausted, target);
+        const int2 it = ahead != NO_CLAIM ? item_claimed_ahead(p, c, g, ahead, exhausted, target)
+                                          : claim_work(p, c, g, exhausted, target);
+        ahead = NO_CLAIM;
         last_reduce = it.x == ITEM_REDUCE;
         if (p.mode == MK_MODE_ADAPTIVE) target = ld_relaxed_gpu(&c.hdr->target_nr);   // used by the next claim
         if (!wait_bar<false>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
@@ -1128,6 +1151,7 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
         }
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
+        if (ahead_mode) ahead = atomicAdd(&c.hdr->compute_next, 1u);   // consumed at the next claim
         const int u = it.y;
         int t, r, tm, tn;
         unit_tile(p, p.tiles_m, u, t, r);
@@ -1365,12 +1389,16 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     uint32_t pushed = 0, ring_free_at = 0;
     bool last_reduce = false;
     uint32_t target = 0;   // adaptive split: target_nr as last read (see claim_work)
+    const bool ahead_mode = leader && claims_ahead(p);
+    uint32_t ahead = NO_CLAIM;   // compute unit claimed ahead, not yet queued
     while (!stop) {
         int2 it;
         if (leader) {
             // reduce items: at most one claimed ahead of the one in progress (see run1_producer)
             if (last_reduce && !wait_epilogue_done(&s.epi_done, pushed - 1, c)) break;
-            it = claim_work(p, c, g, exhausted, target);
+            it = ahead != NO_CLAIM ? item_claimed_ahead(p, c, g, ahead, exhausted, target)
+                                   : claim_work(p, c, g, exhausted, target);
+            ahead = NO_CLAIM;
             last_reduce = it.x == ITEM_REDUCE;
             if (p.mode == MK_MODE_ADAPTIVE) target = ld_relaxed_gpu(&c.hdr->target_nr);   // used by the next claim
             if (!wait_bar<true>(smem_u32(&s.wempty[wq]), wphase ^ 1u, c, SITE_WORK_EMPTY, 0)) break;
@@ -1391,6 +1419,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (it.x == ITEM_REDUCE) ring_free_at = pushed;
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
+        if (ahead_mode) ahead = atomicAdd(&c.hdr->compute_next, 1u);   // consumed at the next claim
         const int u = it.y;
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
         // tile owners exist only with 128-column tiles: the 256-column kernel keeps one unit per item
