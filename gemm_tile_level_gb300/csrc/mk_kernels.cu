@@ -28,7 +28,9 @@
 // Two more ways to form the sum use the compute blocks alone (no reduce role):
 //   chained    : the epilogue of (tile, r) acquires flag[tile][r-1], adds its accumulator to the
 //                running sum of ranks 0..r-1 and stores it (rank P-1 writes the output): the
-//                reduce role's additions in its order, so the same bits;
+//                reduce role's additions in its order, so the same bits.  On a short M one SM
+//                pair owns each 256 x 128 tile instead, computes its P ranks in turn and keeps
+//                the running sum in TMEM (owner_tile);
 //   accumulate : the epilogue adds its accumulator into one fp32 tile with L2 reductions, and
 //                the last of the P contributions writes the output (no fixed order).
 //
