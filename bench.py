@@ -269,6 +269,7 @@ _RASTER_GROUP = 0  # --raster-group (0 = chosen by the library)
 
 
 BF16_PARTIALS_FLAG = 128   # MK_FLAG_BF16_PARTIALS (--bf16-partials)
+B_NK_FLAG = 256            # MK_FLAG_B_NK (--b-nk)
 
 
 def split_opts(api, mk, split: str, comm_sms: int):
@@ -293,8 +294,10 @@ class Problem:
         self.wl = wl
         A, B = host if host is not None else ig.make_operands(wl)
         self.A_host, self.B_host = A, B
+        # the device copies of B: K_r x N, or N x K_r (a linear layer's weight) with --b-nk
+        self.B_dev_host = [np.ascontiguousarray(b.T) for b in B] if _EXTRA_FLAGS & B_NK_FLAG else B
         self.Ad = [api.bf16_device(a) for a in A]
-        self.Bd = [api.bf16_device(b) for b in B]
+        self.Bd = [api.bf16_device(b) for b in self.B_dev_host]
         out_t = torch.bfloat16 if wl.out_dtype == "bf16" else torch.float32
         self.out_code = mk.MK_BF16 if wl.out_dtype == "bf16" else mk.MK_F32
         self.rs = wl.op == "reducescatter"
@@ -454,6 +457,7 @@ def gpu_arm(args, wl, ranks):
                        "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype, "split": args.split,
                        "accumulate": "fp32", "seed": wl.seed, "tiles": args.tiles,
                        "partial_tiles": "bf16" if bf16_partials else "fp32",
+                       "b_layout": "N x K_r" if _EXTRA_FLAGS & B_NK_FLAG else "K_r x N",
                        "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
                        "parallelism": f"{wl.P} logical ranks on one GPU" + (
                            f"; {ranks.world} replicas" if ranks.world > 1 else "")},
@@ -477,7 +481,7 @@ def e2e_leg(torch, prob, opts, stream, steps, ranks):
     wl = prob.wl
     mk = prob.mk
     A_pin = [torch.from_numpy(a).view(torch.bfloat16).pin_memory() for a in prob.A_host]
-    B_pin = [torch.from_numpy(b).view(torch.bfloat16).pin_memory() for b in prob.B_host]
+    B_pin = [torch.from_numpy(b).view(torch.bfloat16).pin_memory() for b in prob.B_dev_host]
     outs = prob.C if isinstance(prob.C, list) else [prob.C]
     C_pin = [torch.empty(c.shape, dtype=c.dtype, pin_memory=True) for c in outs]
     h2d = sum(t.numel() * 2 for t in A_pin + B_pin)
@@ -591,7 +595,7 @@ def allgather_arm(args):
         ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
 
         def timed(mode, steps):
-            o = api.make_opts(mode, flags=_EXTRA_FLAGS & ~BF16_PARTIALS_FLAG)
+            o = api.make_opts(mode, flags=_EXTRA_FLAGS & ~(BF16_PARTIALS_FLAG | B_NK_FLAG))
             for _ in range(args.warmup):
                 mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -698,6 +702,8 @@ def main():
                     help="compute the P ranks of each tile back to back instead of band by band")
     ap.add_argument("--reduce-split", type=int, default=0,
                     help="column slices per output tile's reduction (0 = the library's choice)")
+    ap.add_argument("--b-nk", action="store_true",
+                    help="give each B_r as N x K_r (K contiguous, the layout of a linear layer's weight)")
     ap.add_argument("--bf16-partials", action="store_true",
                     help="adaptive / static / unfused splits: store partial tiles as bf16 (MK_FLAG_BF16_PARTIALS)")
     ap.add_argument("--shape", default="", help="P,M,N,K_per_rank override (same distributions); "
@@ -719,7 +725,8 @@ def main():
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     global _EXTRA_FLAGS, _REDUCE_SPLIT, _RASTER_GROUP
     _EXTRA_FLAGS = (2 if args.tiles == "single" else 0) | (8 if args.no_cooperative else 0) | \
-        (16 if args.tile_major else 0) | (BF16_PARTIALS_FLAG if args.bf16_partials else 0)
+        (16 if args.tile_major else 0) | (BF16_PARTIALS_FLAG if args.bf16_partials else 0) | \
+        (B_NK_FLAG if args.b_nk else 0)
     _REDUCE_SPLIT = args.reduce_split
     _RASTER_GROUP = args.raster_group
     if args.sweep:

@@ -246,10 +246,14 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
 
     MkParams p;
     memset(&p, 0, sizeof p);
+    // B as given (K_r x N, 64-column boxes), or N x K_r with one box of this CTA's B rows per
+    // K slice (all BN rows with one-SM tiles, BN/2 with SM pairs)
+    p.b_nk = (o.flags & MK_FLAG_B_NK) ? 1 : 0;
+    const int b_rows = pair ? g.bn / 2 : g.bn;
     for (int r = 0; r < P && Kr > 0; ++r) {
         st = encode_2d(&p.tmA[r], A[r], M, Kr, MK_BK, MK_BM);
         if (st != MK_OK) return st;
-        st = encode_2d(&p.tmB[r], B[r], Kr, N, 64, MK_BK);
+        st = p.b_nk ? encode_2d(&p.tmB[r], B[r], N, Kr, MK_BK, b_rows) : encode_2d(&p.tmB[r], B[r], Kr, N, 64, MK_BK);
         if (st != MK_OK) return st;
     }
     if (op == MK_IOP_RS) {
@@ -395,6 +399,8 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
                     "GEMM + ReduceScatter");
     if (o.flags & MK_FLAG_BF16_PARTIALS)
         return fail(MK_ERR_INVALID_ARG, "MK_FLAG_BF16_PARTIALS applies to GEMM + AllReduce and GEMM + ReduceScatter");
+    if (o.flags & MK_FLAG_B_NK)
+        return fail(MK_ERR_INVALID_ARG, "MK_FLAG_B_NK applies to GEMM + AllReduce and GEMM + ReduceScatter");
     if (N % 8 || K % 8)
         return fail(MK_ERR_UNSUPPORTED_SHAPE, "N=%lld and K=%lld must be multiples of 8", (long long)N, (long long)K);
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(MK_ERR_UNSUPPORTED_SHAPE, "dimension above 2^31-1");

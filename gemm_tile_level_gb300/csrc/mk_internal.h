@@ -62,7 +62,7 @@ static_assert(sizeof(MkWsHeader) == MK_WS_HEADER_BYTES, "workspace header size")
 // Launch parameters, passed as one __grid_constant__ kernel argument.
 struct MkParams {
     CUtensorMap tmA[MK_MAX_P];   // A_r: dims {K_r, M}, box {64, 128}, 128-byte swizzle
-    CUtensorMap tmB[MK_MAX_P];   // B_r: dims {N, K_r}, box {64, 64}, 128-byte swizzle
+    CUtensorMap tmB[MK_MAX_P];   // B_r: dims {N, K_r}, box {64, 64}; b_nk: dims {K_r, N}, box {64, B rows}; 128-byte swizzle
     void *out[MK_MAX_P];         // AR: distinct result buffers; RS: the P shards
     MkWsHeader *hdr;
     uint32_t *flags;             // [num_tiles][P] readiness flags (epoch-valued)
@@ -90,6 +90,7 @@ struct MkParams {
     int32_t ctrl_tail_ns;        // adaptive split: grid time per reduce item at the end of the call
     int32_t epi_pace_ns;         // pause between an epilogue's 32-column store chunks (0 = none)
     int32_t partial_bf16;        // role split / unfused: partial tiles stored as bf16 (RNE), summed in fp32
+    int32_t b_nk;                // B_r given as N x K_r (K-major operand; one TMA box of B rows per stage)
     int32_t chain_owner;         // chained mode, short M: one SM pair computes all P ranks of a tile in
                                  // rank order and keeps the running sum in registers (BN = 128 only)
 };

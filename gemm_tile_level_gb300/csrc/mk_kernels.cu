@@ -1169,10 +1169,14 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
             uint8_t *sb = sa + T::A_BYTES;
             mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
             tma_load_2d_hint(smem_u32(sa), &p.tmA[r], fb, kb * MK_BK, tm * MK_BM, pol_a);
+            if (p.b_nk) {   // B given as N x K_r: the tile's BN rows of this K slice, one box
+                tma_load_2d_hint(smem_u32(sb), &p.tmB[r], fb, kb * MK_BK, tn * BN, pol_b);
+            } else {
 #pragma unroll
-            for (int j = 0; j < T::B_BOXES; ++j)
-                tma_load_2d_hint(smem_u32(sb + j * T::B_BOX_BYTES), &p.tmB[r], fb, tn * BN + j * 64, kb * MK_BK,
-                                 pol_b);
+                for (int j = 0; j < T::B_BOXES; ++j)
+                    tma_load_2d_hint(smem_u32(sb + j * T::B_BOX_BYTES), &p.tmB[r], fb, tn * BN + j * 64,
+                                     kb * MK_BK, pol_b);
+            }
             ++s.issued;
             if (++stage == T::STAGES) {
                 stage = 0;
@@ -1191,6 +1195,9 @@ template <int BN>
 __device__ void run1_mma(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
                          uint32_t tmem_base) {
     using T = Cfg1<BN>;
+    const uint32_t b_lbo = p.b_nk ? 16u : static_cast<uint32_t>(T::B_BOX_BYTES);   // as in run2_mma
+    const uint64_t b_kstep = p.b_nk ? 2u : 128u;
+    const uint32_t idesc = p.b_nk ? (T::IDESC & ~(1u << 16)) : T::IDESC;
     int stage = 0, acc = 0, wq = 0;
     uint32_t phase = 0, aphase = 0, wphase = 0;
     for (;;) {
@@ -1218,12 +1225,12 @@ __device__ void run1_mma(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_
             const uint32_t sb = sa + T::A_BYTES;
             // A: K-major, rows 128 B apart, 8-row groups 1024 B apart; K step of 16 = +32 B.
             // B: MN-major, 64-column boxes 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO);
-            //    K step of 16 rows = +2048 B.
+            //    K step of 16 rows = +2048 B.  With b_nk, B is K-major like A.
             const uint64_t ad = sw128_desc(sa, 16, 1024);
-            const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
+            const uint64_t bd = sw128_desc(sb, b_lbo, 1024);
 #pragma unroll
             for (int kk = 0; kk < MK_BK / 16; ++kk)
-                umma_bf16(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128), T::IDESC,
+                umma_bf16(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk) * b_kstep, idesc,
                           static_cast<uint32_t>((kb | kk) != 0));
             umma_commit(smem_u32(&s.empty[stage]));
             if (++stage == T::STAGES) {
@@ -1459,10 +1466,15 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
                 const uint32_t sb = sa + T::A_BYTES;
                 mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
                 tma_load_2d_pair_hint(sa, amap, fb, kb * MK_BK, ay, pol_a);
+                if (p.b_nk) {   // B given as N x K_r: this CTA's BN/2 rows of the K slice, one box
+                    tma_load_2d_pair_hint(sb, &p.tmB[r], fb, kb * MK_BK, tn * BN + static_cast<int>(crank) * (BN / 2),
+                                          pol_b);
+                } else {
 #pragma unroll
-                for (int j = 0; j < T::B_BOXES; ++j)
-                    tma_load_2d_pair_hint(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
-                                          tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK, pol_b);
+                    for (int j = 0; j < T::B_BOXES; ++j)
+                        tma_load_2d_pair_hint(sb + j * T::B_BOX_BYTES, &p.tmB[r], fb,
+                                              tn * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * MK_BK, pol_b);
+                }
                 ++s.issued;
                 if (++stage == T::STAGES) {
                     stage = 0;
@@ -1483,6 +1495,11 @@ template <int BN>
 __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
                          uint32_t tmem_base) {
     using T = Cfg2<BN>;
+    // B operand: MN-major 64-column boxes (K x N input; K advances by 16 rows = 2 KiB), or K-major
+    // rows like A (N x K input; K advances by 16 elements = 32 bytes), descriptor units of 16 bytes
+    const uint32_t b_lbo = p.b_nk ? 16u : static_cast<uint32_t>(T::B_BOX_BYTES);
+    const uint64_t b_kstep = p.b_nk ? 2u : 128u;
+    const uint32_t idesc = p.b_nk ? (T::IDESC & ~(1u << 16)) : T::IDESC;
     int stage = 0, acc = 0, wq = 0;
     uint32_t phase = 0, aphase = 0, wphase = 0;
     for (;;) {
@@ -1518,11 +1535,11 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
                 // Per-CTA halves at identical offsets in both CTAs: A 128 rows (K-major), B BN/2
                 // columns (MN-major, 64-column boxes 8 KiB apart).
                 const uint64_t ad = sw128_desc(sa, 16, 1024);
-                const uint64_t bd = sw128_desc(sb, T::B_BOX_BYTES, 1024);
+                const uint64_t bd = sw128_desc(sb, b_lbo, 1024);
 #pragma unroll
                 for (int kk = 0; kk < MK_BK / 16; ++kk)
-                    umma_bf16_pair(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
-                                   T::IDESC, static_cast<uint32_t>((kb | kk) != 0));
+                    umma_bf16_pair(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk) * b_kstep,
+                                   idesc, static_cast<uint32_t>((kb | kk) != 0));
                 umma_commit_pair(smem_u32(&s.empty[stage]), 0x3);
                 if (++stage == T::STAGES) {
                     stage = 0;

@@ -238,7 +238,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
 }
 
 // Instruction descriptor for kind::f16: fp32 accumulator (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
+// (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1; cleared for a
+// K-major B),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |

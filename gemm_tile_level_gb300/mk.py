@@ -44,6 +44,7 @@ MK_FLAG_TILE_MAJOR = 16
 MK_FLAG_RANK_MAJOR = 32
 MK_FLAG_NO_EPILOGUE_PACING = 64
 MK_FLAG_BF16_PARTIALS = 128
+MK_FLAG_B_NK = 256
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",

@@ -99,6 +99,11 @@ typedef enum {
                                       rounding per partial.  MK_ERR_INVALID_ARG with the accumulate
                                       and chained splits and with mk_allgather_gemm (no partial
                                       tiles). */
+#define MK_FLAG_B_NK 256u         /* GEMM + AllReduce and GEMM + ReduceScatter: each B[r] is given as an
+                                     N x K_per_rank row-major matrix (K contiguous: the layout of a linear
+                                     layer's weight [out, in]) instead of K_per_rank x N; the operands are
+                                     then both K-major for the tensor cores.  The result is the same.
+                                     MK_ERR_INVALID_ARG with mk_allgather_gemm. */
 #define MK_FLAG_TILE_MAJOR 16u    /* compute the P ranks of each tile back to back */
 #define MK_FLAG_RANK_MAJOR 32u    /* compute bands of tile rows rank by rank (see raster_group); without
                                      either flag the order is rank-major for M >= 1024, else tile-major */

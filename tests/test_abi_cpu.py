@@ -136,6 +136,12 @@ def test_argument_checks_return_before_any_launch(mk):
     st = mk.mk_allgather_gemm(2, 256, 128, 64, [FAKE] * 2, [FAKE] * 2, [FAKE] * 2, [FAKE] * 2, mk.MK_BF16, FAKE,
                               ws_bytes=1 << 30, opts=o, stream=0)
     assert st == mk.MK_ERR_INVALID_ARG and "BF16_PARTIALS" in mk.mk_last_error()
+    # B given as N x K_r is for the row-parallel ops only
+    o = mk.mk_opts_default()
+    o.flags = mk.MK_FLAG_B_NK
+    st = mk.mk_allgather_gemm(2, 256, 128, 64, [FAKE] * 2, [FAKE] * 2, [FAKE] * 2, [FAKE] * 2, mk.MK_BF16, FAKE,
+                              ws_bytes=1 << 30, opts=o, stream=0)
+    assert st == mk.MK_ERR_INVALID_ARG and "B_NK" in mk.mk_last_error()
     # ReduceScatter needs M divisible by P
     st = mk.mk_gemm_reducescatter(3, 128, 128, 64, [FAKE] * 3, [FAKE] * 3, [FAKE] * 3, 0, FAKE,
                                   ws_bytes=1 << 30, stream=0)
