@@ -79,8 +79,12 @@ typedef enum {
                                r-1's release, adds its partial tile to the running sum of ranks
                                0..r-1 and stores it (rank P-1 writes the output).  The same fp32
                                additions in the same order as the reduce role, so the same bits
-                               (AllReduce and ReduceScatter only).  Uses one-SM tiles for
-                               M <= 512. */
+                               (AllReduce and ReduceScatter only).  For M <= 256 one SM pair
+                               instead computes all P ranks of a 256 x 128 tile in rank order
+                               and keeps the running sum in tensor memory (the same additions);
+                               for 256 < M <= 512 it uses one-SM tiles.  A tile-kind or
+                               unit-order flag, or debug_skip_unit, selects the rank-ordered
+                               chain at any M. */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */
