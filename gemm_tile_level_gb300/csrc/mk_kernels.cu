@@ -769,15 +769,19 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
     const bool last = r == p.P - 1;
     float *S = partial_tile<BN>(p, 0, lt);
     const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+    // The running sum is private to this mode, so it has a layout of its own: [BN/8 column
+    // groups][128 rows][8 floats], which a thread reads and writes with 32-byte accesses (half the
+    // store instructions of 16-byte ones; measured 1-2 % faster, and the stores are what the fold
+    // costs the GEMM).
 #pragma unroll 1
     for (int cc = 0; cc < BN / 64; ++cc) {
         const int col0 = half * (BN / 2) + cc * 32;
-        float *base = S + (static_cast<size_t>(col0 >> 2) * MK_BM + row) * 4;
+        float *base = S + (static_cast<size_t>(col0 >> 3) * MK_BM + row) * 8;
         // the running sum's loads go out first, so that their L2 latency overlaps the TMEM load
-        float4 sv[8];
+        float sv[4][8];
         if (r > 0) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sv[q] = ld_cg_f4(reinterpret_cast<const float4 *>(base + q * MK_BM * 4));
+            for (int q = 0; q < 4; ++q) ld_cg_f8(base + q * MK_BM * 8, sv[q]);
         }
         uint32_t v[32];
         if (p.num_kb > 0) {
@@ -786,29 +790,25 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
 #pragma unroll
             for (int q = 0; q < 32; ++q) v[q] = 0u;
         }
-        float4 x[8];
+        float x[4][8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            x[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                               __uint_as_float(v[4 * q + 3]));
-        if (r > 0) {
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
-                x[q].x = sv[q].x + x[q].x; x[q].y = sv[q].y + x[q].y;
-                x[q].z = sv[q].z + x[q].z; x[q].w = sv[q].w + x[q].w;
-            }
-        }
+            for (int j = 0; j < 8; ++j)   // S_{r-1} + p_r (fp32 addition commutes bit for bit)
+                x[q][j] = r > 0 ? sv[q][j] + __uint_as_float(v[8 * q + j]) : __uint_as_float(v[8 * q + j]);
         if (last) {
             if (grow < p.M) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int gcol = tn * BN + col0 + 8 * q;
-                    if (gcol < p.N) store_out8(p, grow, gcol, x[2 * q], x[2 * q + 1]);
+                    if (gcol < p.N)
+                        store_out8(p, grow, gcol, make_float4(x[q][0], x[q][1], x[q][2], x[q][3]),
+                                   make_float4(x[q][4], x[q][5], x[q][6], x[q][7]));
                 }
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) st_f4_hint(base + q * MK_BM * 4, x[q].x, x[q].y, x[q].z, x[q].w, pol);
+            for (int q = 0; q < 4; ++q) st_f8_hint(base + q * MK_BM * 8, x[q], pol);
         }
         epilogue_pace(p);
     }

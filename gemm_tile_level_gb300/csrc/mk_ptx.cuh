@@ -423,6 +423,20 @@ __device__ __forceinline__ void st_f4(void *p, float a, float b, float c, float 
                  : "memory");
 }
 
+// 32-byte load of eight floats, cached in L2 only (the address is 32-byte aligned).
+__device__ __forceinline__ void ld_cg_f8(const float *p, float (&v)[8]) {
+    asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+
+// 32-byte store of eight floats with an L2 eviction-priority policy (32-byte aligned address).
+__device__ __forceinline__ void st_f8_hint(float *p, const float (&v)[8], uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "f"(v[0]),
+                 "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "l"(policy)
+                 : "memory");
+}
+
 // 16-byte store with an L2 eviction-priority policy.
 __device__ __forceinline__ void st_f4_hint(void *p, float a, float b, float c, float d, uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
