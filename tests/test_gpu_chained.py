@@ -155,3 +155,16 @@ def test_mid_workload_full_oracle_and_same_bits():
     got = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=ch_opts())
     gu.check_tolerance(gu.host_values(got), oracle.allreduce(A, B), out_bf16=True)
     assert torch.equal(got, gu.call_ar(Ad, Bd, mk.MK_BF16))
+
+
+@pytest.mark.parametrize("num_ctas", [4, 10, 34])
+@pytest.mark.parametrize("M", [256, 1024])   # tile owners; the rank-ordered chain
+def test_small_grids(num_ctas, M):
+    """Few SM pairs, so that every pair claims many tiles (or units) one ahead of the one it
+    computes: the result must not depend on the grid."""
+    P, N, Kr = 8, 1024, 128
+    wl = ig.Workload("ch_grid", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32", seed=M + num_ctas)
+    A, B, Ad, Bd = gu.upload(wl)
+    ref = gu.rounded_reference(oracle.allreduce(A, B), False)
+    C = gu.call_ar(Ad, Bd, mk.MK_F32, opts=ch_opts(num_ctas=num_ctas))
+    gu.assert_bit_exact(gu.host_values(C), ref)
