@@ -207,7 +207,8 @@ size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank
  * communication; reduction of the ranks' partial tiles, then broadcast of the
  * result.)
  *   A[r] : M x K_per_rank bf16   (rank r's slice of the activations' K)
- *   B[r] : K_per_rank x N bf16   (rank r's slice of the weight rows)
+ *   B[r] : K_per_rank x N bf16   (rank r's slice of the weight rows; N x K_per_rank with
+ *          MK_FLAG_B_NK)
  *   C[r] : M x N, out_dtype      (rank r's copy of the result; entries may
  *                                 alias: each distinct pointer is written once)
  * The sum over ranks is taken in fixed order r = 0, 1, ..., P-1 on fp32
