@@ -61,6 +61,20 @@ int main(void) {
     assert got == want
 
 
+def test_constants_match_header(mk):
+    """Every MK_FLAG_* bit, status code, split mode, op and dtype the header defines has the same
+    value in the binding (a wrong flag bit would silently select another layout or mode)."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    flags = dict(re.findall(r"#define\s+(MK_FLAG_[A-Z0-9_]+)\s+(\d+)u", src))
+    assert flags, "no MK_FLAG_ definitions found"
+    for name, value in flags.items():
+        assert getattr(mk, name) == int(value), name
+    enums = dict(re.findall(r"\b(MK_(?:ERR|OK|SPLIT|OP|BF16|F32)[A-Z0-9_]*)\s*=\s*(\d+)", src))
+    assert len(enums) >= 15
+    for name, value in enums.items():
+        assert getattr(mk, name) == int(value), name
+
+
 def test_defaults_and_strings(mk):
     o = mk.mk_opts_default()
     assert o.split_mode == mk.MK_SPLIT_ADAPTIVE and o.debug_skip_unit == -1
