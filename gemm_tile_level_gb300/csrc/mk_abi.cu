@@ -537,6 +537,14 @@ size_t mk_internal_flags_bytes(int P, int64_t M, int64_t N, int64_t K_per_rank) 
     return g.partials_off - g.flags_off;
 }
 
+bool mk_internal_accumulator_region(int P, int64_t M, int64_t N, int64_t K_per_rank, size_t *offset, size_t *bytes) {
+    Geometry g;
+    if (!make_geometry(P, M, N, K_per_rank, &g)) return false;
+    *offset = g.partials_off;
+    *bytes = static_cast<size_t>(g.num_tiles) * MK_BM * g.bn * sizeof(float);
+    return true;
+}
+
 extern "C" {
 
 void mk_opts_default(mk_opts *o) {

@@ -99,6 +99,9 @@ struct MkParams {
 // flag region (which follows the 256-byte header) of the AllReduce workspace for a shape.
 void mk_internal_set_error(const char *msg);
 size_t mk_internal_flags_bytes(int P, int64_t M, int64_t N, int64_t K_per_rank);
+// Offset and bytes of the accumulator tiles an accumulate-mode call (MK_SPLIT_ACCUMULATE) of this
+// shape adds into: one fp32 tile per output tile at the start of the partial-tile region.
+bool mk_internal_accumulator_region(int P, int64_t M, int64_t N, int64_t K_per_rank, size_t *offset, size_t *bytes);
 
 // Implemented in mk_kernels.cu.  `pair` selects the SM-pair (cta_group::2, 256 x BN) kernel,
 // otherwise the one-SM (128 x BN) kernel.

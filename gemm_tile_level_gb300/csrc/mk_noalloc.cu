@@ -7,6 +7,7 @@
 // mk_gemm_allreduce needs (partial tiles, readiness flags, counters) lives in the library
 // itself: one file-scope device array per GPU that loads libmk.so, held until the process
 // exits.  The caller still owns and passes the operands and the outputs.
+#include <cstddef>
 #include <cstdio>
 #include <mutex>
 
@@ -14,6 +15,8 @@
 #include "mk_internal.h"
 
 namespace {
+
+static_assert(MK_ACC_FRESH == 0, "a zeroed header marks the accumulator tiles fresh");
 
 // The library-owned workspace.  In host code `g_noalloc_ws` is only a host-side stand-in for
 // the symbol, never a device address: the address is obtained per device below.
@@ -79,12 +82,28 @@ extern "C" mk_status mk_gemm_allreduce_noalloc(int P, int64_t M, int64_t N, int6
     // The readiness flags move with the shape, so a previous call's partial tiles may now sit
     // where this call's flags live: clear them (stream-ordered, no allocation).  The header
     // keeps the call epoch and stays as the last call left it.
+    const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    unsigned char *wsb = static_cast<unsigned char *>(ws);
     const size_t flags = need ? mk_internal_flags_bytes(P, M, N, K_per_rank) : 0;
     if (flags && M > 0 && N > 0) {
-        e = cudaMemsetAsync(static_cast<unsigned char *>(ws) + MK_WS_HEADER_BYTES, 0, flags,
-                            static_cast<cudaStream_t>(cuda_stream));
+        e = cudaMemsetAsync(wsb + MK_WS_HEADER_BYTES, 0, flags, stream);
         if (e != cudaSuccess) {
             mk_internal_set_error("mk_gemm_allreduce_noalloc: clearing the flag region failed");
+            return MK_ERR_CUDA;
+        }
+    }
+    // An accumulate-mode call adds into fp32 accumulator tiles that must start at zero, and the
+    // kernel refuses to run (recording the refusal only in the header, which this entry point
+    // never reads) unless the header says they are.  Every other mode leaves partial tiles
+    // there, so clear the accumulators and mark them fresh before each accumulate call.
+    const bool accumulate = opts && opts->split_mode == MK_SPLIT_ACCUMULATE;
+    size_t acc_off = 0, acc_bytes = 0;
+    if (accumulate && M > 0 && N > 0 && mk_internal_accumulator_region(P, M, N, K_per_rank, &acc_off, &acc_bytes)) {
+        e = cudaMemsetAsync(wsb + acc_off, 0, acc_bytes, stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(wsb + offsetof(MkWsHeader, acc_state), 0, sizeof(uint32_t), stream);   // MK_ACC_FRESH
+        if (e != cudaSuccess) {
+            mk_internal_set_error("mk_gemm_allreduce_noalloc: clearing the accumulator tiles failed");
             return MK_ERR_CUDA;
         }
     }

@@ -270,10 +270,16 @@ mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *
  *   each call clears the part that must start at zero.  Calls whose kernels overlap
  *   on the GPU (different streams without ordering, or several host threads) race on
  *   the array and give wrong results: order them.
- *   The return value covers argument, size and launch errors.  Errors the kernel
- *   detects (a bounded wait that ran out) are recorded in the static array and are
- *   not reported here; callers that need them use mk_gemm_allreduce and
- *   mk_status_check with a workspace of their own.
+ *   Every split mode is accepted.  Before an MK_SPLIT_ACCUMULATE call the entry
+ *   point also clears the accumulator tiles (stream-ordered memsets), so accumulate
+ *   calls work after calls in any other mode.
+ *   The return value covers argument, size and launch errors.  What the kernel itself
+ *   detects is recorded in the static array and is not reported here: a bounded wait
+ *   that ran out (MK_ERR_TIMEOUT: a wait_timeout_ns too short for the shape, or a
+ *   withheld unit from debug_skip_unit) and, in accumulate mode, an output tile that
+ *   did not receive all P contributions (MK_ERR_INTERNAL).  In either case some output
+ *   tiles may be left unwritten.  Callers that need these errors use
+ *   mk_gemm_allreduce and mk_status_check with a workspace of their own.
  *   This entry point calls no allocating routine.
  */
 #define MK_NOALLOC_MAX_WS_BYTES (64u << 20)
