@@ -235,6 +235,18 @@ class Ranks:
             self.dist.destroy_process_group()
 
 
+def workload_config(args, wl, world: int = 1) -> dict:
+    """The `config` object of the JSON line: the same keys for the GPU arm and the reference arm."""
+    bf16_partials = bool(_EXTRA_FLAGS & BF16_PARTIALS_FLAG) and args.split in ("adaptive", "static", "unfused")
+    return {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
+            "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype, "split": args.split,
+            "accumulate": "fp32", "seed": wl.seed, "tiles": args.tiles,
+            "partial_tiles": "bf16" if bf16_partials else "fp32",
+            "b_layout": "N x K_r" if _EXTRA_FLAGS & B_NK_FLAG else "K_r x N",
+            "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
+            "parallelism": f"{wl.P} logical ranks on one GPU" + (f"; {world} replicas" if world > 1 else "")}
+
+
 def reference_arm(args, wl, ranks):
     """--impl reference: the fp64 oracle on host cores, rank 0 only."""
     if ranks.rank != 0:
@@ -254,8 +266,7 @@ def reference_arm(args, wl, ranks):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
-                       "K_per_rank": wl.Kr, "implementation": "fp64 CPU oracle"},
+            "config": workload_config(args, wl, ranks.world), "implementation": "fp64 CPU oracle",
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -418,7 +429,20 @@ def gpu_arm(args, wl, ranks):
                        "note": "MK_SPLIT_CHAINED: each rank's epilogue adds its tile to the running sum of the ranks "
                                "before it, in rank order (the reduce role's additions, same bits)"}
 
+        # ---------------- the controller's trace of one adaptive call (Figure 7a of the method)
+        if args.trace:
+            trace_leg(torch, api, mk, prob, stream, args.trace, "adaptive")
+
     peaks, peak_src = load_peaks()
+
+    # ---------------- every other configuration, on the same GPU in the same run
+    A_host, B_host = prob.A_host, prob.B_host
+    configs = None
+    if not args.no_configs and not args.shape and args.workload == DEFAULT_WORKLOAD and ranks.world == 1:
+        del prob
+        torch.cuda.empty_cache()
+        with torch.cuda.stream(stream):
+            configs = configs_leg(torch, api, mk, stream, peaks, args.config_steps, 3)
     kernel_ms = statistics.mean(per_launch)
     achieved = wl.flops / (kernel_ms * 1e-3) / 1e12
     bf16_partials = bool(_EXTRA_FLAGS & BF16_PARTIALS_FLAG) and args.split in ("adaptive", "static", "unfused")
@@ -444,7 +468,7 @@ def gpu_arm(args, wl, ranks):
         return
     cpu = None
     if not args.no_cpu_baseline and ranks.world == 1:
-        v, rows, secs = time_oracle(wl, prob.A_host, prob.B_host, target_s=args.cpu_seconds)
+        v, rows, secs = time_oracle(wl, A_host, B_host, target_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"rows 0..{rows - 1} of {wl.M}, all N={wl.N}, all P={wl.P} ranks, "
                          f"K_r={wl.Kr}; {secs:.1f} s fp64"}
@@ -453,21 +477,99 @@ def gpu_arm(args, wl, ranks):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": wl.name, "op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N,
-                       "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype, "split": args.split,
-                       "accumulate": "fp32", "seed": wl.seed, "tiles": args.tiles,
-                       "partial_tiles": "bf16" if bf16_partials else "fp32",
-                       "b_layout": "N x K_r" if _EXTRA_FLAGS & B_NK_FLAG else "K_r x N",
-                       "l2": "operands %.0f MB > 129 MB L2, no flush" % ((wl.P * (wl.M + wl.N) * wl.Kr * 2) / 1e6),
-                       "parallelism": f"{wl.P} logical ranks on one GPU" + (
-                           f"; {ranks.world} replicas" if ranks.world > 1 else "")},
+            "config": workload_config(args, wl, ranks.world),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * (2 if args.split == "unfused" else 1),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "unfused_baseline": unfused, "adaptive_split": adaptive, "accumulate_variant": accumulate,
-            "chained_variant": chained}
+            "chained_variant": chained, "configs": configs}
     print(json.dumps(line), flush=True)
+
+
+def roofline_of(flops: float, nbytes: float, ms: float, peaks: dict) -> dict:
+    """Bound and achieved fraction of max(FLOPs / tensor peak, bytes / HBM bandwidth) for one call."""
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    return {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "frac": max(t_tensor, t_hbm) / (ms * 1e-3),
+            "roofline_ms": max(t_tensor, t_hbm) * 1e3}
+
+
+CONFIG_WORKLOADS = ("ar_p2_m128_n128_k256", "ar_p8_m2048_n4096_k512", "rs_p8_m16384_n8192_k1024",
+                    "ar_sweep_p8_m256_n8192_k1024", "ar_sweep_p8_m4096_n8192_k1024")
+CONFIG_SPLITS = ("chained", "adaptive", "unfused", "accumulate")
+AG_SHAPE = (8, 8192, 3584, 4096)
+
+
+def configs_leg(torch, api, mk, stream, peaks, steps: int, warmup: int):
+    """Every other configuration of the study, timed on the same GPU in the same run: ms per call,
+    TFLOP/s and the roofline fraction of each split (the chained default, the controller-driven
+    role split, the unfused two-kernel baseline and the accumulate variant), then AllGather + GEMM
+    fused against unfused.  About 20 calls per point."""
+    out = {}
+    for name in CONFIG_WORKLOADS:
+        wl = workload_by_name(name)
+        prob = Problem(wl, torch, api, mk)
+        nbytes = algorithmic_bytes(wl, 4)
+        rec = {"op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N, "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype,
+               "flops": wl.flops, "algorithmic_bytes": nbytes, "steps": steps}
+        for split in CONFIG_SPLITS:
+            if split == "accumulate":
+                prob.ws.zero_()   # the other modes leave partial tiles where its accumulators go
+            tot, _ = time_launches(torch, prob, split_opts(api, mk, split, 0), steps, warmup, stream)
+            ms = tot / steps
+            rf = roofline_of(wl.flops, nbytes, ms, peaks)
+            rec["bound"] = rf["bound"]
+            rec["roofline_ms"] = rf["roofline_ms"]
+            rec[split] = {"ms": ms, "us": ms * 1e3, "tflops": wl.flops / (ms * 1e-3) / 1e12,
+                          "roofline_frac": rf["frac"]}
+        rec["chained_over_unfused"] = rec["chained"]["ms"] / rec["unfused"]["ms"]
+        rec["adaptive_over_unfused"] = rec["adaptive"]["ms"] / rec["unfused"]["ms"]
+        out[name] = rec
+        del prob
+        torch.cuda.empty_cache()
+    P, M, N, K = AG_SHAPE
+    ag = AgProblem(torch, api, mk, P, M, N, K)
+    rec = {"op": "allgather_gemm", "P": P, "M": M, "N": N, "K": K, "out_dtype": "bf16", "flops": ag.flops,
+           "algorithmic_bytes": ag.nbytes, "steps": steps}
+    for split, mode in (("fused", mk.MK_SPLIT_ADAPTIVE), ("unfused", mk.MK_SPLIT_UNFUSED)):
+        ms = ag.time(mode, steps, warmup, stream)
+        rf = roofline_of(ag.flops, ag.nbytes, ms, peaks)
+        rec["bound"] = rf["bound"]
+        rec["roofline_ms"] = rf["roofline_ms"]
+        rec[split] = {"ms": ms, "us": ms * 1e3, "tflops": ag.flops / (ms * 1e-3) / 1e12, "roofline_frac": rf["frac"]}
+    rec["fused_over_unfused"] = rec["fused"]["ms"] / rec["unfused"]["ms"]
+    out[f"ag_p{P}_m{M}_n{N}_k{K}"] = rec
+    del ag
+    torch.cuda.empty_cache()
+    return out
+
+
+def trace_leg(torch, api, mk, prob, stream, path: str, split: str, comm_sms: int = 0):
+    """One call with the controller's trace buffer attached; writes its records (time, published
+    reduce-role SMs, compute units and reduce items finished) to `path` as JSON."""
+    cap = 1 << 16
+    buf = torch.zeros(cap * 32, dtype=torch.uint8, device="cuda")
+    opts = split_opts(api, mk, split, comm_sms)
+    opts.trace = buf.data_ptr()
+    opts.trace_bytes = buf.numel()
+    mk.check(prob.call(opts, stream))
+    mk.check(mk.mk_status_check(prob.ws, stream))
+    hdr = prob.ws[:64].cpu().numpy().view(np.uint32)
+    n = int(hdr[9])   # trace_count of the workspace header
+    recs = buf[: n * 32].cpu().numpy().view(np.uint64).reshape(-1, 4)
+    rows = []
+    for r in recs:
+        t_ns = int(r[0])
+        w1, w2 = int(r[1]), int(r[2])
+        rows.append({"t_ns": t_ns, "target_sms": w1 & 0xFFFFFFFF, "units_done": w1 >> 32,
+                     "tiles_done": w2 & 0xFFFFFFFF, "num_blocks": w2 >> 32})
+    wl = prob.wl
+    doc = {"workload": wl.name, "split": split, "comm_sms": comm_sms, "P": wl.P, "M": wl.M, "N": wl.N,
+           "K_per_rank": wl.Kr, "records": rows}
+    with open(path, "w") as f:
+        json.dump(doc, f)
+    return len(rows)
 
 
 def e2e_leg(torch, prob, opts, stream, steps, ranks):
@@ -569,6 +671,47 @@ def e2e_leg(torch, prob, opts, stream, steps, ranks):
 
 
 # ------------------------------------------------------------------ AllGather + GEMM
+class AgProblem:
+    """Device-resident operands, gathered buffers, outputs and workspace of AllGather + GEMM: P
+    row shards of A ((M/P) x K, N(0,1)) and P column shards of B (K x N, N(0,1/K)), seed 0."""
+
+    def __init__(self, torch, api, mk, P, M, N, K):
+        self.torch, self.api, self.mk = torch, api, mk
+        self.P, self.M, self.N, self.K = P, M, N, K
+        A = [np.empty((M // P, K), np.uint16) for _ in range(P)]
+        B = [np.empty((K, N), np.uint16) for _ in range(P)]
+        for r in range(P):
+            ig.fill_bf16(A[r].reshape(-1), ig.normal(1.0), 0, r, ig.TID_A)
+            ig.fill_bf16(B[r].reshape(-1), ig.normal(1.0 / K), 0, r, ig.TID_B)
+        self.flops = 2.0 * P * M * N * K
+        # shards read once, P gathered copies written and read, B once, P outputs written
+        self.nbytes = M * K * 2 + 2 * P * M * K * 2 + P * K * N * 2 + P * M * N * 2
+        self.Ad = [api.bf16_device(a) for a in A]
+        self.Bd = [api.bf16_device(b) for b in B]
+        self.C = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        self.G = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        self.ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
+
+    def call(self, mode, stream):
+        o = self.api.make_opts(mode, flags=_EXTRA_FLAGS & ~(BF16_PARTIALS_FLAG | B_NK_FLAG))
+        return self.mk.mk_allgather_gemm(self.P, self.M, self.N, self.K, self.Ad, self.Bd, self.G, self.C,
+                                         self.mk.MK_BF16, self.ws, opts=o, stream=stream)
+
+    def time(self, mode, steps, warmup, stream) -> float:
+        torch, mk = self.torch, self.mk
+        for _ in range(warmup):
+            mk.check(self.call(mode, stream))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            mk.check(self.call(mode, stream))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mk.check(mk.mk_status_check(self.ws, stream))
+        return e0.elapsed_time(e1) / steps
+
+
 def allgather_arm(args):
     """`--op allgather`: the fused AllGather + GEMM (communication pairs gather 128-row chunks of
     the row-sharded A into every rank's buffer, compute pairs multiply as chunks arrive) against
@@ -581,39 +724,15 @@ def allgather_arm(args):
     P, M, N, K = (int(x) for x in args.ag_shape.split(","))
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
-    A = [np.empty((M // P, K), np.uint16) for _ in range(P)]
-    B = [np.empty((K, N), np.uint16) for _ in range(P)]
-    for r in range(P):
-        ig.fill_bf16(A[r].reshape(-1), ig.normal(1.0), 0, r, ig.TID_A)
-        ig.fill_bf16(B[r].reshape(-1), ig.normal(1.0 / K), 0, r, ig.TID_B)
-    flops = 2.0 * P * M * N * K
     with torch.cuda.stream(stream):
-        Ad = [api.bf16_device(a) for a in A]
-        Bd = [api.bf16_device(b) for b in B]
-        C = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-        G = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-        ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
-
-        def timed(mode, steps):
-            o = api.make_opts(mode, flags=_EXTRA_FLAGS & ~(BF16_PARTIALS_FLAG | B_NK_FLAG))
-            for _ in range(args.warmup):
-                mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            e0.record(stream)
-            for _ in range(steps):
-                mk.check(mk.mk_allgather_gemm(P, M, N, K, Ad, Bd, G, C, mk.MK_BF16, ws, opts=o, stream=stream))
-            e1.record(stream)
-            torch.cuda.synchronize()
-            mk.check(mk.mk_status_check(ws, stream))
-            return e0.elapsed_time(e1) / steps
-
+        ag = AgProblem(torch, api, mk, P, M, N, K)
         clocks = ClockSampler(0)
         clocks.start()
-        fused_ms = timed(mk.MK_SPLIT_ADAPTIVE, args.steps)
+        fused_ms = ag.time(mk.MK_SPLIT_ADAPTIVE, args.steps, args.warmup, stream)
         clocks.stop()
-        unfused_ms = timed(mk.MK_SPLIT_UNFUSED, max(3, min(args.steps, 50)))
+        unfused_ms = ag.time(mk.MK_SPLIT_UNFUSED, max(3, min(args.steps, 50)), args.warmup, stream)
     peaks, peak_src = load_peaks()
+    flops = ag.flops
     value = flops / (fused_ms * 1e-3) / 1e12
     clk = clocks.summary()
     line = {"metric": "fused AllGather+GEMM TFLOP/s on 1 GB300", "value": value, "unit": "TFLOP/s", "n_gpus": 1,
@@ -642,8 +761,12 @@ def sweep(args):
     stream = torch.cuda.Stream()
     results = []
     with torch.cuda.stream(stream):
-        for M in (args.sweep_m or ig.SWEEP_M):
-            wl = ig.sweep_workload(M)
+        if args.sweep_workload:
+            wls = [workload_by_name(n) for n in args.sweep_workload]
+        else:
+            wls = [ig.sweep_workload(M) for M in (args.sweep_m or ig.SWEEP_M)]
+        for wl in wls:
+            M = wl.M
             prob = Problem(wl, torch, api, mk)
             steps, warm = args.sweep_steps, 2
 
@@ -664,7 +787,11 @@ def sweep(args):
             acc = ms(split_opts(api, mk, "accumulate", 0))
             chn = ms(split_opts(api, mk, "chained", 0))
             best_nr = min(static, key=static.get)
-            rec = {"M": M, "adaptive_ms": adaptive, "best_static_ms": static[best_nr],
+            if args.sweep_trace_dir:
+                os.makedirs(args.sweep_trace_dir, exist_ok=True)
+                trace_leg(torch, api, mk, prob, stream, os.path.join(args.sweep_trace_dir, f"{wl.name}_adaptive.json"),
+                          "adaptive")
+            rec = {"workload": wl.name, "M": M, "adaptive_ms": adaptive, "best_static_ms": static[best_nr],
                    "best_static_comm_sms": best_nr, "adaptive_over_best_static": adaptive / static[best_nr],
                    "unfused_ms": unf, "fused_over_unfused": adaptive / unf,
                    "accumulate_ms": acc, "accumulate_over_unfused": acc / unf,
@@ -721,6 +848,15 @@ def main():
     ap.add_argument("--sweep-steps", type=int, default=10)
     ap.add_argument("--sweep-stride", type=int, default=1)
     ap.add_argument("--sweep-out", default="")
+    ap.add_argument("--sweep-workload", nargs="*", default=[],
+                    help="sweep these workloads instead of the M sweep (e.g. the MLP or ReduceScatter shape)")
+    ap.add_argument("--sweep-trace-dir", default="",
+                    help="also write one adaptive call's controller trace per swept workload into this folder")
+    ap.add_argument("--trace", default="",
+                    help="write the controller trace of one adaptive call of the workload to this JSON file")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other configurations (they run by default with the default workload)")
+    ap.add_argument("--config-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     global _EXTRA_FLAGS, _REDUCE_SPLIT, _RASTER_GROUP

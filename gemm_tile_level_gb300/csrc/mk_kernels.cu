@@ -588,9 +588,10 @@ __device__ void do_reduce(const MkParams &p, const Ctx &c, int tm, int tn, int s
     const bool exists = tm < p.tiles_m;
     const int lt = tm * p.tiles_n + tn;
     if (exists && etid < 32) ok = wait_tile_ready(p, c, lt, epoch, etid);
-    // partials written by other blocks' generic-proxy stores are read below by bulk copies
-    if (exists && ok && etid == 0) fence_proxy_async_global();
+    // The barrier orders every lane's flag acquire before what thread 0 does next; thread 0 then
+    // orders those acquires (generic proxy) before its bulk copies of the partials (async proxy).
     ok = bar_and(1, MK_EPI_THREADS, ok);
+    if (exists && ok && etid == 0) fence_proxy_async_global();
     if (exists && ok) {
         const long long t0 = clock64();
         reduce_tile_staged<BN>(p, c, tm, tn, sub, nsub, etid, st);

@@ -69,6 +69,7 @@ import bench, inputgen as ig
 
 class Args:
     warmup, steps, gpus, reference_step_s = 0, 1, 2, 0.05
+    split, tiles = "chained", "pair"
 
 r = bench.Ranks(2)
 wl = ig.WORKLOADS["ar_p2_m128_n128_k256"]
