@@ -154,3 +154,55 @@ def sweep_workload(M: int) -> Workload:
     """The SM-split sweep: GEMM+AllReduce, P=8, N=8192, K_r=1024, A ~ N(0,1), B ~ N(0,1/8192)."""
     return Workload(f"ar_sweep_p8_m{M}_n8192_k1024", "allreduce", 8, M, 8192, 1024, normal(1.0),
                     normal(1 / 8192), "bf16")
+
+
+# ---------------------------------------------------------------- Ring Attention (sequence parallel)
+TID_Q, TID_K, TID_V = 2, 3, 4
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """One seeded Ring Attention problem: P ranks, each holding a slice of S tokens of the sequence
+    as Q_r, K_r, V_r (H heads x S rows x d, bf16, row-major)."""
+    name: str
+    P: int
+    H: int
+    S: int
+    d: int
+    q_dist: tuple
+    k_dist: tuple
+    v_dist: tuple
+    out_dtype: str = "bf16"
+    seed: int = 0
+
+    @property
+    def flops(self) -> int:
+        """Q K^T and P V over the whole sequence: 4 * (P S)^2 * d per head."""
+        return 4 * (self.P * self.S) ** 2 * self.d * self.H
+
+    def with_shape(self, **kw) -> "AttnWorkload":
+        d = dict(name=self.name, P=self.P, H=self.H, S=self.S, d=self.d, q_dist=self.q_dist,
+                 k_dist=self.k_dist, v_dist=self.v_dist, out_dtype=self.out_dtype, seed=self.seed)
+        d.update(kw)
+        return AttnWorkload(**d)
+
+
+def make_attn_operands(wl: AttnWorkload):
+    """Return ([Q_r], [K_r], [V_r]) as uint16 bf16-bit arrays of shape (H, S, d), one per rank."""
+    Q, K, V = [], [], []
+    for r in range(wl.P):
+        for lst, dist, tid in ((Q, wl.q_dist, TID_Q), (K, wl.k_dist, TID_K), (V, wl.v_dist, TID_V)):
+            x = np.empty((wl.H, wl.S, wl.d), np.uint16)
+            fill_bf16(x.reshape(-1), dist, wl.seed, r, tid)
+            lst.append(x)
+    return Q, K, V
+
+
+# Sequence-parallel attention: a small case the oracle finishes in seconds, and a long-context
+# case (8 ranks x 4096 tokens = 32768 tokens, 32 heads of 128) for the bench.
+ATTN_WORKLOADS = {
+    "ring_p2_h2_s256_d128": AttnWorkload("ring_p2_h2_s256_d128", 2, 2, 256, 128, normal(1.0), normal(1.0),
+                                         normal(1.0)),
+    "ring_p8_h32_s4096_d128": AttnWorkload("ring_p8_h32_s4096_d128", 8, 32, 4096, 128, normal(1.0), normal(1.0),
+                                           normal(1.0)),
+}

@@ -12,8 +12,12 @@ tensor-parallel rows):
                           B column-sharded).
 Partial tiles stored at half width (bf16) are a variant of the boundary without a counterpart on
 those pages: ``allreduce_bf16_partials`` defines it.
-Parity pins: every function here is pinned by tests/test_oracle_pins.py against exact
-arithmetic, closed forms, invariants or numpy's fp64 matmul.
+Ring Attention (the same Table 3, row "Ring Attention (SP)"; the arithmetic is in
+``mk_oracle_attn.c``): every rank's queries attend, with softmax attention, to the keys and values
+of the whole sequence, whose P slices the ring brings to each rank in turn.
+Parity pins: every function here is pinned by tests/test_oracle_pins.py (the GEMM forms) and
+tests/test_oracle_attention_pins.py (Ring Attention) against exact arithmetic, closed forms,
+invariants, numpy's fp64 routines or a 50-digit brute force.
 """
 from __future__ import annotations
 
@@ -25,16 +29,18 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mk_oracle.c")
+_SRC_ATTN = os.path.join(_HERE, "mk_oracle_attn.c")
 _LIB = os.path.join(_HERE, "_libmk_oracle.so")
 _lib = None
 
 
 def build(force: bool = False) -> str:
     """Compile the oracle (gcc -O2, OpenMP over rows, no FP contraction)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_ATTN))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC",
-                               "-shared", "-o", tmp, _SRC, "-lm"])
+                               "-shared", "-o", tmp, _SRC, _SRC_ATTN, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -50,8 +56,10 @@ def _load():
         lib.mko_rank_sum_at.argtypes = [ctypes.c_int, i64, i64, vp, vp, i64, vp, vp, vp]
         lib.mko_round_bf16.argtypes = [vp, i64, vp]
         lib.mko_round_f32.argtypes = [vp, i64, vp]
+        lib.mko_attention_rows.argtypes = [ctypes.c_int, i64, i64, i64, vp, vp, vp, ctypes.c_int, i64, i64, vp,
+                                           ctypes.c_double, vp, vp, vp]
         for f in (lib.mko_gemm_rows, lib.mko_rank_sum_rows, lib.mko_rank_sum_at,
-                  lib.mko_round_bf16, lib.mko_round_f32):
+                  lib.mko_round_bf16, lib.mko_round_f32, lib.mko_attention_rows):
             f.restype = None
         _lib = lib
     return _lib
@@ -188,3 +196,57 @@ def bf16_to_f64(bits) -> np.ndarray:
     """Exact widening of bf16 bit patterns to fp64 (for comparisons)."""
     bits = np.asarray(bits, np.uint16)
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- Ring Attention
+def _check_attn(Q, K, V):
+    P = len(Q)
+    if P == 0 or len(K) != P or len(V) != P:
+        raise ValueError("need P >= 1 matching Q_r, K_r, V_r")
+    H, S, d = Q[0].shape
+    for x in list(Q) + list(K) + list(V):
+        if x.shape != (H, S, d):
+            raise ValueError("inconsistent rank shapes (each rank holds H x S x d)")
+    return P, H, S, d
+
+
+def attention_rows(Q, K, V, rank: int, head: int, rows, scale: float | None = None):
+    """Softmax attention of query rows ``rows`` of head ``head`` on rank ``rank`` over the keys and
+    values of every rank (fp64).  Q, K, V: lists of P arrays of bf16 bits, each H x S x d.  Returns
+    (O [n x d], lse [n], err [n x d]); lse is the natural-log logsumexp of the scaled scores and
+    err the scale of the error that rounding each probability would add (see mk_oracle_attn.c).
+    ``scale`` defaults to 1/sqrt(d)."""
+    Q = [_bits(x) for x in Q]
+    K = [_bits(x) for x in K]
+    V = [_bits(x) for x in V]
+    P, H, S, d = _check_attn(Q, K, V)
+    rows = np.ascontiguousarray(rows, np.int64)
+    assert 0 <= rank < P and 0 <= head < H and ((rows >= 0) & (rows < S)).all()
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    n = rows.size
+    O = np.empty((n, d), np.float64)
+    err = np.empty((n, d), np.float64)
+    lse = np.empty(n, np.float64)
+    if n and d:
+        _load().mko_attention_rows(P, H, S, d, _ptr_array(Q), _ptr_array(K), _ptr_array(V), rank, head, n,
+                                   rows.ctypes.data, float(scale), O.ctypes.data, lse.ctypes.data, err.ctypes.data)
+    return O, lse, err
+
+
+def ring_attention(Q, K, V, scale: float | None = None):
+    """The whole Ring Attention result: per rank, O_r (H x S x d), lse_r (H x S) and err_r (H x S x d),
+    fp64."""
+    P, H, S, d = _check_attn(Q, K, V)
+    outs, lses, errs = [], [], []
+    rows = np.arange(S, dtype=np.int64)
+    for r in range(P):
+        O = np.empty((H, S, d))
+        L = np.empty((H, S))
+        E = np.empty((H, S, d))
+        for h in range(H):
+            O[h], L[h], E[h] = attention_rows(Q, K, V, r, h, rows, scale)
+        outs.append(O)
+        lses.append(L)
+        errs.append(E)
+    return outs, lses, errs
