@@ -542,6 +542,7 @@ def configs_leg(torch, api, mk, stream, peaks, steps: int, warmup: int):
     out[f"ag_p{P}_m{M}_n{N}_k{K}"] = rec
     del ag
     torch.cuda.empty_cache()
+    out[RING_WORKLOAD] = ring_record(torch, api, mk, stream, peaks, max(3, steps // 4), 2)
     return out
 
 
@@ -712,6 +713,109 @@ class AgProblem:
         return e0.elapsed_time(e1) / steps
 
 
+class RingProblem:
+    """Device-resident Q, K, V of every rank, outputs, logsumexp, ring buffers and workspace of one
+    Ring Attention workload (inputgen.ATTN_WORKLOADS)."""
+
+    def __init__(self, torch, api, mk, wl):
+        self.torch, self.api, self.mk, self.wl = torch, api, mk, wl
+        Q, K, V = ig.make_attn_operands(wl)
+        P, H, S, d = wl.P, wl.H, wl.S, wl.d
+        self.Qd = [api.bf16_device(x) for x in Q]
+        self.Kd = [api.bf16_device(x) for x in K]
+        self.Vd = [api.bf16_device(x) for x in V]
+        self.O = [torch.empty((H, S, d), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        self.L = [torch.empty((H, S), dtype=torch.float32, device="cuda") for _ in range(P)]
+        self.R = [torch.empty((P - 1, 2, H, S, d), dtype=torch.bfloat16, device="cuda") for _ in range(P)] if P > 1 else None
+        self.ws = api.ring_attention_workspace(P, H, S, d)
+        # Q, K, V read, the KV forwarded P-1 times (read and written), O and lse written
+        self.nbytes = 3 * P * H * S * d * 2 + 2 * (P - 1) * P * H * S * d * 2 * 2 + P * H * S * (d * 2 + 4)
+
+    def call(self, form, stream, comm_sms=0):
+        mk, wl = self.mk, self.wl
+        mode = {"fused": mk.MK_SPLIT_ADAPTIVE, "static": mk.MK_SPLIT_STATIC, "unfused": mk.MK_SPLIT_UNFUSED,
+                "inplace": mk.MK_SPLIT_ADAPTIVE}[form]
+        o = self.api.make_opts(mode, comm_sms=comm_sms)
+        return mk.mk_ring_attention(wl.P, wl.H, wl.S, wl.d, self.Qd, self.Kd, self.Vd, self.O, self.L,
+                                    None if form == "inplace" else self.R, mk.MK_BF16, 0.0, self.ws, opts=o,
+                                    stream=stream)
+
+    def time(self, form, steps, warmup, stream, comm_sms=0) -> float:
+        torch, mk = self.torch, self.mk
+        for _ in range(warmup):
+            mk.check(self.call(form, stream, comm_sms))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            mk.check(self.call(form, stream, comm_sms))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mk.check(mk.mk_status_check(self.ws, stream))
+        return e0.elapsed_time(e1) / steps
+
+
+RING_WORKLOAD = "ring_p8_h32_s4096_d128"
+
+
+def ring_record(torch, api, mk, stream, peaks, steps, warmup, name=RING_WORKLOAD):
+    """Ring Attention: the fused kernel (communication blocks forward the KV tiles, compute blocks
+    attend), the same attention reading every slice in place (nothing forwarded), and the unfused
+    form (a forwarding kernel, then the attention kernel)."""
+    wl = ig.ATTN_WORKLOADS[name]
+    rp = RingProblem(torch, api, mk, wl)
+    rec = {"op": "ring_attention", "P": wl.P, "H": wl.H, "S_per_rank": wl.S, "d": wl.d, "out_dtype": "bf16",
+           "flops": wl.flops, "algorithmic_bytes": rp.nbytes, "steps": steps}
+    for form in ("fused", "inplace", "unfused"):
+        ms = rp.time(form, steps, warmup, stream)
+        rf = roofline_of(wl.flops, rp.nbytes, ms, peaks)
+        rec["bound"] = rf["bound"]
+        rec["roofline_ms"] = rf["roofline_ms"]
+        rec[form] = {"ms": ms, "tflops": wl.flops / (ms * 1e-3) / 1e12, "roofline_frac": rf["frac"]}
+    rec["fused_over_unfused"] = rec["fused"]["ms"] / rec["unfused"]["ms"]
+    rec["fused_over_inplace"] = rec["fused"]["ms"] / rec["inplace"]["ms"]
+    del rp
+    torch.cuda.empty_cache()
+    return rec
+
+
+def ring_arm(args):
+    """`--op ring`: Ring Attention on P logical ranks of one GPU, fused against its unfused form."""
+    import torch
+    from gemm_tile_level_gb300 import api, mk
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    peaks, peak_src = load_peaks()
+    wl = ig.ATTN_WORKLOADS[args.ring_workload]
+    with torch.cuda.stream(stream):
+        rp = RingProblem(torch, api, mk, wl)
+        clocks = ClockSampler(0)
+        for _ in range(args.warmup):
+            mk.check(rp.call("fused", stream))
+        clocks.start()
+        fused_ms = rp.time("fused", args.steps, 0, stream)
+        clocks.stop()
+        del rp
+        torch.cuda.empty_cache()
+        rec = ring_record(torch, api, mk, stream, peaks, max(3, min(args.steps, 20)), 2, args.ring_workload)
+    value = wl.flops / (fused_ms * 1e-3) / 1e12
+    clk = clocks.summary()
+    line = {"metric": "fused Ring Attention TFLOP/s on 1 GB300", "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": fused_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "op": "ring_attention", "P": wl.P, "H": wl.H, "S_per_rank": wl.S,
+                       "d": wl.d, "out_dtype": "bf16", "causal": False},
+            "roofline": {"bound": "tensor", "achieved": value, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": value / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json, burst)"},
+            "gpu_launches": args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "forms": rec}
+    print(json.dumps(line), flush=True)
+
+
 def allgather_arm(args):
     """`--op allgather`: the fused AllGather + GEMM (communication pairs gather 128-row chunks of
     the row-sharded A into every rank's buffer, compute pairs multiply as chunks arrive) against
@@ -840,8 +944,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-s", type=float, default=8.0)
-    ap.add_argument("--op", choices=["rowparallel", "allgather"], default="rowparallel",
-                    help="allgather: time the fused AllGather + GEMM against its unfused form instead")
+    ap.add_argument("--op", choices=["rowparallel", "allgather", "ring"], default="rowparallel",
+                    help="allgather: time the fused AllGather + GEMM against its unfused form instead; "
+                         "ring: Ring Attention (sequence parallelism)")
+    ap.add_argument("--ring-workload", default=RING_WORKLOAD, help="Ring Attention workload of --op ring")
     ap.add_argument("--ag-shape", default="8,8192,3584,4096", help="P,M,N,K of --op allgather")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-m", type=int, nargs="*")
@@ -870,6 +976,9 @@ def main():
         return
     if args.op == "allgather":
         allgather_arm(args)
+        return
+    if args.op == "ring":
+        ring_arm(args)
         return
     wl = workload_by_name(args.workload)
     if args.shape:

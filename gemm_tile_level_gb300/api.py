@@ -92,3 +92,31 @@ def allgather_gemm(A_shards, B, out_dtype=mk.MK_BF16, gather=True, C=None, gathe
     st = mk.mk_allgather_gemm(P, M, N, K, A_shards, B, gathered if gather else None, C, out_dtype, ws, opts=opts,
                               stream=stream)
     return C, gathered, st
+
+
+def ring_attention_workspace(P: int, H: int, S: int, d: int, device="cuda") -> torch.Tensor:
+    """A zeroed Ring Attention workspace (header and one flag per forwarded KV tile)."""
+    n = mk.mk_ring_attention_workspace_size(P, H, S, d)
+    if n == 0:
+        raise ValueError("invalid shape for mk_ring_attention_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ring_attention(Q, K, V, out_dtype=mk.MK_BF16, scale=0.0, ring=True, lse=True, O=None, kv_ring=None, ws=None,
+                   opts=None, stream=None):
+    """O[r] = softmax(scale Q[r] K_all^T) V_all via mk_ring_attention; Q[r], K[r], V[r] are H x S x d
+    bf16 tensors.  With ring=True the KV slices are forwarded around the ring through P receive
+    buffers (returned).  Returns (O, lse, kv_ring, status)."""
+    P = len(Q)
+    H, S, d = Q[0].shape
+    dev = Q[0].device
+    if O is None:
+        O = [torch.empty((H, S, d), dtype=_TORCH_OUT[out_dtype], device=dev) for _ in range(P)]
+    L = [torch.empty((H, S), dtype=torch.float32, device=dev) for _ in range(P)] if lse else None
+    if ring and kv_ring is None and P > 1:
+        kv_ring = [torch.empty((P - 1, 2, H, S, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    if ws is None:
+        ws = ring_attention_workspace(P, H, S, d, dev)
+    st = mk.mk_ring_attention(P, H, S, d, Q, K, V, O, L, kv_ring if ring else None, out_dtype, scale, ws,
+                              opts=opts, stream=stream)
+    return O, L, kv_ring, st

@@ -11,8 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmk.so")
-SOURCES = ["mk_abi.cu", "mk_kernels.cu", "mk_noalloc.cu"]
-HEADERS = ["mk_internal.h", "mk_ptx.cuh"]
+SOURCES = ["mk_abi.cu", "mk_kernels.cu", "mk_noalloc.cu", "mk_attention.cu"]
+HEADERS = ["mk_internal.h", "mk_ptx.cuh", "mk_device.cuh"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -2,6 +2,7 @@
 // tensor-map encoding and the launches behind the extern "C" entry points of mk.h.
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -86,6 +87,7 @@ int auto_raster_group(bool pair, int P, int64_t Kr, int64_t row_tiles, bool rank
     return static_cast<int>(g);
 }
 constexpr int kCtrlPeriodNs = 1000;
+constexpr int kTileMajorReducePairs = 8;   // adaptive split, tile-major order: reduce-role units at the start
 
 // Column slices per output tile's reduction: by default the smallest power of two (at most 8)
 // that gives every role unit a reduce item (each item restarts the staged pipeline, so finer
@@ -295,12 +297,19 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
         int nr = (o.comm_sms + per_role - 1) / per_role;
         if (nr > role_units - 1) nr = role_units - 1;
         p.static_nr = nr < 1 ? 1 : nr;
-        // the adaptive controller starts from the caller's count, else from one role unit
-        p.init_nr = o.comm_sms > 0 ? p.static_nr : 1;
     }
     // Rank-major bands pay off once there are several bands; a short M has a single band, whose
     // tiles would all complete in the last 1/P of the GEMM, so it keeps the tile-major order.
     p.rank_major = (o.flags & MK_FLAG_TILE_MAJOR) ? 0 : (o.flags & MK_FLAG_RANK_MAJOR) ? 1 : (M >= kRankMajorMinRows);
+    // Where the adaptive controller starts (the caller's count if given).  In rank-major order a
+    // tile's ranks finish a band pass apart, so its partial tiles are read back from HBM whenever
+    // it is reduced, and an SM that reduces during the GEMM only moves bytes the end of the call
+    // would move at the same cost: the measured static sweeps are fastest with no reduce role,
+    // so the controller starts there.  In tile-major order (short M) a tile's partials are
+    // written back to back and reducing them while the GEMM runs hides a reduction that has too
+    // few tiles to fill the grid at the end: the sweeps were fastest with 2 to 42 reduce SMs at
+    // M = 256 and 512, so it starts with kTileMajorReducePairs.
+    p.init_nr = o.comm_sms > 0 ? p.static_nr : p.rank_major ? 0 : (kTileMajorReducePairs < role_units - 1 ? kTileMajorReducePairs : role_units - 1);
     const int64_t order_rows = pair ? g.pair_tiles_m : g.tiles_m;
     p.raster_group = o.raster_group > 0 ? o.raster_group
                                         : auto_raster_group(pair, P, Kr, order_rows, p.rank_major != 0);
@@ -527,6 +536,153 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the fused kernel");
 }
 
+// ------------------------------------------------------------------ Ring Attention
+// bf16 3-D tensor {cols (inner), rows, planes}, row-major planes, box {64, 128, 1}, 128-byte
+// swizzle; rows past the end of a plane read as zero.
+mk_status encode_3d(CUtensorMap *map, const void *ptr, int64_t planes, int64_t rows, int64_t cols) {
+    auto enc = encoder();
+    if (!enc) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(rows * cols) * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (CUresult %d)", static_cast<int>(r));
+    return MK_OK;
+}
+
+int64_t attn_kv_tiles(int64_t S) { return (S + 127) / 128; }
+
+size_t attn_workspace_bytes(int P, int64_t H, int64_t S) {
+    const int64_t nflags = static_cast<int64_t>(P) * (P - 1) * H * attn_kv_tiles(S);
+    return MK_WS_HEADER_BYTES + align_up(static_cast<size_t>(nflags > 0 ? nflags : 1) * sizeof(uint32_t), MK_WS_ALIGN);
+}
+
+// Communication blocks of the fused form: in proportion to the copy's share of the SM time, at
+// per-SM rates taken low on purpose for the copies (about 40 GB/s of bulk copies through shared
+// memory against 8 TFLOP/s of attention per SM), so that the forwarded tiles of a head are ready
+// before the compute blocks reach them.
+int attn_copy_blocks(int grid, int P, int64_t H, int64_t S, int64_t d) {
+    const double copy_bytes = static_cast<double>(P) * (P - 1) * H * S * d * 2.0 * 2.0;
+    const double flops = 4.0 * static_cast<double>(P * S) * static_cast<double>(P * S) * d * H;
+    const double tc = copy_bytes / 40e9, ta = flops / 8e12;
+    int n = static_cast<int>(grid * tc / (tc + ta) + 0.5);
+    if (n < 1) n = 1;
+    if (n > grid - 1) n = grid - 1;
+    return n;
+}
+
+mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void *const *Q, const void *const *K,
+                             const void *const *V, void *const *O, float *const *lse, void *const *kv_ring,
+                             mk_dtype out_dtype, float scale, void *ws, size_t ws_bytes, const mk_opts *opts_in,
+                             void *stream) {
+    g_last_error[0] = '\0';
+    if (P < 1 || P > MK_MAX_P) return fail(MK_ERR_INVALID_ARG, "P=%d outside [1, %d]", P, MK_MAX_P);
+    if (H < 0 || S < 0 || d < 0) return fail(MK_ERR_INVALID_ARG, "negative dimension");
+    if (out_dtype != MK_BF16 && out_dtype != MK_F32) return fail(MK_ERR_INVALID_ARG, "unknown out_dtype");
+    if (!Q || !K || !V || !O || !ws) return fail(MK_ERR_INVALID_ARG, "null pointer array or workspace");
+    if (!(scale >= 0.0f) || scale == INFINITY) return fail(MK_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    mk_opts o;
+    mk_opts_default(&o);
+    if (opts_in) o = *opts_in;
+    mk_status st = check_opts(&o);
+    if (st != MK_OK) return st;
+    if (o.split_mode != MK_SPLIT_ADAPTIVE && o.split_mode != MK_SPLIT_STATIC && o.split_mode != MK_SPLIT_UNFUSED)
+        return fail(MK_ERR_INVALID_ARG, "Ring Attention takes the adaptive, static or unfused split");
+    if (o.flags & (MK_FLAG_BF16_PARTIALS | MK_FLAG_B_NK))
+        return fail(MK_ERR_INVALID_ARG, "MK_FLAG_BF16_PARTIALS and MK_FLAG_B_NK apply to the GEMM operations");
+    if (d != MK_ATTN_D) return fail(MK_ERR_UNSUPPORTED_SHAPE, "head dimension d=%lld (supported: %d)", (long long)d, MK_ATTN_D);
+    if (H > INT32_MAX || S > INT32_MAX || H * S > INT32_MAX)
+        return fail(MK_ERR_UNSUPPORTED_SHAPE, "H * S above 2^31-1");
+    const int64_t nq = (S + 255) / 256;
+    if (H * P * nq > INT32_MAX || H * P * (P - 1) * attn_kv_tiles(S) > INT32_MAX)
+        return fail(MK_ERR_UNSUPPORTED_SHAPE, "too many tiles");
+    if (H == 0 || S == 0) return MK_OK;
+    int n_lse = 0, n_ring = 0;
+    for (int r = 0; r < P; ++r) {
+        if (!Q[r] || !K[r] || !V[r] || !O[r]) return fail(MK_ERR_INVALID_ARG, "Q, K, V or O of rank %d is null", r);
+        if (!aligned16(Q[r]) || !aligned16(K[r]) || !aligned16(V[r]) || !aligned16(O[r]))
+            return fail(MK_ERR_ALIGNMENT, "Q, K, V or O of rank %d not 16-byte aligned", r);
+        if (lse && lse[r]) {
+            ++n_lse;
+            if (reinterpret_cast<uintptr_t>(lse[r]) & 3u) return fail(MK_ERR_ALIGNMENT, "lse[%d] not 4-byte aligned", r);
+        }
+        if (kv_ring && kv_ring[r]) {
+            ++n_ring;
+            if (!aligned16(kv_ring[r])) return fail(MK_ERR_ALIGNMENT, "kv_ring[%d] not 16-byte aligned", r);
+        }
+    }
+    if (n_lse != 0 && n_lse != P) return fail(MK_ERR_INVALID_ARG, "lse must hold P buffers or none");
+    if (n_ring != 0 && n_ring != P) return fail(MK_ERR_INVALID_ARG, "kv_ring must hold P buffers or none");
+    if (reinterpret_cast<uintptr_t>(ws) % MK_WS_ALIGN) return fail(MK_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+    const size_t need = attn_workspace_bytes(P, H, S);
+    if (ws_bytes < need) return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, need);
+    const bool ring = n_ring == P && P > 1;
+
+    int resident = 0;
+    cudaError_t e = mk_attn_max_ctas(&resident);
+    if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
+    if (resident < 2)
+        return fail(MK_ERR_NOT_RESIDENT, "the attention kernel (%zu bytes of shared memory, %d threads) fits %d blocks "
+                    "on this device", mk_attn_smem_bytes(), MK_ATTN_THREADS, resident);
+    const int grid = o.num_ctas > 0 ? o.num_ctas : resident;
+    if (grid > resident)
+        return fail(MK_ERR_NOT_RESIDENT, "persistent grid of %d blocks cannot be co-resident (%d fit)", grid, resident);
+    if (grid < 2) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d too small", grid);
+    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > grid - 1)
+        return fail(MK_ERR_INVALID_ARG, "comm_sms=%d leaves no compute SMs in a grid of %d", o.comm_sms, grid);
+
+    MkAttnParams p;
+    memset(&p, 0, sizeof p);
+    for (int r = 0; r < P; ++r) {
+        if ((st = encode_3d(&p.tmQ[r], Q[r], H, S, d)) != MK_OK) return st;
+        if ((st = encode_3d(&p.tmK[r], K[r], H, S, d)) != MK_OK) return st;
+        if ((st = encode_3d(&p.tmV[r], V[r], H, S, d)) != MK_OK) return st;
+        if (ring && (st = encode_3d(&p.tmR[r], kv_ring[r], static_cast<int64_t>(P - 1) * 2 * H, S, d)) != MK_OK) return st;
+        p.k[r] = K[r];
+        p.v[r] = V[r];
+        p.ring[r] = ring ? kv_ring[r] : nullptr;
+        p.out[r] = O[r];
+        p.lse[r] = n_lse ? lse[r] : nullptr;
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    p.hdr = reinterpret_cast<MkWsHeader *>(wsb);
+    p.flags = reinterpret_cast<uint32_t *>(wsb + MK_WS_HEADER_BYTES);
+    p.timeout_ns = o.wait_timeout_ns ? o.wait_timeout_ns : kDefaultTimeoutNs;
+    const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / sqrt(static_cast<double>(d));
+    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
+    p.P = P;
+    p.H = static_cast<int32_t>(H);
+    p.S = static_cast<int32_t>(S);
+    p.nt = static_cast<int32_t>(attn_kv_tiles(S));
+    p.nq = static_cast<int32_t>(nq);
+    p.num_units = static_cast<int32_t>(H * P * nq);
+    p.num_copies = ring ? static_cast<int32_t>(H * P * (P - 1) * attn_kv_tiles(S)) : 0;
+    p.use_ring = ring ? 1 : 0;
+    p.out_bf16 = out_dtype == MK_BF16;
+    p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!ring) {
+        p.mode = MK_ATTN_COMPUTE_ONLY;
+        e = mk_launch_attention(p, grid, s);
+        return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the attention kernel");
+    }
+    if (o.split_mode == MK_SPLIT_UNFUSED) {
+        p.mode = MK_ATTN_COPY_ONLY;   // the KV forwarding of every step first, then the attention
+        e = mk_launch_attention(p, grid, s);
+        if (e != cudaSuccess) return fail_cuda(e, "launch of the KV forwarding kernel");
+        p.mode = MK_ATTN_COMPUTE_ONLY;
+        e = mk_launch_attention(p, grid, s);
+        return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the attention kernel");
+    }
+    p.mode = MK_ATTN_FUSED;
+    p.copy_ctas = o.comm_sms > 0 ? o.comm_sms : attn_copy_blocks(grid, P, H, S, d);
+    e = mk_launch_attention(p, grid, s);
+    return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the fused Ring Attention kernel");
+}
+
 }  // namespace
 
 void mk_internal_set_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
@@ -587,6 +743,18 @@ mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *
                             const void *const *B, void *const *A_gathered, void *const *C, mk_dtype out_dtype,
                             void *ws, size_t ws_bytes, const mk_opts *opts, void *cuda_stream) {
     return run_allgather(P, M, N, K, A_shard, B, A_gathered, C, out_dtype, ws, ws_bytes, opts, cuda_stream);
+}
+
+size_t mk_ring_attention_workspace_size(int P, int64_t H, int64_t S, int64_t d) {
+    if (P < 1 || P > MK_MAX_P || H < 0 || S < 0 || d < 0) return 0;
+    return attn_workspace_bytes(P, H, S);
+}
+
+mk_status mk_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void *const *Q, const void *const *K,
+                            const void *const *V, void *const *O, float *const *lse, void *const *kv_ring,
+                            mk_dtype out_dtype, float scale, void *ws, size_t ws_bytes, const mk_opts *opts,
+                            void *cuda_stream) {
+    return run_ring_attention(P, H, S, d, Q, K, V, O, lse, kv_ring, out_dtype, scale, ws, ws_bytes, opts, cuda_stream);
 }
 
 mk_status mk_status_check(void *ws, void *cuda_stream) {

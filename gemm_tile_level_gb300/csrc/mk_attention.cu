@@ -1,0 +1,632 @@
+// mk_attention.cu -- Ring Attention (sequence parallelism) for sm_103a: one persistent kernel
+// whose blocks either forward KV tiles around the ring (communication role) or run the
+// attention of 256 query rows against the whole sequence's KV, slice by slice in ring order
+// (compute role).
+//
+// Method (mKernel: Fast Multi-GPU, Multi-Node Fused Kernels; Table 3, row "Ring Attention (SP)";
+// abstract, Figure 2): the sequence is cut into P slices, one per rank.  At ring step s rank r
+// attends with its own queries to the KV slice of rank (r - s) mod P while that slice moves on to
+// rank r + 1; the computations of one step are independent of each other, and KV moves in
+// 128-row tiles.  Here the P ranks are P partitions of one GPU's memory.  Communication blocks
+// forward each 128-row KV tile from rank r-1's buffer into rank r's ring buffer (bulk copies
+// through shared memory) and release a readiness flag per tile; compute blocks acquire the flag
+// of each tile before loading it.  Without ring buffers the compute blocks read every slice in
+// place.
+//
+// Compute block (320 threads, one per SM, persistent): a unit is (head h, rank r, 256 query
+// rows), computed as two 128-row query tiles A and B over the P * nt KV tiles of the sequence in
+// ring order (step 0 = the rank's own slice).  Per KV tile j:
+//   warp 0    TMA: K_j and V_j (two 64-column boxes each, 128-byte swizzle) into a ring of three
+//             32 KiB slots, in the order K_0, K_1, V_0, K_2, V_1, ... (keys run one tile ahead)
+//   warp 1    tcgen05.mma (M = 128, N = 128, K = 16 steps):
+//               S_A(j+1) = Q_A K_{j+1}^T, O_A += P_A(j) V_j, S_B(j+1) = Q_B K_{j+1}^T, O_B += P_B(j) V_j
+//             S_A, S_B, O_A, O_B are 128 columns of TMEM each (all 512)
+//   warps 2-5 softmax of tile A, warps 6-9 of tile B (one query row per thread = one TMEM lane):
+//             load S, running maximum m in the log2 domain, P = 2^(S*scale*log2e - m) to shared
+//             memory as bf16 (the layout a K-major operand tile has), row sum l in fp32; when the
+//             maximum grows by more than 8 (a factor 256), rescale O in TMEM and l first
+//             (otherwise the stale maximum is kept, so P stays below 256)
+// and at the end of the unit O / l and lse = (m + log2 l) ln 2 go to memory.
+//
+// Every wait is bounded (see mk_device.cuh); a wait that runs out raises MK_ERR_TIMEOUT and
+// the grid-wide abort, after which every block drains what it has in flight and exits.
+#include "mk.h"
+#include "mk_device.cuh"
+#include "mk_internal.h"
+#include "mk_ptx.cuh"
+
+namespace mk {
+namespace attn {
+
+constexpr int BQ = 128;                          // query rows per tile
+constexpr int BKV = 128;                         // KV rows per tile
+constexpr int D = MK_ATTN_D;
+constexpr uint32_t BOX_BYTES = 128 * 64 * 2;     // one 64-column box of 128 rows
+constexpr uint32_t TILE_BYTES = 2 * BOX_BYTES;   // one Q, K, V or P tile (128 x 128 bf16)
+constexpr int NSLOT = 3;                         // KV ring slots
+constexpr int COPY_WARPS = 8;                    // warps 2-9 of a communication block
+constexpr uint32_t COPY_PIECE = 8192;            // bytes per bulk copy piece
+constexpr int COPY_BUFS = 3;                     // staging buffers per copy warp
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV) & ~(1u << 16);   // B = K tile, K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D);                   // B = V tile, MN-major
+
+// Shared memory (1024-byte aligned): Q_A, Q_B, three KV slots, P_A, P_B (7 x 32 KiB), then control.
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = 2 * TILE_BYTES;
+constexpr uint32_t OFF_P = OFF_KV + NSLOT * TILE_BYTES;
+constexpr uint32_t DATA_BYTES = OFF_P + 2 * TILE_BYTES;
+static_assert(COPY_WARPS * COPY_BUFS * COPY_PIECE <= DATA_BYTES, "copy staging fits");
+
+struct Ctl {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+    uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
+    uint64_t drain;
+    uint64_t cbar[COPY_WARPS][COPY_BUFS];
+    uint32_t tmem_base;
+    uint32_t epoch;
+    int abort;
+    uint32_t kv_issued;     // KV loads the producer issued
+    uint32_t q_issued;      // Q loads the producer issued
+};
+
+struct Unit {
+    int h, r, qp;
+};
+
+__device__ __forceinline__ Unit unit_of(const MkAttnParams &p, int u) {
+    Unit x;
+    x.qp = u % p.nq;
+    const int hr = u / p.nq;
+    x.r = hr % p.P;
+    x.h = hr / p.P;
+    return x;
+}
+
+// Readiness flag of KV tile t of head h that rank r received at ring step s (1 <= s < P).
+__device__ __forceinline__ uint32_t *kv_flag(const MkAttnParams &p, int r, int s, int h, int t) {
+    return p.flags + ((static_cast<size_t>(r) * (p.P - 1) + (s - 1)) * p.H + h) * p.nt + t;
+}
+
+// Wait (bounded) until `f` holds `epoch`, with acquire semantics; false on abort or timeout.
+__device__ bool wait_flag(const Ctx &c, const uint32_t *f, uint32_t epoch, uint32_t index) {
+    uint64_t t0 = 0;
+    for (uint32_t polls = 0; ld_acquire_gpu(f) != epoch; ++polls) {
+        if (t0 == 0) t0 = globaltimer();
+        if ((polls & 15u) == 15u) {
+            if (global_abort(c)) return false;
+            if (globaltimer() - t0 > c.timeout_ns || polls > (1u << 30)) {
+                raise_error(c, MK_ERR_TIMEOUT, SITE_FLAG, index);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ communication role
+// One copy warp forwards KV tile t of head h from rank r-1 to rank r at ring step s: the K and the
+// V rows of the tile (contiguous in both buffers) move through three 8 KiB staging buffers with
+// bulk copies, then the tile's flag is released.  At step 1 the source is rank r-1's own K_{r-1},
+// V_{r-1}; later it is what rank r-1 received one step earlier, so the copy first acquires that
+// tile's flag.  Dependencies point to copies with a smaller index only, and every copy warp
+// finishes a copy before it starts the next, so the copies always make progress.
+__device__ void copy_tile(const MkAttnParams &p, const Ctx &c, int item, uint8_t *stage, uint64_t *bars,
+                          uint32_t &seq, uint32_t epoch) {
+    const int per_step = p.P * p.nt;
+    const int per_head = (p.P - 1) * per_step;
+    const int h = item / per_head;
+    const int rem = item - h * per_head;
+    const int s = rem / per_step + 1;
+    const int rem2 = rem - (s - 1) * per_step;
+    const int r = rem2 / p.nt;
+    const int t = rem2 - r * p.nt;
+    const int src_rank = (r + p.P - 1) % p.P;
+    const int rows = min(BKV, p.S - t * BKV);
+    const uint32_t bytes = static_cast<uint32_t>(rows) * D * 2;
+    const size_t row0 = static_cast<size_t>(t) * BKV;
+    const char *src[2];
+    char *dst[2];
+    for (int kv = 0; kv < 2; ++kv) {
+        if (s == 1)
+            src[kv] = static_cast<const char *>(kv ? p.v[src_rank] : p.k[src_rank]) +
+                      (static_cast<size_t>(h) * p.S + row0) * D * 2;
+        else
+            src[kv] = static_cast<const char *>(p.ring[src_rank]) +
+                      (((static_cast<size_t>(s - 2) * 2 + kv) * p.H + h) * p.S + row0) * D * 2;
+        dst[kv] = static_cast<char *>(p.ring[r]) + (((static_cast<size_t>(s - 1) * 2 + kv) * p.H + h) * p.S + row0) * D * 2;
+    }
+    if (s >= 2) {
+        if (!wait_flag(c, kv_flag(p, src_rank, s - 1, h, t), epoch, static_cast<uint32_t>(item))) return;
+        fence_proxy_async_global();   // the acquire above before the bulk reads of the source
+    }
+    const uint32_t npk = (bytes + COPY_PIECE - 1) / COPY_PIECE;   // pieces per K (or V) part
+    const uint32_t npieces = 2 * npk;
+    auto piece = [&](uint32_t k, const char *&from, char *&to, uint32_t &n) {
+        const int kv = k >= npk;
+        const uint32_t off = (k - kv * npk) * COPY_PIECE;
+        from = src[kv] + off;
+        to = dst[kv] + off;
+        n = bytes - off < COPY_PIECE ? bytes - off : COPY_PIECE;
+    };
+    auto load = [&](uint32_t k) {
+        const char *from;
+        char *to;
+        uint32_t n;
+        piece(k, from, to, n);
+        const uint32_t b = (seq + k) % COPY_BUFS;
+        mbar_arrive_expect_tx(smem_u32(&bars[b]), n);
+        bulk_load(smem_u32(stage + b * COPY_PIECE), from, n, smem_u32(&bars[b]));
+    };
+    for (uint32_t k = 0; k < COPY_BUFS - 1 && k < npieces; ++k) load(k);
+    for (uint32_t k = 0; k < npieces; ++k) {
+        const uint32_t q = seq + k;
+        const uint32_t b = q % COPY_BUFS;
+        if (!wait_bar<false>(smem_u32(&bars[b]), (q / COPY_BUFS) & 1u, c, SITE_STAGE_FULL, k)) break;
+        const char *from;
+        char *to;
+        uint32_t n;
+        piece(k, from, to, n);
+        bulk_store(to, smem_u32(stage + b * COPY_PIECE), n);
+        bulk_commit();
+        if (k + COPY_BUFS - 1 < npieces) {
+            bulk_wait_read<COPY_BUFS - 2>();   // the store that last used buffer (k + BUFS - 1) % BUFS has read it
+            load(k + COPY_BUFS - 1);
+        }
+    }
+    seq += npieces;
+    bulk_wait_all();
+    fence_proxy_async_global();        // the bulk writes before the release below
+    st_release_gpu(kv_flag(p, r, s, h, t), epoch);
+}
+
+__device__ void run_copies(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, int copy_block, int nblocks,
+                           int warp, uint32_t epoch) {
+    const int cw = warp - 2;
+    uint8_t *stage = smem + static_cast<uint32_t>(cw) * COPY_BUFS * COPY_PIECE;   // a copy block holds no tiles
+    uint64_t *bars = s.cbar[cw];
+    uint32_t seq = 0;
+    const int workers = nblocks * COPY_WARPS;
+    for (int item = copy_block * COPY_WARPS + cw; item < p.num_copies; item += workers) {
+        if (global_abort(c)) break;
+        copy_tile(p, c, item, stage, bars, seq, epoch);
+    }
+    bulk_wait_all();
+}
+
+// ------------------------------------------------------------------ compute role
+// Operand descriptors: a 128-row tile is two 64-column boxes of 16 KiB (128-byte rows, 128-byte
+// swizzle).  K-major operands (Q, P as A; K as B) advance 32 bytes per 16-column K step inside a
+// box; the V tile (B, MN-major: K = KV rows, N = d columns) advances 16 rows = 2 KiB per K step,
+// with its two 64-column boxes 16 KiB apart.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    return sw128_desc(tile + static_cast<uint32_t>(kk >> 2) * BOX_BYTES + static_cast<uint32_t>(kk & 3) * 32u, 16, 1024);
+}
+
+__device__ __forceinline__ void mma_s(uint32_t d_tmem, uint32_t q_tile, uint32_t k_tile) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+        umma_bf16(d_tmem, kmajor_desc(q_tile, kk), kmajor_desc(k_tile, kk), IDESC_S, static_cast<uint32_t>(kk != 0));
+}
+
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tile, uint32_t v_tile, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < BKV / 16; ++kk)
+        umma_bf16(d_tmem, kmajor_desc(p_tile, kk), sw128_desc(v_tile + static_cast<uint32_t>(kk) * 2048u, BOX_BYTES, 1024),
+                  IDESC_PV, static_cast<uint32_t>(accumulate || kk != 0));
+}
+
+// Producer (warp 0, one thread): Q of each unit, then the KV tiles in the order K_0, K_1, V_0,
+// K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}, which is the order the MMA thread consumes them.
+__device__ void run_producer(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, int cblock, int ncompute,
+                             uint32_t epoch) {
+    const uint32_t base = smem_u32(smem);
+    const int n = p.P * p.nt;
+    const uint64_t pol_q = policy_evict_first();
+    const uint64_t pol_kv = policy_evict_last();   // every query unit of the head reads them
+    uint32_t q = 0, k = 0;
+    bool stop = false;
+    for (int u = cblock; u < p.num_units && !stop; u += ncompute, ++k) {
+        if (global_abort(c)) break;
+        const Unit x = unit_of(p, u);
+        if (k > 0 && !wait_bar<false>(smem_u32(&s.q_empty), (k - 1) & 1u, c, SITE_STAGE_EMPTY, u)) break;
+        mbar_arrive_expect_tx(smem_u32(&s.q_full), 4 * BOX_BYTES);
+        for (int half = 0; half < 2; ++half)
+            for (int box = 0; box < 2; ++box)
+                tma_load_3d_hint(base + OFF_Q + half * TILE_BYTES + box * BOX_BYTES, &p.tmQ[x.r], smem_u32(&s.q_full),
+                                 box * 64, x.qp * 2 * BQ + half * BQ, x.h, pol_q);
+        ++s.q_issued;
+        // the load sequence: (tile, kind) with kind 0 = K, 1 = V
+        for (int e = 0; e < 2 * n && !stop; ++e) {
+            int j, kind;
+            if (e == 0) { j = 0; kind = 0; }
+            else if (e == 2 * n - 1) { j = n - 1; kind = 1; }
+            else if (e & 1) { j = (e + 1) / 2; kind = 0; }   // K_{j}, j = 1..n-1
+            else { j = e / 2 - 1; kind = 1; }                 // V_{j}, j = 0..n-2
+            const int st = j / p.nt, t = j - st * p.nt;
+            const int o = (x.r - st + p.P) % p.P;
+            const CUtensorMap *map;
+            int z;
+            if (st == 0 || !p.use_ring) {
+                map = kind ? &p.tmV[o] : &p.tmK[o];
+                z = x.h;
+            } else {
+                map = &p.tmR[x.r];
+                z = ((st - 1) * 2 + kind) * p.H + x.h;
+                if (kind == 0 && p.mode == MK_ATTN_FUSED) {
+                    if (!wait_flag(c, kv_flag(p, x.r, st, x.h, t), epoch, static_cast<uint32_t>(u))) { stop = true; break; }
+                    fence_proxy_async_global();   // the acquire before the TMA reads of the tile
+                }
+            }
+            const uint32_t slot = q % NSLOT;
+            if (q >= NSLOT && !wait_bar<false>(smem_u32(&s.kv_empty[slot]), ((q / NSLOT) - 1) & 1u, c, SITE_STAGE_EMPTY, u)) {
+                stop = true;
+                break;
+            }
+            const uint32_t dst = base + OFF_KV + slot * TILE_BYTES;
+            mbar_arrive_expect_tx(smem_u32(&s.kv_full[slot]), TILE_BYTES);
+            tma_load_3d_hint(dst, map, smem_u32(&s.kv_full[slot]), 0, t * BKV, z, pol_kv);
+            tma_load_3d_hint(dst + BOX_BYTES, map, smem_u32(&s.kv_full[slot]), 64, t * BKV, z, pol_kv);
+            ++q;
+            s.kv_issued = q;
+        }
+    }
+    // every TMA load this thread issued must have landed before the block exits
+    const uint32_t nq = s.kv_issued;
+    for (uint32_t i = nq > NSLOT ? nq - NSLOT : 0; i < nq; ++i)
+        wait_bar<false>(smem_u32(&s.kv_full[i % NSLOT]), (i / NSLOT) & 1u, c, SITE_DRAIN, i);
+    if (s.q_issued) wait_bar<false>(smem_u32(&s.q_full), (s.q_issued - 1) & 1u, c, SITE_DRAIN, 0);
+}
+
+// MMA issue (warp 1, one thread).  Per KV tile j the order is S_A(j+1), O_A += P_A(j) V_j,
+// S_B(j+1), O_B += P_B(j) V_j, so that each softmax group has the other group's MMAs to hide
+// behind.  Completion counters (all continue across units) give each barrier's phase parity.
+__device__ void run_mma(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, uint32_t tmem, int cblock,
+                        int ncompute) {
+    const uint32_t base = smem_u32(smem);
+    const int n = p.P * p.nt;
+    uint32_t q = 0;                  // KV sequence position
+    uint32_t ns[2] = {0, 0};         // S MMAs issued per group
+    uint32_t npv[2] = {0, 0};        // PV MMAs issued per group
+    uint32_t k = 0;
+    bool ok = true;
+    auto take = [&](uint32_t &slot) -> bool {   // the next KV tile of the sequence
+        slot = q % NSLOT;
+        const bool r = wait_bar<false>(smem_u32(&s.kv_full[slot]), (q / NSLOT) & 1u, c, SITE_STAGE_FULL, q);
+        ++q;
+        tc_fence_after();
+        return r;
+    };
+    auto issue_s = [&](int g, uint32_t k_tile) -> bool {
+        if (ns[g] > 0 && !wait_bar<false>(smem_u32(&s.s_free[g]), (ns[g] - 1) & 1u, c, SITE_ACC_EMPTY, ns[g])) return false;
+        tc_fence_after();
+        mma_s(tmem + static_cast<uint32_t>(g) * 128u, base + OFF_Q + static_cast<uint32_t>(g) * TILE_BYTES, k_tile);
+        umma_commit(smem_u32(&s.s_full[g]));
+        ++ns[g];
+        return true;
+    };
+    auto issue_pv = [&](int g, uint32_t v_tile, bool first) -> bool {
+        if (!wait_bar<false>(smem_u32(&s.p_full[g]), npv[g] & 1u, c, SITE_ACC_FULL, npv[g])) return false;
+        if (first && k > 0 && !wait_bar<false>(smem_u32(&s.o_free[g]), (k - 1) & 1u, c, SITE_ACC_EMPTY, k)) return false;
+        tc_fence_after();
+        mma_pv(tmem + 256u + static_cast<uint32_t>(g) * 128u, base + OFF_P + static_cast<uint32_t>(g) * TILE_BYTES, v_tile,
+               !first);
+        umma_commit(smem_u32(&s.o_done[g]));
+        ++npv[g];
+        return true;
+    };
+    for (int u = cblock; u < p.num_units && ok; u += ncompute, ++k) {
+        if (!wait_bar<false>(smem_u32(&s.q_full), k & 1u, c, SITE_STAGE_FULL, u)) break;
+        tc_fence_after();
+        uint32_t ks, vs;
+        if (!(ok = take(ks))) break;
+        if (!(ok = issue_s(0, base + OFF_KV + ks * TILE_BYTES))) break;
+        if (!(ok = issue_s(1, base + OFF_KV + ks * TILE_BYTES))) break;
+        umma_commit(smem_u32(&s.kv_empty[ks]));
+        if (n == 1) umma_commit(smem_u32(&s.q_empty));
+        for (int j = 0; j < n && ok; ++j) {
+            const bool more = j + 1 < n;
+            if (more) {
+                if (!(ok = take(ks))) break;
+                if (!(ok = issue_s(0, base + OFF_KV + ks * TILE_BYTES))) break;
+            }
+            if (!(ok = take(vs))) break;
+            if (!(ok = issue_pv(0, base + OFF_KV + vs * TILE_BYTES, j == 0))) break;
+            if (more) {
+                if (!(ok = issue_s(1, base + OFF_KV + ks * TILE_BYTES))) break;
+                umma_commit(smem_u32(&s.kv_empty[ks]));
+                if (j + 2 == n) umma_commit(smem_u32(&s.q_empty));   // the unit's last S MMAs are issued
+            }
+            if (!(ok = issue_pv(1, base + OFF_KV + vs * TILE_BYTES, j == 0))) break;
+            umma_commit(smem_u32(&s.kv_empty[vs]));
+        }
+    }
+    // every MMA issued must complete before TMEM is released
+    umma_commit(smem_u32(&s.drain));
+    wait_bar<false>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
+}
+
+// One pass over a row's 128 scores in TMEM (four 32-column loads): the probabilities
+// 2^(s * cl - m) as packed bf16 pairs (column pairs 2i, 2i+1 in pk[i]), their fp32 sum and the
+// row's largest valid score.  Columns at or past `valid` (the end of the sequence slice) count as
+// probability 0.
+__device__ __forceinline__ void softmax_pass(uint32_t t_s, int valid, float cl, float m, uint32_t (&pk)[64],
+                                             float &rowsum, float &mx) {
+    rowsum = 0.0f;
+    mx = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        uint32_t v[16];
+        tmem_ld16(t_s + static_cast<uint32_t>(cc * 16), v);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const int col = cc * 16 + i;
+            const float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
+            const bool ok0 = col < valid, ok1 = col + 1 < valid;
+            const float p0 = ok0 ? ex2_approx(fmaf(x0, cl, -m)) : 0.0f;
+            const float p1 = ok1 ? ex2_approx(fmaf(x1, cl, -m)) : 0.0f;
+            if (ok0) mx = fmaxf(mx, x0);
+            if (ok1) mx = fmaxf(mx, x1);
+            rowsum += p0 + p1;
+            pk[col >> 1] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+
+// Softmax group g (warps 2-5: g = 0, query tile A; warps 6-9: g = 1, tile B).  The running
+// maximum m is only raised when a tile's maximum exceeds it by more than 8 (in the log2 domain);
+// otherwise the probabilities are formed against the stale maximum (at most 2^8), which needs no
+// first pass for the tile maximum.  A unit's first tile takes one (m = -inf), and a row whose
+// tile maximum does exceed m + 8 forms the tile again against its new maximum, after O and l are
+// scaled down by 2^(m_old - m_new).
+__device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, uint32_t tmem, int cblock,
+                            int ncompute, int g, int warp, int lane) {
+    const int quarter = warp & 3;                 // the TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
+    const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lanes + static_cast<uint32_t>(g) * 128u;
+    const uint32_t t_o = tmem + lanes + 256u + static_cast<uint32_t>(g) * 128u;
+    const uint32_t p_tile = smem_u32(smem + OFF_P + static_cast<uint32_t>(g) * TILE_BYTES);
+    const int n = p.P * p.nt;
+    const float cl = p.scale_log2;
+    uint32_t gt = 0;       // KV tiles processed by this group (all units)
+    for (int u = cblock; u < p.num_units; u += ncompute) {
+        const Unit x = unit_of(p, u);
+        float m = -INFINITY, l = 0.0f;
+        for (int j = 0; j < n; ++j, ++gt) {
+            if (!wait_bar<false>(smem_u32(&s.s_full[g]), gt & 1u, c, SITE_ACC_FULL, gt)) return;
+            tc_fence_after();
+            const int t = j % p.nt;
+            const int valid = min(BKV, p.S - t * BKV);
+            float alpha = 1.0f;
+            if (j == 0) {
+                // the unit's first tile: its maximum first
+                float mx = -INFINITY;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(t_s + static_cast<uint32_t>(cc * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (cc * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+                }
+                m = mx * cl;
+                alpha = 0.0f;
+            }
+            uint32_t pk[64];
+            float rowsum;
+#pragma unroll 1
+            for (int attempt = 0;; ++attempt) {
+                float mx;
+                softmax_pass(t_s, valid, cl, m, pk, rowsum, mx);
+                const float mt = mx * cl;
+                const bool grow = attempt == 0 && mt > m + 8.0f;
+                if (!__any_sync(0xFFFFFFFFu, grow)) break;
+                // rows whose maximum grew past m + 8 form the tile again against it; the other rows
+                // of the warp recompute the same values
+                if (grow) {
+                    alpha = ex2_approx(m - mt);
+                    m = mt;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.s_free[g]));
+            if (j > 0) {
+                // the previous P V has finished reading P and writing O
+                if (!wait_bar<false>(smem_u32(&s.o_done[g]), (gt - 1) & 1u, c, SITE_ACC_FULL, gt)) return;
+                tc_fence_after();
+                if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t ov[16];
+                        tmem_ld16(t_o + static_cast<uint32_t>(cc * 16), ov);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st16(t_o + static_cast<uint32_t>(cc * 16), ov);
+                    }
+                }
+            }
+            l = l * alpha + rowsum;
+            // P into the K-major swizzled layout: 16-byte chunk (row, g8) of box g8 / 8 sits at
+            // row * 128 + ((g8 % 8) ^ (row % 8)) * 16
+#pragma unroll
+            for (int g8 = 0; g8 < 16; ++g8) {
+                const uint32_t addr = p_tile + static_cast<uint32_t>(g8 >> 3) * BOX_BYTES + static_cast<uint32_t>(row) * 128u +
+                                      (static_cast<uint32_t>((g8 & 7) ^ (row & 7)) << 4);
+                st_shared_u4(addr, pk[4 * g8], pk[4 * g8 + 1], pk[4 * g8 + 2], pk[4 * g8 + 3]);
+            }
+            fence_proxy_async_smem();   // the generic-proxy stores of P before the tensor core reads them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.p_full[g]));
+        }
+        // epilogue: O / l and the logsumexp of the unit's query rows
+        if (!wait_bar<false>(smem_u32(&s.o_done[g]), (gt - 1) & 1u, c, SITE_ACC_FULL, gt)) return;
+        tc_fence_after();
+        const int qrow = x.qp * 2 * BQ + g * BQ + row;
+        const bool store = qrow < p.S;
+        const size_t obase = (static_cast<size_t>(x.h) * p.S + (store ? qrow : 0)) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+            uint32_t ov[16];
+            tmem_ld16(t_o + static_cast<uint32_t>(cc * 16), ov);
+            if (!store) continue;
+            float o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __fdiv_rn(__uint_as_float(ov[i]), l);
+            if (p.out_bf16) {
+                uint16_t *dst = static_cast<uint16_t *>(p.out[x.r]) + obase + cc * 16;
+#pragma unroll
+                for (int v = 0; v < 2; ++v)
+                    st_u4(dst + 8 * v, pack_bf16x2(o[8 * v], o[8 * v + 1]), pack_bf16x2(o[8 * v + 2], o[8 * v + 3]),
+                          pack_bf16x2(o[8 * v + 4], o[8 * v + 5]), pack_bf16x2(o[8 * v + 6], o[8 * v + 7]));
+            } else {
+                float *dst = static_cast<float *>(p.out[x.r]) + obase + cc * 16;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) st_f4(dst + 4 * v, o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            }
+        }
+        if (store && p.lse[x.r]) p.lse[x.r][static_cast<size_t>(x.h) * p.S + qrow] = (m + log2f(l)) * 0.69314718055994531f;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.o_free[g]));
+    }
+}
+
+// Last block out records the epoch the call used and resets the per-call state.
+__device__ void finish_call(const MkAttnParams &p, uint32_t epoch) {
+    MkWsHeader *h = p.hdr;
+    __threadfence();
+    const uint32_t prev = atomicAdd(&h->done_ctas, 1u);
+    if (prev == gridDim.x - 1) {
+        __threadfence();
+        h->acc_state = MK_ACC_DIRTY;   // the flags are not accumulator tiles of a GEMM call
+        h->abort = 0;
+        h->epoch = epoch;
+        h->done_ctas = 0;
+        __threadfence();
+    }
+}
+
+__global__ void __launch_bounds__(MK_ATTN_THREADS, 1) mk_attn_kernel(const __grid_constant__ MkAttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Ctl &s = *reinterpret_cast<Ctl *>(smem + DATA_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ncompute = p.mode == MK_ATTN_COPY_ONLY ? 0
+                         : p.mode == MK_ATTN_COMPUTE_ONLY ? static_cast<int>(gridDim.x)
+                                                          : static_cast<int>(gridDim.x) - p.copy_ctas;
+    const bool compute = static_cast<int>(blockIdx.x) < ncompute;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&s.q_full), 1);
+        mbar_init(smem_u32(&s.q_empty), 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(smem_u32(&s.kv_full[i]), 1);
+            mbar_init(smem_u32(&s.kv_empty[i]), 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(smem_u32(&s.s_full[g]), 1);
+            mbar_init(smem_u32(&s.s_free[g]), 4);
+            mbar_init(smem_u32(&s.p_full[g]), 4);
+            mbar_init(smem_u32(&s.o_done[g]), 1);
+            mbar_init(smem_u32(&s.o_free[g]), 4);
+        }
+        mbar_init(smem_u32(&s.drain), 1);
+        for (int w = 0; w < COPY_WARPS; ++w)
+            for (int b = 0; b < COPY_BUFS; ++b) mbar_init(smem_u32(&s.cbar[w][b]), 1);
+        fence_mbar_init();
+        s.abort = 0;
+        s.kv_issued = 0;
+        s.q_issued = 0;
+        uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
+        if (e == 0u) e = 1u;
+        s.epoch = e;
+    }
+    if (compute && warp == 0 && lane == 0)
+        for (int r = 0; r < p.P; ++r) {
+            prefetch_tmap(&p.tmQ[r]);
+            prefetch_tmap(&p.tmK[r]);
+            prefetch_tmap(&p.tmV[r]);
+            if (p.use_ring) prefetch_tmap(&p.tmR[r]);
+        }
+    if (compute && warp == 1) {
+        tmem_alloc(smem_u32(&s.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t epoch = s.epoch;
+    const Ctx c{p.hdr, &s.abort, p.timeout_ns, 4 * p.timeout_ns};
+
+    if (compute) {
+        const uint32_t tmem = s.tmem_base;
+        if (warp == 0) {
+            if (lane == 0) run_producer(p, c, s, smem, blockIdx.x, ncompute, epoch);
+        } else if (warp == 1) {
+            if (lane == 0) run_mma(p, c, s, smem, tmem, blockIdx.x, ncompute);
+        } else {
+            run_softmax(p, c, s, smem, tmem, blockIdx.x, ncompute, warp < 6 ? 0 : 1, warp, lane);
+        }
+    } else if (warp >= 2 && lane == 0) {
+        const int nblocks = static_cast<int>(gridDim.x) - ncompute;
+        run_copies(p, c, s, smem, static_cast<int>(blockIdx.x) - ncompute, nblocks, warp, epoch);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (compute && warp == 1) tmem_dealloc(s.tmem_base, 512);
+    if (threadIdx.x == 0) finish_call(p, epoch);
+}
+
+}  // namespace attn
+}  // namespace mk
+
+size_t mk_attn_smem_bytes() { return mk::attn::DATA_BYTES + sizeof(mk::attn::Ctl) + 1024; }
+
+cudaError_t mk_attn_max_ctas(int *ctas) {
+    static int cached[64] = {};   // co-resident blocks + 1 per device; 0 = not yet known
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) {
+        *ctas = cached[dev] - 1;
+        return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(mk::attn::mk_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(mk_attn_smem_bytes()));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mk::attn::mk_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mk::attn::mk_attn_kernel, MK_ATTN_THREADS,
+                                                      mk_attn_smem_bytes());
+    if (e != cudaSuccess) return e;
+    *ctas = per_sm * sms;
+    if (dev >= 0 && dev < 64) cached[dev] = *ctas + 1;
+    return cudaSuccess;
+}
+
+cudaError_t mk_launch_attention(const MkAttnParams &p, int num_ctas, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
+    cfg.blockDim = dim3(MK_ATTN_THREADS);
+    cfg.dynamicSmemBytes = mk_attn_smem_bytes();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    int n = 0;
+    if (p.cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;   // every block co-resident, or no launch
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, mk::attn::mk_attn_kernel, p);
+}

@@ -95,6 +95,35 @@ struct MkParams {
                                  // rank order and keeps the running sum in registers (BN = 128 only)
 };
 
+// Ring Attention (sequence parallelism): launch parameters of mk_attn_kernel.
+enum MkAttnMode {
+    MK_ATTN_FUSED = 0,        // copy-role blocks forward KV tiles around the ring, compute blocks attend
+    MK_ATTN_COMPUTE_ONLY = 1, // every block attends (the KV it reads is in place, or forwarded earlier)
+    MK_ATTN_COPY_ONLY = 2     // every block forwards KV tiles (first kernel of the unfused form)
+};
+
+#define MK_ATTN_D 128          // supported head dimension
+#define MK_ATTN_THREADS 320    // warp 0 TMA producer, warp 1 MMA, warps 2-9 softmax (two groups of four)
+
+struct MkAttnParams {
+    CUtensorMap tmQ[MK_MAX_P];   // Q_r: dims {d, S, H}, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmK[MK_MAX_P];   // K_r: same
+    CUtensorMap tmV[MK_MAX_P];   // V_r: same
+    CUtensorMap tmR[MK_MAX_P];   // ring buffer of rank r: dims {d, S, (P-1)*2*H}, box {64, 128, 1}
+    const void *k[MK_MAX_P];     // K_r, V_r and the ring buffers as plain pointers (bulk copies)
+    const void *v[MK_MAX_P];
+    void *ring[MK_MAX_P];
+    void *out[MK_MAX_P];         // O_r: H x S x d
+    float *lse[MK_MAX_P];        // H x S or null
+    MkWsHeader *hdr;
+    uint32_t *flags;             // [P][P-1][H][nt] readiness of forwarded KV tiles (epoch-valued)
+    uint64_t timeout_ns;
+    float scale_log2;            // softmax scale * log2(e)
+    int32_t P, H, S, nt, nq;     // nt: 128-row KV tiles per slice; nq: 256-row query units per slice
+    int32_t num_units, num_copies;
+    int32_t mode, copy_ctas, use_ring, out_bf16, cooperative;
+};
+
 // Implemented in mk_abi.cu: set the host thread's mk_last_error() text; bytes of the readiness
 // flag region (which follows the 256-byte header) of the AllReduce workspace for a shape.
 void mk_internal_set_error(const char *msg);
@@ -109,3 +138,8 @@ size_t mk_persistent_smem_bytes(int bn, bool pair);
 cudaError_t mk_max_persistent_ctas(int bn, bool pair, int *ctas);
 cudaError_t mk_launch_persistent(const MkParams &p, int bn, bool pair, int num_ctas, cudaStream_t s);
 cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s);
+
+// Implemented in mk_attention.cu.
+size_t mk_attn_smem_bytes();
+cudaError_t mk_attn_max_ctas(int *ctas);
+cudaError_t mk_launch_attention(const MkAttnParams &p, int num_ctas, cudaStream_t s);

@@ -43,6 +43,7 @@
 
 #include "mk_internal.h"
 #include "mk_ptx.cuh"
+#include "mk_device.cuh"
 #include "mk.h"
 
 namespace mk {
@@ -50,13 +51,6 @@ namespace mk {
 enum { ITEM_END = 0, ITEM_COMPUTE = 1, ITEM_REDUCE = 2 };
 
 #define MK_REDUCE_RING_BYTES (192u * 1024u)   // staging ring of the standalone reduce kernel
-
-// Which wait gave up (written to the workspace header with MK_ERR_TIMEOUT).
-enum {
-    SITE_WORK_EMPTY = 1, SITE_WORK_FULL = 2, SITE_STAGE_EMPTY = 3, SITE_STAGE_FULL = 4,
-    SITE_ACC_EMPTY = 5, SITE_ACC_FULL = 6, SITE_FLAG = 7, SITE_DRAIN = 8, SITE_GATE = 9,
-    SITE_WATCHDOG = 10, SITE_CLAIMED = 11, SITE_ACC_STATE = 12
-};
 
 constexpr int WQ = 4;          // depth of the per-block work queue
 constexpr int ACC = 2;         // TMEM accumulators per block
@@ -108,73 +102,6 @@ struct SmemCtl {
     uint32_t issued;        // number of K-slice loads this CTA's producer issued
     uint32_t epi_done;      // work items the epilogue group has finished (read by the scheduler)
 };
-
-struct Ctx {
-    MkWsHeader *hdr;
-    volatile int *s_abort;
-    uint64_t timeout_ns;     // cross-block waits
-    uint64_t pipe_timeout_ns; // waits inside one block's / pair's pipeline
-};
-
-__device__ __forceinline__ void raise_error(const Ctx &c, uint32_t code, uint32_t site, uint32_t index) {
-    if (atomicCAS(&c.hdr->status, 0u, code) == 0u) {
-        c.hdr->err_site = site;
-        c.hdr->err_index = index;
-    }
-    atomicExch(&c.hdr->abort, 1u);
-    *c.s_abort = 1;
-}
-
-__device__ __forceinline__ bool global_abort(const Ctx &c) {
-    if (*c.s_abort) return true;
-    if (ld_relaxed_gpu(&c.hdr->abort)) {
-        *c.s_abort = 1;
-        return true;
-    }
-    return false;
-}
-
-// Bounded pipeline wait on a local mbarrier (cluster-scope acquire when `CLUSTER`): false only
-// when 4 x timeout has passed or 2^32 polls were made; that raises MK_ERR_TIMEOUT.
-template <bool CLUSTER>
-__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctx &c, uint32_t site, uint32_t index) {
-    auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (poll()) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1; i != 0u; ++i) {
-        if (poll()) return true;
-        if ((i & 63u) == 0u && globaltimer() - t0 > c.pipe_timeout_ns) break;
-    }
-    raise_error(c, MK_ERR_TIMEOUT, site, index);
-    return false;
-}
-
-__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.and.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
-        : "memory");
-    return r != 0u;
-}
-
-// Named-barrier OR over n threads.
-__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
-        : "memory");
-    return r != 0u;
-}
 
 // Grouped raster over a tiles_m x tiles_n grid: groups of G rows walked column by column, so
 // that concurrently computed tiles share A rows and B columns in L2.
@@ -331,21 +258,27 @@ __device__ int2 claim_work(const MkParams &p, const Ctx &c, const ClaimGeom &g, 
     return make_int2(ITEM_END, 0);
 }
 
-// Compute-only, accumulate and chained calls claim a compute unit with one atomic.  Their
-// producer issues the claim of the next unit before it loads the current one, so that the
-// atomic's round trip overlaps those loads instead of falling between the last load of one unit
-// and the first load of the next (only STAGES k-slices are buffered ahead of the MMA).
+// A block that has just queued a compute unit claims the next one with one atomic before it loads
+// the current unit, so that the atomic's round trip overlaps those loads instead of falling
+// between the last load of one unit and the first load of the next (only STAGES k-slices are
+// buffered ahead of the MMA).  The unit claimed ahead is always the block's next item, whatever
+// role the controller publishes meanwhile, so the wait-for relation still follows claim order.
 constexpr uint32_t NO_CLAIM = 0xFFFFFFFFu;
 
 __device__ __forceinline__ bool claims_ahead(const MkParams &p) {
-    return p.op != MK_IOP_AG &&
-           (p.mode == MK_MODE_COMPUTE_ONLY || p.mode == MK_MODE_ACCUMULATE || p.mode == MK_MODE_CHAINED);
+    return p.op != MK_IOP_AG && p.mode != MK_MODE_COMM_ONLY;
 }
 
-// The work item for unit `u`, claimed ahead (see claims_ahead).
+// The work item for unit `u`, claimed ahead (see claims_ahead).  Past the last unit, the role
+// split goes on to reduce items; the other modes have nothing left.
 __device__ int2 item_claimed_ahead(const MkParams &p, const Ctx &c, const ClaimGeom &g, uint32_t u, bool &exhausted,
                                    uint32_t target) {
-    if (global_abort(c) || u >= g.num_units) return make_int2(ITEM_END, 0);
+    if (global_abort(c)) return make_int2(ITEM_END, 0);
+    if (u >= g.num_units) {
+        if (p.mode != MK_MODE_ADAPTIVE && p.mode != MK_MODE_STATIC) return make_int2(ITEM_END, 0);
+        exhausted = true;
+        return claim_work(p, c, g, exhausted, target);
+    }
     if (static_cast<int64_t>(u) == p.skip_unit) return claim_work(p, c, g, exhausted, target);
     return make_int2(ITEM_COMPUTE, static_cast<int>(u));
 }
@@ -857,7 +790,9 @@ __device__ void run_controller(const MkParams &p, const Ctx &c, uint32_t num_uni
         if (trace && nrec < p.trace_cap) {
             mk_trace_record rec;
             rec.t_ns = now - start;
-            rec.target = static_cast<uint32_t>(cur * sms_per_role);
+            // once the compute queue is empty every role unit reduces whatever the target says
+            const bool drained = ld_relaxed_gpu(&h->compute_next) >= num_units;
+            rec.target = static_cast<uint32_t>((drained ? role_units : cur) * sms_per_role);
             rec.units_done = u / done_per_unit;
             rec.tiles_done = d;
             rec.num_blocks = static_cast<uint32_t>(S);

@@ -48,8 +48,8 @@ MK_FLAG_B_NK = 256
 
 # Every extern "C" symbol declared in include/mk.h.
 EXPORTED = ("mk_opts_default", "mk_workspace_size", "mk_gemm_allreduce", "mk_gemm_reducescatter",
-            "mk_allgather_gemm", "mk_gemm_allreduce_noalloc", "mk_status_check", "mk_status_string",
-            "mk_last_error")
+            "mk_allgather_gemm", "mk_ring_attention_workspace_size", "mk_ring_attention",
+            "mk_gemm_allreduce_noalloc", "mk_status_check", "mk_status_string", "mk_last_error")
 
 MK_NOALLOC_MAX_WS_BYTES = 64 << 20
 
@@ -92,6 +92,11 @@ for _name in ("mk_gemm_allreduce", "mk_gemm_reducescatter"):
 _lib.mk_allgather_gemm.argtypes = [_i32, _i64, _i64, _i64, _PP, _PP, _PP, _PP, _i32, _vp,
                                    ctypes.c_size_t, ctypes.POINTER(mk_opts), _vp]
 _lib.mk_allgather_gemm.restype = _i32
+_lib.mk_ring_attention_workspace_size.argtypes = [_i32, _i64, _i64, _i64]
+_lib.mk_ring_attention_workspace_size.restype = ctypes.c_size_t
+_lib.mk_ring_attention.argtypes = [_i32, _i64, _i64, _i64, _PP, _PP, _PP, _PP, _PP, _PP, _i32, ctypes.c_float, _vp,
+                                   ctypes.c_size_t, ctypes.POINTER(mk_opts), _vp]
+_lib.mk_ring_attention.restype = _i32
 _lib.mk_gemm_allreduce_noalloc.argtypes = [_i32, _i64, _i64, _i64, _PP, _PP, _PP, _i32,
                                            ctypes.POINTER(mk_opts), _vp]
 _lib.mk_gemm_allreduce_noalloc.restype = _i32
@@ -164,6 +169,18 @@ def mk_allgather_gemm(P, M, N, K, A_shard, B, A_gathered, C, out_dtype, ws, ws_b
                                       _nbytes(ws) if ws_bytes is None else ws_bytes,
                                       ctypes.byref(opts) if opts is not None else None,
                                       _stream(stream)))
+
+
+def mk_ring_attention_workspace_size(P: int, H: int, S: int, d: int) -> int:
+    return int(_lib.mk_ring_attention_workspace_size(P, H, S, d))
+
+
+def mk_ring_attention(P, H, S, d, Q, K, V, O, lse, kv_ring, out_dtype, scale, ws, ws_bytes=None, opts=None,
+                      stream=None) -> int:
+    """Ring Attention over P sequence slices; lse and kv_ring may be None."""
+    return int(_lib.mk_ring_attention(P, H, S, d, _ptrs(Q), _ptrs(K), _ptrs(V), _ptrs(O), _ptrs(lse), _ptrs(kv_ring),
+                                      out_dtype, float(scale), _addr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                                      ctypes.byref(opts) if opts is not None else None, _stream(stream)))
 
 
 def mk_gemm_allreduce_noalloc(P, M, N, K_per_rank, A, B, C, out_dtype, opts=None, stream=None) -> int:

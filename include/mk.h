@@ -254,6 +254,44 @@ mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *
                             void *cuda_stream);
 
 /*
+ * Ring Attention (sequence parallelism).  (mKernel, Table 3, row "Ring Attention
+ * (SP)": the computations of a ring step are independent of each other; each rank
+ * stores its KV slice to the next rank in 128-row tiles; abstract: speedups on Ring
+ * Attention.)  The sequence is cut into P contiguous slices of S tokens, one per
+ * rank.  At ring step s = 0 .. P-1 rank r attends with its queries to the KV slice
+ * of rank (r - s) mod P, which then moves on to rank r + 1, so that after P steps
+ * every rank's queries have attended to the whole sequence:
+ *   O_r[h][i] = sum over every rank o and key row j of softmax_j(scale * Q_r[h][i] . K_o[h][j]) V_o[h][j]
+ * (full, non-causal softmax attention; the pages do not mention a mask).
+ *   Q[r], K[r], V[r] : H x S x d bf16, row-major (head-major; each row of d contiguous)
+ *   O[r]             : H x S x d, out_dtype
+ *   lse[r]           : H x S fp32 natural-log logsumexp of the scaled scores of every
+ *                      query row, or lse == NULL / every entry NULL: not written
+ *   kv_ring[r]       : (P-1) x 2 x H x S x d bf16 receive buffer of rank r, or
+ *                      kv_ring == NULL / every entry NULL.  Given, the call forwards the
+ *                      KV around the ring: slot s-1 (s = 1 .. P-1) of rank r receives, from
+ *                      rank r-1, the K (index 0) and V (index 1) slice of rank (r - s) mod P,
+ *                      one 128-row tile at a time, and the compute reads each step's
+ *                      slice from there once its tile's readiness flag is set.  Not given,
+ *                      the compute reads every slice in place and nothing is forwarded.
+ *   scale            : softmax scale, 0 = 1/sqrt(d)
+ *   d                : head dimension; 128 is supported (MK_ERR_UNSUPPORTED_SHAPE otherwise)
+ * opts: MK_SPLIT_ADAPTIVE (default) and MK_SPLIT_STATIC run one persistent kernel in
+ * which comm_sms blocks (0 = chosen from the shape) forward the KV tiles while the
+ * others compute; MK_SPLIT_UNFUSED forwards every step's KV in one kernel and attends
+ * in a second.  Other split modes and the GEMM flags are MK_ERR_INVALID_ARG.
+ * Arithmetic: scores Q K^T in fp32 from bf16 operands, probabilities as bf16 for P V,
+ * fp32 accumulation, an online softmax over the KV tiles in ring order.
+ * Workspace: mk_ring_attention_workspace_size(P, H, S, d) bytes, zeroed once (it holds
+ * the header and one readiness flag per forwarded tile).
+ */
+size_t mk_ring_attention_workspace_size(int P, int64_t H, int64_t S, int64_t d);
+mk_status mk_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void *const *Q, const void *const *K,
+                            const void *const *V, void *const *O, float *const *lse, void *const *kv_ring,
+                            mk_dtype out_dtype, float scale, void *ws, size_t ws_bytes, const mk_opts *opts,
+                            void *cuda_stream);
+
+/*
  * GEMM + AllReduce without any device allocation by the caller.  The paper has no
  * counterpart to this entry point; it exists for callers that cannot obtain device
  * memory at run time: runtimes that reserve the whole device up front and hand out

@@ -166,3 +166,51 @@ def test_empty_problem_is_a_no_op(mk):
     # M == 0 or N == 0: validated, then nothing to launch
     assert call_ar(mk, M=0) == mk.MK_OK
     assert call_ar(mk, N=0) == mk.MK_OK
+
+
+def call_attn(mk, P=2, H=2, S=256, d=128, Q=None, K=None, V=None, O=None, lse=None, ring=None, dtype=0, scale=0.0,
+              ws=FAKE, ws_bytes=1 << 30, opts=None):
+    Q = Q if Q is not None else [FAKE] * P
+    K = K if K is not None else [FAKE] * P
+    V = V if V is not None else [FAKE] * P
+    O = O if O is not None else [FAKE] * P
+    return mk.mk_ring_attention(P, H, S, d, Q, K, V, O, lse, ring, dtype, scale, ws, ws_bytes=ws_bytes, opts=opts,
+                                stream=0)
+
+
+def test_ring_attention_argument_checks_return_before_any_launch(mk):
+    assert call_attn(mk, P=0) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, P=17, Q=[FAKE] * 17, K=[FAKE] * 17, V=[FAKE] * 17, O=[FAKE] * 17) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, S=-1) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, dtype=3) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, scale=-1.0) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, d=64) == mk.MK_ERR_UNSUPPORTED_SHAPE and "head dimension" in mk.mk_last_error()
+    assert call_attn(mk, ws=0) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, Q=[FAKE, 0]) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, V=[FAKE, FAKE + 8]) == mk.MK_ERR_ALIGNMENT
+    assert call_attn(mk, lse=[FAKE, 0]) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, ring=[FAKE, 0]) == mk.MK_ERR_INVALID_ARG
+    assert call_attn(mk, ring=[FAKE, FAKE + 4]) == mk.MK_ERR_ALIGNMENT
+    assert call_attn(mk, ws=FAKE + 64) == mk.MK_ERR_ALIGNMENT
+    assert call_attn(mk, ws_bytes=256) == mk.MK_ERR_WORKSPACE_TOO_SMALL
+    for mode in (mk.MK_SPLIT_ACCUMULATE, mk.MK_SPLIT_CHAINED):
+        o = mk.mk_opts_default()
+        o.split_mode = mode
+        assert call_attn(mk, opts=o) == mk.MK_ERR_INVALID_ARG
+    for flag in (mk.MK_FLAG_BF16_PARTIALS, mk.MK_FLAG_B_NK):
+        o = mk.mk_opts_default()
+        o.flags = flag
+        assert call_attn(mk, opts=o) == mk.MK_ERR_INVALID_ARG
+    # nothing to compute: validated, then no launch
+    assert call_attn(mk, H=0) == mk.MK_OK
+    assert call_attn(mk, S=0) == mk.MK_OK
+
+
+def test_ring_attention_workspace_size(mk):
+    # header, then one 32-bit readiness flag per forwarded 128-row KV tile: P * (P-1) * H * ceil(S/128)
+    for P, H, S in ((2, 2, 256), (8, 32, 4096), (3, 5, 130), (1, 4, 1000)):
+        n = P * (P - 1) * H * ((S + 127) // 128)
+        want = 256 + ((max(n, 1) * 4 + 255) // 256) * 256
+        assert mk.mk_ring_attention_workspace_size(P, H, S, 128) == want
+    assert mk.mk_ring_attention_workspace_size(0, 1, 1, 128) == 0
+    assert mk.mk_ring_attention_workspace_size(2, -1, 1, 128) == 0
