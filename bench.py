@@ -735,7 +735,7 @@ class RingProblem:
         mk, wl = self.mk, self.wl
         mode = {"fused": mk.MK_SPLIT_ADAPTIVE, "static": mk.MK_SPLIT_STATIC, "unfused": mk.MK_SPLIT_UNFUSED,
                 "inplace": mk.MK_SPLIT_ADAPTIVE}[form]
-        o = self.api.make_opts(mode, comm_sms=comm_sms)
+        o = self.api.make_opts(mode, comm_sms=comm_sms, flags=_EXTRA_FLAGS & 8)   # MK_FLAG_NO_COOPERATIVE
         return mk.mk_ring_attention(wl.P, wl.H, wl.S, wl.d, self.Qd, self.Kd, self.Vd, self.O, self.L,
                                     None if form == "inplace" else self.R, mk.MK_BF16, 0.0, self.ws, opts=o,
                                     stream=stream)

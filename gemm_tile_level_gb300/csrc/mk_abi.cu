@@ -560,20 +560,6 @@ size_t attn_workspace_bytes(int P, int64_t H, int64_t S) {
     return MK_WS_HEADER_BYTES + align_up(static_cast<size_t>(nflags > 0 ? nflags : 1) * sizeof(uint32_t), MK_WS_ALIGN);
 }
 
-// Communication blocks of the fused form: in proportion to the copy's share of the SM time, at
-// per-SM rates taken low on purpose for the copies (about 40 GB/s of bulk copies through shared
-// memory against 8 TFLOP/s of attention per SM), so that the forwarded tiles of a head are ready
-// before the compute blocks reach them.
-int attn_copy_blocks(int grid, int P, int64_t H, int64_t S, int64_t d) {
-    const double copy_bytes = static_cast<double>(P) * (P - 1) * H * S * d * 2.0 * 2.0;
-    const double flops = 4.0 * static_cast<double>(P * S) * static_cast<double>(P * S) * d * H;
-    const double tc = copy_bytes / 40e9, ta = flops / 8e12;
-    int n = static_cast<int>(grid * tc / (tc + ta) + 0.5);
-    if (n < 1) n = 1;
-    if (n > grid - 1) n = grid - 1;
-    return n;
-}
-
 mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void *const *Q, const void *const *K,
                              const void *const *V, void *const *O, float *const *lse, void *const *kv_ring,
                              mk_dtype out_dtype, float scale, void *ws, size_t ws_bytes, const mk_opts *opts_in,
@@ -678,7 +664,9 @@ mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void 
         return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the attention kernel");
     }
     p.mode = MK_ATTN_FUSED;
-    p.copy_ctas = o.comm_sms > 0 ? o.comm_sms : attn_copy_blocks(grid, P, H, S, d);
+    // by default the compute blocks' own copy warps forward every tile; a static split adds
+    // comm_sms whole communication blocks
+    p.copy_ctas = o.split_mode == MK_SPLIT_STATIC ? o.comm_sms : 0;
     e = mk_launch_attention(p, grid, s);
     return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the fused Ring Attention kernel");
 }

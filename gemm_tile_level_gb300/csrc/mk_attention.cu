@@ -28,6 +28,13 @@
 //             (otherwise the stale maximum is kept, so P stays below 256)
 // and at the end of the unit O / l and lse = (m + log2 l) ln 2 go to memory.
 //
+//   warp 10   the communication role inside the compute block: forwards KV tiles around the ring
+//             (register copies), claiming them in ring order from a grid-wide counter, so that no
+//             SM is taken from the attention
+// Blocks given the communication role outright (a static split) forward tiles from the same
+// counter with bulk copies through shared memory; so does every block of the unfused form's
+// first kernel.
+//
 // Every wait is bounded (see mk_device.cuh); a wait that runs out raises MK_ERR_TIMEOUT and
 // the grid-wide abort, after which every block drains what it has in flight and exits.
 #include "mk.h"
@@ -106,6 +113,43 @@ __device__ bool wait_flag(const Ctx &c, const uint32_t *f, uint32_t epoch, uint3
 }
 
 // ------------------------------------------------------------------ communication role
+// Copy item `item` (ring order: head, then step s = 1..P-1, then receiving rank r, then tile t):
+// the K and V rows of KV tile t of head h that rank r receives from rank r-1 at step s.  Its
+// source is rank r-1's own K, V at step 1 and, later, what rank r-1 received one step earlier.
+struct CopyItem {
+    int h, s, r, t, src_rank;
+    uint32_t bytes;          // bytes of the K rows (and of the V rows)
+    const char *src[2];
+    char *dst[2];
+};
+
+__device__ __forceinline__ CopyItem copy_item(const MkAttnParams &p, int item) {
+    CopyItem x;
+    const int per_step = p.P * p.nt;
+    const int per_head = (p.P - 1) * per_step;
+    x.h = item / per_head;
+    const int rem = item - x.h * per_head;
+    x.s = rem / per_step + 1;
+    const int rem2 = rem - (x.s - 1) * per_step;
+    x.r = rem2 / p.nt;
+    x.t = rem2 - x.r * p.nt;
+    x.src_rank = (x.r + p.P - 1) % p.P;
+    const int rows = min(BKV, p.S - x.t * BKV);
+    x.bytes = static_cast<uint32_t>(rows) * D * 2;
+    const size_t row0 = static_cast<size_t>(x.t) * BKV;
+    for (int kv = 0; kv < 2; ++kv) {
+        if (x.s == 1)
+            x.src[kv] = static_cast<const char *>(kv ? p.v[x.src_rank] : p.k[x.src_rank]) +
+                        (static_cast<size_t>(x.h) * p.S + row0) * D * 2;
+        else
+            x.src[kv] = static_cast<const char *>(p.ring[x.src_rank]) +
+                        (((static_cast<size_t>(x.s - 2) * 2 + kv) * p.H + x.h) * p.S + row0) * D * 2;
+        x.dst[kv] = static_cast<char *>(p.ring[x.r]) +
+                    (((static_cast<size_t>(x.s - 1) * 2 + kv) * p.H + x.h) * p.S + row0) * D * 2;
+    }
+    return x;
+}
+
 // One copy warp forwards KV tile t of head h from rank r-1 to rank r at ring step s: the K and the
 // V rows of the tile (contiguous in both buffers) move through three 8 KiB staging buffers with
 // bulk copies, then the tile's flag is released.  At step 1 the source is rank r-1's own K_{r-1},
@@ -114,31 +158,12 @@ __device__ bool wait_flag(const Ctx &c, const uint32_t *f, uint32_t epoch, uint3
 // finishes a copy before it starts the next, so the copies always make progress.
 __device__ void copy_tile(const MkAttnParams &p, const Ctx &c, int item, uint8_t *stage, uint64_t *bars,
                           uint32_t &seq, uint32_t epoch) {
-    const int per_step = p.P * p.nt;
-    const int per_head = (p.P - 1) * per_step;
-    const int h = item / per_head;
-    const int rem = item - h * per_head;
-    const int s = rem / per_step + 1;
-    const int rem2 = rem - (s - 1) * per_step;
-    const int r = rem2 / p.nt;
-    const int t = rem2 - r * p.nt;
-    const int src_rank = (r + p.P - 1) % p.P;
-    const int rows = min(BKV, p.S - t * BKV);
-    const uint32_t bytes = static_cast<uint32_t>(rows) * D * 2;
-    const size_t row0 = static_cast<size_t>(t) * BKV;
-    const char *src[2];
-    char *dst[2];
-    for (int kv = 0; kv < 2; ++kv) {
-        if (s == 1)
-            src[kv] = static_cast<const char *>(kv ? p.v[src_rank] : p.k[src_rank]) +
-                      (static_cast<size_t>(h) * p.S + row0) * D * 2;
-        else
-            src[kv] = static_cast<const char *>(p.ring[src_rank]) +
-                      (((static_cast<size_t>(s - 2) * 2 + kv) * p.H + h) * p.S + row0) * D * 2;
-        dst[kv] = static_cast<char *>(p.ring[r]) + (((static_cast<size_t>(s - 1) * 2 + kv) * p.H + h) * p.S + row0) * D * 2;
-    }
-    if (s >= 2) {
-        if (!wait_flag(c, kv_flag(p, src_rank, s - 1, h, t), epoch, static_cast<uint32_t>(item))) return;
+    const CopyItem x = copy_item(p, item);
+    const uint32_t bytes = x.bytes;
+    const char *const *src = x.src;
+    char *const *dst = x.dst;
+    if (x.s >= 2) {
+        if (!wait_flag(c, kv_flag(p, x.src_rank, x.s - 1, x.h, x.t), epoch, static_cast<uint32_t>(item))) return;
         fence_proxy_async_global();   // the acquire above before the bulk reads of the source
     }
     const uint32_t npk = (bytes + COPY_PIECE - 1) / COPY_PIECE;   // pieces per K (or V) part
@@ -178,21 +203,73 @@ __device__ void copy_tile(const MkAttnParams &p, const Ctx &c, int item, uint8_t
     seq += npieces;
     bulk_wait_all();
     fence_proxy_async_global();        // the bulk writes before the release below
-    st_release_gpu(kv_flag(p, r, s, h, t), epoch);
+    st_release_gpu(kv_flag(p, x.r, x.s, x.h, x.t), epoch);
 }
 
-__device__ void run_copies(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, int copy_block, int nblocks,
-                           int warp, uint32_t epoch) {
+// Copy items are claimed in ring order from one grid-wide counter by every copy worker (the warps
+// of communication blocks, and warp 10 of compute blocks in the fused form).  A copy waits only on
+// a copy with a smaller index, which was claimed earlier by a worker that is copying and waits on
+// nothing else, so the copies always make progress whatever the compute blocks do.
+__device__ __forceinline__ int claim_copy(const MkAttnParams &p) { return static_cast<int>(atomicAdd(&p.hdr->reduce_next, 1u)); }
+
+// A communication block's warp (one thread): bulk copies through its slice of shared memory.
+__device__ void run_copies(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, int warp, uint32_t epoch) {
     const int cw = warp - 2;
     uint8_t *stage = smem + static_cast<uint32_t>(cw) * COPY_BUFS * COPY_PIECE;   // a copy block holds no tiles
     uint64_t *bars = s.cbar[cw];
     uint32_t seq = 0;
-    const int workers = nblocks * COPY_WARPS;
-    for (int item = copy_block * COPY_WARPS + cw; item < p.num_copies; item += workers) {
+    for (;;) {
         if (global_abort(c)) break;
+        const int item = claim_copy(p);
+        if (item >= p.num_copies) break;
         copy_tile(p, c, item, stage, bars, seq, epoch);
     }
     bulk_wait_all();
+}
+
+// Warp 10 of a compute block: the same copies with 16-byte register loads and stores, sixteen per
+// lane in flight (8 KiB per warp).
+__device__ void run_copy_warp(const MkAttnParams &p, const Ctx &c, int lane, uint32_t epoch) {
+    constexpr int DEPTH = 16;
+    for (;;) {
+        int item = 0, stop = 0;
+        if (lane == 0) {
+            stop = global_abort(c) ? 1 : 0;
+            item = stop ? 0 : claim_copy(p);
+        }
+        stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
+        item = __shfl_sync(0xFFFFFFFFu, item, 0);
+        if (stop || item >= p.num_copies) break;
+        const CopyItem x = copy_item(p, item);
+        if (x.s >= 2) {
+            int ok = 1;
+            if (lane == 0) ok = wait_flag(c, kv_flag(p, x.src_rank, x.s - 1, x.h, x.t), epoch, static_cast<uint32_t>(item));
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;   // lane 0's acquire, then the warp barrier, orders the loads
+        }
+        const uint32_t n16 = x.bytes / 16;      // 16-byte pieces of the K (or V) rows
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint4 *from = reinterpret_cast<const uint4 *>(x.src[kv]);
+            uint4 *to = reinterpret_cast<uint4 *>(x.dst[kv]);
+            for (uint32_t base = 0; base < n16; base += 32 * DEPTH) {
+                uint4 v[DEPTH];
+#pragma unroll
+                for (int k = 0; k < DEPTH; ++k) {
+                    const uint32_t i = base + static_cast<uint32_t>(k * 32 + lane);
+                    if (i < n16) v[k] = __ldcg(from + i);
+                }
+#pragma unroll
+                for (int k = 0; k < DEPTH; ++k) {
+                    const uint32_t i = base + static_cast<uint32_t>(k * 32 + lane);
+                    if (i < n16) to[i] = v[k];
+                }
+            }
+        }
+        __syncwarp();                           // every lane's stores before lane 0's release
+        if (lane == 0) {
+            __threadfence();
+            st_release_gpu(kv_flag(p, x.r, x.s, x.h, x.t), epoch);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ compute role
@@ -347,31 +424,69 @@ __device__ void run_mma(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *sm
     wait_bar<false>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
 }
 
-// One pass over a row's 128 scores in TMEM (four 32-column loads): the probabilities
-// 2^(s * cl - m) as packed bf16 pairs (column pairs 2i, 2i+1 in pk[i]), their fp32 sum and the
-// row's largest valid score.  Columns at or past `valid` (the end of the sequence slice) count as
-// probability 0.
+// Two fp32 lanes at once (sm_100 family packed fp32 arithmetic, each lane IEEE-rounded exactly
+// as the scalar instruction would be).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// One pass over a row's 128 scores in TMEM (eight 16-column loads): the probabilities
+// 2^(s * cl - m) as packed bf16 pairs (columns 2i, 2i+1 in pk[i]), their fp32 sum and the row's
+// largest valid score.  With MASK, columns at or past `valid` (the end of the sequence slice)
+// count as probability 0.
+template <bool MASK>
 __device__ __forceinline__ void softmax_pass(uint32_t t_s, int valid, float cl, float m, uint32_t (&pk)[64],
                                              float &rowsum, float &mx) {
-    rowsum = 0.0f;
+    const uint64_t c2 = f2_pack(cl, cl), nm2 = f2_pack(-m, -m);
+    uint64_t sum2 = f2_pack(0.0f, 0.0f);
     mx = -INFINITY;
+    // the load of chunk cc + 1 is in flight while chunk cc is worked on
+    uint32_t buf[2][16];
+    tmem_ld16_nowait(t_s, buf[0]);
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc) {
-        uint32_t v[16];
-        tmem_ld16(t_s + static_cast<uint32_t>(cc * 16), v);
+        uint32_t (&v)[16] = buf[cc & 1];
+        tmem_wait_ld16(v);
+        if (cc + 1 < 8) tmem_ld16_nowait(t_s + static_cast<uint32_t>((cc + 1) * 16), buf[(cc + 1) & 1]);
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
             const int col = cc * 16 + i;
-            const float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
-            const bool ok0 = col < valid, ok1 = col + 1 < valid;
-            const float p0 = ok0 ? ex2_approx(fmaf(x0, cl, -m)) : 0.0f;
-            const float p1 = ok1 ? ex2_approx(fmaf(x1, cl, -m)) : 0.0f;
-            if (ok0) mx = fmaxf(mx, x0);
-            if (ok1) mx = fmaxf(mx, x1);
-            rowsum += p0 + p1;
+            float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
+            if (MASK) {
+                if (col >= valid) x0 = -INFINITY;
+                if (col + 1 >= valid) x1 = -INFINITY;
+            }
+            mx = max3(mx, x0, x1);
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(x0, x1), c2, nm2), a0, a1);   // s * cl - m, both lanes
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);   // 2^-inf = 0 for masked columns
+            sum2 = f2_add(sum2, f2_pack(p0, p1));
             pk[col >> 1] = pack_bf16x2(p0, p1);
         }
     }
+    float s0, s1;
+    f2_unpack(sum2, s0, s1);
+    rowsum = s0 + s1;
 }
 
 // Softmax group g (warps 2-5: g = 0, query tile A; warps 6-9: g = 1, tile B).  The running
@@ -419,7 +534,10 @@ __device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t
 #pragma unroll 1
             for (int attempt = 0;; ++attempt) {
                 float mx;
-                softmax_pass(t_s, valid, cl, m, pk, rowsum, mx);
+                if (valid == BKV)
+                    softmax_pass<false>(t_s, valid, cl, m, pk, rowsum, mx);
+                else
+                    softmax_pass<true>(t_s, valid, cl, m, pk, rowsum, mx);
                 const float mt = mx * cl;
                 const bool grow = attempt == 0 && mt > m + 8.0f;
                 if (!__any_sync(0xFFFFFFFFu, grow)) break;
@@ -503,6 +621,7 @@ __device__ void finish_call(const MkAttnParams &p, uint32_t epoch) {
     if (prev == gridDim.x - 1) {
         __threadfence();
         h->acc_state = MK_ACC_DIRTY;   // the flags are not accumulator tiles of a GEMM call
+        h->reduce_next = 0;            // the copy counter
         h->abort = 0;
         h->epoch = epoch;
         h->done_ctas = 0;
@@ -568,12 +687,13 @@ __global__ void __launch_bounds__(MK_ATTN_THREADS, 1) mk_attn_kernel(const __gri
             if (lane == 0) run_producer(p, c, s, smem, blockIdx.x, ncompute, epoch);
         } else if (warp == 1) {
             if (lane == 0) run_mma(p, c, s, smem, tmem, blockIdx.x, ncompute);
-        } else {
+        } else if (warp < 10) {
             run_softmax(p, c, s, smem, tmem, blockIdx.x, ncompute, warp < 6 ? 0 : 1, warp, lane);
+        } else if (p.mode == MK_ATTN_FUSED) {
+            run_copy_warp(p, c, lane, epoch);
         }
-    } else if (warp >= 2 && lane == 0) {
-        const int nblocks = static_cast<int>(gridDim.x) - ncompute;
-        run_copies(p, c, s, smem, static_cast<int>(blockIdx.x) - ncompute, nblocks, warp, epoch);
+    } else if (warp >= 2 && warp < 2 + COPY_WARPS && lane == 0) {
+        run_copies(p, c, s, smem, warp, epoch);
     }
     __syncwarp();
     tc_fence_before();

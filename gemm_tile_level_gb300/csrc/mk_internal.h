@@ -103,7 +103,8 @@ enum MkAttnMode {
 };
 
 #define MK_ATTN_D 128          // supported head dimension
-#define MK_ATTN_THREADS 320    // warp 0 TMA producer, warp 1 MMA, warps 2-9 softmax (two groups of four)
+#define MK_ATTN_THREADS 352    // warp 0 TMA producer, warp 1 MMA, warps 2-9 softmax (two groups of four),
+                               // warp 10 forwards KV tiles around the ring
 
 struct MkAttnParams {
     CUtensorMap tmQ[MK_MAX_P];   // Q_r: dims {d, S, H}, box {64, 128, 1}, 128-byte swizzle

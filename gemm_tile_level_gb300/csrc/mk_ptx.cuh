@@ -471,6 +471,30 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// 16 consecutive 32-bit columns of the warp's 32 TMEM lanes, without waiting: the registers hold
+// the values only after tmem_wait_ld16 on them.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Wait for every tcgen05.ld this thread issued; the registers of `v` are tied to the wait so
+// that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                   "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                   "+r"(v[14]), "+r"(v[15])
+                 :
+                 : "memory");
+}
+
 // 2^x with the hardware approximation (subnormal results flush to zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

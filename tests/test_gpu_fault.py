@@ -35,8 +35,12 @@ def test_missing_unit_times_out_then_recovers(split, tiles):
     gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
 
 
-def test_controller_trace_records():
-    wl = ig.sweep_workload(4096)
+@pytest.mark.parametrize("M,first_target", [(4096, 0), (256, 16)])
+def test_controller_trace_records(M, first_target):
+    """The controller's records: time, units and reduced tiles never go backwards; the target
+    starts where the host put it (no reduce role in rank-major order, eight SM pairs in tile-major
+    order) and is the whole grid once every compute unit has been claimed."""
+    wl = ig.sweep_workload(M)
     A, B, Ad, Bd = gu.upload(wl)
     trace = torch.zeros(4096 * 32, dtype=torch.uint8, device="cuda")
     gu.call_ar(Ad, Bd, mk.MK_BF16, opts=api.make_opts(mk.MK_SPLIT_ADAPTIVE, trace=trace))
@@ -47,7 +51,9 @@ def test_controller_trace_records():
     rec = rec[:n]
     S = gu.num_sms()
     assert (rec["blocks"] == S).all()
-    assert (rec["target"] >= 0).all() and (rec["target"] <= S - 1).all()
+    assert (rec["target"] >= 0).all() and (rec["target"] <= S).all()
+    assert rec["target"][0] == first_target
+    assert rec["target"][-1] == S
     assert (np.diff(rec["t"].astype(np.int64)) >= 0).all()
     assert (np.diff(rec["units"].astype(np.int64)) >= 0).all()
     assert (np.diff(rec["tiles"].astype(np.int64)) >= 0).all()
