@@ -537,14 +537,14 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
 }
 
 // ------------------------------------------------------------------ Ring Attention
-// bf16 3-D tensor {cols (inner), rows, planes}, row-major planes, box {64, 128, 1}, 128-byte
+// bf16 3-D tensor {cols (inner), rows, planes}, row-major planes, box {64, box_rows, 1}, 128-byte
 // swizzle; rows past the end of a plane read as zero.
-mk_status encode_3d(CUtensorMap *map, const void *ptr, int64_t planes, int64_t rows, int64_t cols) {
+mk_status encode_3d(CUtensorMap *map, const void *ptr, int64_t planes, int64_t rows, int64_t cols, int box_rows) {
     auto enc = encoder();
     if (!enc) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(rows * cols) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -582,7 +582,7 @@ mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void 
     if (d != MK_ATTN_D) return fail(MK_ERR_UNSUPPORTED_SHAPE, "head dimension d=%lld (supported: %d)", (long long)d, MK_ATTN_D);
     if (H > INT32_MAX || S > INT32_MAX || H * S > INT32_MAX)
         return fail(MK_ERR_UNSUPPORTED_SHAPE, "H * S above 2^31-1");
-    const int64_t nq = (S + 255) / 256;
+    const int64_t nq = (S + 511) / 512;   // a query unit: 512 rows, four 128-row tiles over an SM pair
     if (H * P * nq > INT32_MAX || H * P * (P - 1) * attn_kv_tiles(S) > INT32_MAX)
         return fail(MK_ERR_UNSUPPORTED_SHAPE, "too many tiles");
     if (H == 0 || S == 0) return MK_OK;
@@ -616,17 +616,21 @@ mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void 
     const int grid = o.num_ctas > 0 ? o.num_ctas : resident;
     if (grid > resident)
         return fail(MK_ERR_NOT_RESIDENT, "persistent grid of %d blocks cannot be co-resident (%d fit)", grid, resident);
-    if (grid < 2) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d too small", grid);
-    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > grid - 1)
+    if (grid < 2 || (grid & 1)) return fail(MK_ERR_INVALID_ARG, "num_ctas=%d: the grid is SM pairs (even, >= 2)", grid);
+    if (o.split_mode == MK_SPLIT_STATIC && o.comm_sms > grid - 2)
         return fail(MK_ERR_INVALID_ARG, "comm_sms=%d leaves no compute SMs in a grid of %d", o.comm_sms, grid);
 
     MkAttnParams p;
     memset(&p, 0, sizeof p);
     for (int r = 0; r < P; ++r) {
-        if ((st = encode_3d(&p.tmQ[r], Q[r], H, S, d)) != MK_OK) return st;
-        if ((st = encode_3d(&p.tmK[r], K[r], H, S, d)) != MK_OK) return st;
-        if ((st = encode_3d(&p.tmV[r], V[r], H, S, d)) != MK_OK) return st;
-        if (ring && (st = encode_3d(&p.tmR[r], kv_ring[r], static_cast<int64_t>(P - 1) * 2 * H, S, d)) != MK_OK) return st;
+        if ((st = encode_3d(&p.tmQ[r], Q[r], H, S, d, 128)) != MK_OK) return st;
+        if ((st = encode_3d(&p.tmK[r], K[r], H, S, d, 64)) != MK_OK) return st;
+        if ((st = encode_3d(&p.tmV[r], V[r], H, S, d, 128)) != MK_OK) return st;
+        if (ring) {
+            const int64_t planes = static_cast<int64_t>(P - 1) * 2 * H;
+            if ((st = encode_3d(&p.tmRK[r], kv_ring[r], planes, S, d, 64)) != MK_OK) return st;
+            if ((st = encode_3d(&p.tmRV[r], kv_ring[r], planes, S, d, 128)) != MK_OK) return st;
+        }
         p.k[r] = K[r];
         p.v[r] = V[r];
         p.ring[r] = ring ? kv_ring[r] : nullptr;
@@ -666,7 +670,7 @@ mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void 
     p.mode = MK_ATTN_FUSED;
     // by default the compute blocks' own copy warps forward every tile; a static split adds
     // comm_sms whole communication blocks
-    p.copy_ctas = o.split_mode == MK_SPLIT_STATIC ? o.comm_sms : 0;
+    p.copy_ctas = o.split_mode == MK_SPLIT_STATIC ? (o.comm_sms + 1) / 2 * 2 : 0;   // whole SM pairs
     e = mk_launch_attention(p, grid, s);
     return e == cudaSuccess ? MK_OK : fail_cuda(e, "launch of the fused Ring Attention kernel");
 }

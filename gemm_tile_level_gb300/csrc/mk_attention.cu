@@ -1,7 +1,7 @@
 // mk_attention.cu -- Ring Attention (sequence parallelism) for sm_103a: one persistent kernel
 // whose blocks either forward KV tiles around the ring (communication role) or run the
-// attention of 256 query rows against the whole sequence's KV, slice by slice in ring order
-// (compute role).
+// attention of 512 query rows per SM pair against the whole sequence's KV, slice by slice in
+// ring order (compute role).
 //
 // Method (mKernel: Fast Multi-GPU, Multi-Node Fused Kernels; Table 3, row "Ring Attention (SP)";
 // abstract, Figure 2): the sequence is cut into P slices, one per rank.  At ring step s rank r
@@ -13,24 +13,25 @@
 // of each tile before loading it.  Without ring buffers the compute blocks read every slice in
 // place.
 //
-// Compute block (320 threads, one per SM, persistent): a unit is (head h, rank r, 256 query
-// rows), computed as two 128-row query tiles A and B over the P * nt KV tiles of the sequence in
-// ring order (step 0 = the rank's own slice).  Per KV tile j:
-//   warp 0    TMA: K_j and V_j (two 64-column boxes each, 128-byte swizzle) into a ring of three
-//             32 KiB slots, in the order K_0, K_1, V_0, K_2, V_1, ... (keys run one tile ahead)
-//   warp 1    tcgen05.mma (M = 128, N = 128, K = 16 steps):
-//               S_A(j+1) = Q_A K_{j+1}^T, O_A += P_A(j) V_j, S_B(j+1) = Q_B K_{j+1}^T, O_B += P_B(j) V_j
-//             S_A, S_B, O_A, O_B are 128 columns of TMEM each (all 512)
+// Compute blocks run as SM pairs (clusters of two, tcgen05 cta_group::2; 352 threads each).  A
+// unit is (head h, rank r, 512 query rows) over the P * nt KV tiles of the sequence in ring order
+// (step 0 = the rank's own slice): two 256-row query tiles A and B, of which each CTA holds 128
+// rows, so that one MMA spans both SMs and each CTA loads only half of every K and V tile.
+// Per KV tile j:
+//   warp 0    TMA: this CTA's 64 rows of K_j and 64 columns of V_j (16 KiB each, 128-byte swizzle)
+//             into a ring of ten slots, in the order K_0, V_0, K_1, V_1, ...
+//   warp 1    (even CTA) tcgen05.mma, M = 256 over the pair:
+//               O_A += P_A(j) V_j, S_A(j+1) = Q_A K_{j+1}^T, O_B += P_B(j) V_j, S_B(j+1) = Q_B K_{j+1}^T
+//             S_A, S_B, O_A, O_B are 128 TMEM columns each (all 512); P_X is read from TMEM
 //   warps 2-5 softmax of tile A, warps 6-9 of tile B (one query row per thread = one TMEM lane):
-//             load S, running maximum m in the log2 domain, P = 2^(S*scale*log2e - m) to shared
-//             memory as bf16 (the layout a K-major operand tile has), row sum l in fp32; when the
-//             maximum grows by more than 8 (a factor 256), rescale O in TMEM and l first
-//             (otherwise the stale maximum is kept, so P stays below 256)
+//             running maximum m in the log2 domain, P = 2^(S*scale*log2e - m) as bf16 written back
+//             over the first 64 columns of S, row sum l in fp32; when the maximum grows by more
+//             than 8 (a factor 256), O and l are rescaled first (otherwise the stale maximum is
+//             kept, so P stays below 256)
 // and at the end of the unit O / l and lse = (m + log2 l) ln 2 go to memory.
-//
-//   warp 10   the communication role inside the compute block: forwards KV tiles around the ring
+//   warp 10   the communication role inside every compute block: forwards KV tiles around the ring
 //             (register copies), claiming them in ring order from a grid-wide counter, so that no
-//             SM is taken from the attention
+//             SM is taken from the attention.
 // Blocks given the communication role outright (a static split) forward tiles from the same
 // counter with bulk copies through shared memory; so does every block of the unfused form's
 // first kernel.
@@ -45,38 +46,47 @@
 namespace mk {
 namespace attn {
 
-constexpr int BQ = 128;                          // query rows per tile
+constexpr int BQ = 128;                          // query rows per CTA tile (one TMEM lane each)
 constexpr int BKV = 128;                         // KV rows per tile
 constexpr int D = MK_ATTN_D;
-constexpr uint32_t BOX_BYTES = 128 * 64 * 2;     // one 64-column box of 128 rows
-constexpr uint32_t TILE_BYTES = 2 * BOX_BYTES;   // one Q, K, V or P tile (128 x 128 bf16)
-constexpr int NSLOT = 3;                         // KV ring slots
+constexpr uint32_t QBOX = 128 * 64 * 2;          // a 64-column box of 128 rows (16 KiB)
+constexpr uint32_t QTILE = 2 * QBOX;             // one CTA's 128 query rows x d
+constexpr uint32_t KBOX = 64 * 64 * 2;           // a 64-column box of 64 rows (8 KiB)
+constexpr uint32_t SLOT = 16384;                 // one CTA's half of a K tile (64 rows x d) or of a V tile (128 rows x 64)
+constexpr int NSLOT = 10;                        // KV ring slots (five KV tiles)
 constexpr int COPY_WARPS = 8;                    // warps 2-9 of a communication block
 constexpr uint32_t COPY_PIECE = 8192;            // bytes per bulk copy piece
 constexpr int COPY_BUFS = 3;                     // staging buffers per copy warp
-constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV) & ~(1u << 16);   // B = K tile, K-major
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D);                   // B = V tile, MN-major
+// SM-pair MMAs (M = 256: each CTA's 128 rows): S = Q K^T with N = 128 KV rows (each CTA supplies 64,
+// K-major), O += P V with N = d = 128 (each CTA supplies 64 columns of V, MN-major) and P read from
+// tensor memory
+constexpr uint32_t IDESC_S = idesc_bf16_f32(2 * BQ, BKV) & ~(1u << 16);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(2 * BQ, D);
 
-// Shared memory (1024-byte aligned): Q_A, Q_B, three KV slots, P_A, P_B (7 x 32 KiB), then control.
+// Shared memory (1024-byte aligned): Q_A, Q_B (this CTA's rows), ten 16 KiB KV slots, then control.
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = 2 * TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_KV + NSLOT * TILE_BYTES;
-constexpr uint32_t DATA_BYTES = OFF_P + 2 * TILE_BYTES;
+constexpr uint32_t OFF_KV = 2 * QTILE;
+constexpr uint32_t DATA_BYTES = OFF_KV + NSLOT * SLOT;
 static_assert(COPY_WARPS * COPY_BUFS * COPY_PIECE <= DATA_BYTES, "copy staging fits");
 
+// Barriers.  Those the MMA thread (even CTA) waits on live in the even CTA: q_full and kv_full (two
+// producers' expected bytes), p_full and o_free (four softmax warps of each CTA).  Those the MMA
+// commits to are multicast to both CTAs: q_empty, kv_empty, s_full, o_done.
 struct Ctl {
     uint64_t q_full, q_empty;
     uint64_t kv_full[NSLOT], kv_empty[NSLOT];
-    uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain;
     uint64_t cbar[COPY_WARPS][COPY_BUFS];
     uint32_t tmem_base;
     uint32_t epoch;
     int abort;
-    uint32_t kv_issued;     // KV loads the producer issued
-    uint32_t q_issued;      // Q loads the producer issued
+    uint32_t kv_issued, q_issued;              // loads this CTA's producer issued
+    uint32_t peer_kv_issued, peer_q_issued;    // even CTA: the odd CTA's counts, stored there at exit
 };
 
+// A unit: head h, rank r, 512 query rows (qp): tile A is rows [0, 256) of it, tile B [256, 512);
+// CTA c of the pair holds rows [128 c, 128 c + 128) of each.
 struct Unit {
     int h, r, qp;
 };
@@ -273,154 +283,146 @@ __device__ void run_copy_warp(const MkAttnParams &p, const Ctx &c, int lane, uin
 }
 
 // ------------------------------------------------------------------ compute role
-// Operand descriptors: a 128-row tile is two 64-column boxes of 16 KiB (128-byte rows, 128-byte
-// swizzle).  K-major operands (Q, P as A; K as B) advance 32 bytes per 16-column K step inside a
-// box; the V tile (B, MN-major: K = KV rows, N = d columns) advances 16 rows = 2 KiB per K step,
-// with its two 64-column boxes 16 KiB apart.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-    return sw128_desc(tile + static_cast<uint32_t>(kk >> 2) * BOX_BYTES + static_cast<uint32_t>(kk & 3) * 32u, 16, 1024);
+// Operand descriptors.  Q (A of S = Q K^T): two 64-column boxes of 128 rows, K-major, 32 bytes per
+// 16-column K step.  This CTA's 64 rows of a K tile (B, K-major): two 64-column boxes of 64 rows.
+// This CTA's 64 columns of a V tile (B, MN-major: K = KV rows, N = d): one box of 128 rows, 16 rows
+// = 2 KiB per K step.
+__device__ __forceinline__ uint64_t q_desc(uint32_t tile, int kk) {
+    return sw128_desc(tile + static_cast<uint32_t>(kk >> 2) * QBOX + static_cast<uint32_t>(kk & 3) * 32u, 16, 1024);
+}
+__device__ __forceinline__ uint64_t k_desc(uint32_t slot, int kk) {
+    return sw128_desc(slot + static_cast<uint32_t>(kk >> 2) * KBOX + static_cast<uint32_t>(kk & 3) * 32u, 16, 1024);
+}
+__device__ __forceinline__ uint64_t v_desc(uint32_t slot, int kk) {
+    return sw128_desc(slot + static_cast<uint32_t>(kk) * 2048u, SLOT, 1024);
 }
 
-__device__ __forceinline__ void mma_s(uint32_t d_tmem, uint32_t q_tile, uint32_t k_tile) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-        umma_bf16(d_tmem, kmajor_desc(q_tile, kk), kmajor_desc(k_tile, kk), IDESC_S, static_cast<uint32_t>(kk != 0));
-}
-
-__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tile, uint32_t v_tile, bool accumulate) {
-#pragma unroll
-    for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(d_tmem, kmajor_desc(p_tile, kk), sw128_desc(v_tile + static_cast<uint32_t>(kk) * 2048u, BOX_BYTES, 1024),
-                  IDESC_PV, static_cast<uint32_t>(accumulate || kk != 0));
-}
-
-// Producer (warp 0, one thread): Q of each unit, then the KV tiles in the order K_0, K_1, V_0,
-// K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}, which is the order the MMA thread consumes them.
-__device__ void run_producer(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, int cblock, int ncompute,
-                             uint32_t epoch) {
+// Producer (warp 0 of each CTA, one thread): this CTA's rows of Q for each unit, then its halves of
+// the KV tiles in the order K_0, V_0, K_1, V_1, ..., counted on the even CTA's barriers.
+__device__ void run_producer(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, int pair, int npairs,
+                             uint32_t crank, uint32_t epoch) {
     const uint32_t base = smem_u32(smem);
     const int n = p.P * p.nt;
     const uint64_t pol_q = policy_evict_first();
     const uint64_t pol_kv = policy_evict_last();   // every query unit of the head reads them
+    const uint32_t q_full0 = mapa_shared(smem_u32(&s.q_full), 0);
+    const uint32_t kv_full0 = mapa_shared(smem_u32(&s.kv_full[0]), 0);
+    const int half = static_cast<int>(crank);
     uint32_t q = 0, k = 0;
     bool stop = false;
-    for (int u = cblock; u < p.num_units && !stop; u += ncompute, ++k) {
+    for (int u = pair; u < p.num_units && !stop; u += npairs, ++k) {
         if (global_abort(c)) break;
         const Unit x = unit_of(p, u);
         if (k > 0 && !wait_bar<false>(smem_u32(&s.q_empty), (k - 1) & 1u, c, SITE_STAGE_EMPTY, u)) break;
-        mbar_arrive_expect_tx(smem_u32(&s.q_full), 4 * BOX_BYTES);
-        for (int half = 0; half < 2; ++half)
+        mbar_arrive_expect_tx_cluster(q_full0, 2 * QTILE);
+        for (int g = 0; g < 2; ++g)
             for (int box = 0; box < 2; ++box)
-                tma_load_3d_hint(base + OFF_Q + half * TILE_BYTES + box * BOX_BYTES, &p.tmQ[x.r], smem_u32(&s.q_full),
-                                 box * 64, x.qp * 2 * BQ + half * BQ, x.h, pol_q);
-        ++s.q_issued;
-        // the load sequence: (tile, kind) with kind 0 = K, 1 = V
+                tma_load_3d_pair_hint(base + OFF_Q + g * QTILE + box * QBOX, &p.tmQ[x.r], q_full0, box * 64,
+                                      x.qp * 4 * BQ + g * 2 * BQ + half * BQ, x.h, pol_q);
+        s.q_issued = k + 1;
         for (int e = 0; e < 2 * n && !stop; ++e) {
-            int j, kind;
-            if (e == 0) { j = 0; kind = 0; }
-            else if (e == 2 * n - 1) { j = n - 1; kind = 1; }
-            else if (e & 1) { j = (e + 1) / 2; kind = 0; }   // K_{j}, j = 1..n-1
-            else { j = e / 2 - 1; kind = 1; }                 // V_{j}, j = 0..n-2
+            const int j = e >> 1, kind = e & 1;   // kind 0 = this CTA's 64 rows of K_j, 1 = its 64 columns of V_j
             const int st = j / p.nt, t = j - st * p.nt;
             const int o = (x.r - st + p.P) % p.P;
-            const CUtensorMap *map;
-            int z;
-            if (st == 0 || !p.use_ring) {
-                map = kind ? &p.tmV[o] : &p.tmK[o];
-                z = x.h;
-            } else {
-                map = &p.tmR[x.r];
-                z = ((st - 1) * 2 + kind) * p.H + x.h;
-                if (kind == 0 && p.mode == MK_ATTN_FUSED) {
-                    if (!wait_flag(c, kv_flag(p, x.r, st, x.h, t), epoch, static_cast<uint32_t>(u))) { stop = true; break; }
-                    fence_proxy_async_global();   // the acquire before the TMA reads of the tile
-                }
+            const bool ring = st > 0 && p.use_ring;
+            if (ring && kind == 0 && p.mode == MK_ATTN_FUSED) {
+                if (!wait_flag(c, kv_flag(p, x.r, st, x.h, t), epoch, static_cast<uint32_t>(u))) { stop = true; break; }
+                fence_proxy_async_global();   // the acquire before the TMA reads of the tile
             }
             const uint32_t slot = q % NSLOT;
             if (q >= NSLOT && !wait_bar<false>(smem_u32(&s.kv_empty[slot]), ((q / NSLOT) - 1) & 1u, c, SITE_STAGE_EMPTY, u)) {
                 stop = true;
                 break;
             }
-            const uint32_t dst = base + OFF_KV + slot * TILE_BYTES;
-            mbar_arrive_expect_tx(smem_u32(&s.kv_full[slot]), TILE_BYTES);
-            tma_load_3d_hint(dst, map, smem_u32(&s.kv_full[slot]), 0, t * BKV, z, pol_kv);
-            tma_load_3d_hint(dst + BOX_BYTES, map, smem_u32(&s.kv_full[slot]), 64, t * BKV, z, pol_kv);
+            const uint32_t dst = base + OFF_KV + slot * SLOT;
+            const uint32_t bar = kv_full0 + 8u * slot;
+            mbar_arrive_expect_tx_cluster(bar, SLOT);
+            const int z = ring ? ((st - 1) * 2 + kind) * p.H + x.h : x.h;
+            if (kind == 0) {
+                const CUtensorMap *map = ring ? &p.tmRK[x.r] : &p.tmK[o];
+                tma_load_3d_pair_hint(dst, map, bar, 0, t * BKV + half * (BKV / 2), z, pol_kv);
+                tma_load_3d_pair_hint(dst + KBOX, map, bar, 64, t * BKV + half * (BKV / 2), z, pol_kv);
+            } else {
+                const CUtensorMap *map = ring ? &p.tmRV[x.r] : &p.tmV[o];
+                tma_load_3d_pair_hint(dst, map, bar, half * 64, t * BKV, z, pol_kv);
+            }
             ++q;
             s.kv_issued = q;
         }
     }
-    // every TMA load this thread issued must have landed before the block exits
-    const uint32_t nq = s.kv_issued;
-    for (uint32_t i = nq > NSLOT ? nq - NSLOT : 0; i < nq; ++i)
-        wait_bar<false>(smem_u32(&s.kv_full[i % NSLOT]), (i / NSLOT) & 1u, c, SITE_DRAIN, i);
-    if (s.q_issued) wait_bar<false>(smem_u32(&s.q_full), (s.q_issued - 1) & 1u, c, SITE_DRAIN, 0);
 }
 
-// MMA issue (warp 1, one thread).  Per KV tile j the order is S_A(j+1), O_A += P_A(j) V_j,
-// S_B(j+1), O_B += P_B(j) V_j, so that each softmax group has the other group's MMAs to hide
-// behind.  Completion counters (all continue across units) give each barrier's phase parity.
-__device__ void run_mma(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, uint32_t tmem, int cblock,
-                        int ncompute) {
+// MMA issue (warp 1 of the even CTA, one thread).  P_X lives in the first 64 TMEM columns of S_X,
+// so S_X(j+1) is issued after O_X += P_X(j) V_j, which MMA issue order keeps behind it.  Per KV
+// tile j: O_A += P_A(j) V_j, S_A(j+1), O_B += P_B(j) V_j, S_B(j+1): while one softmax group works,
+// the tensor cores run the other group's two MMAs.
+__device__ void run_mma(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, uint32_t tmem, int pair,
+                        int npairs) {
     const uint32_t base = smem_u32(smem);
     const int n = p.P * p.nt;
     uint32_t q = 0;                  // KV sequence position
-    uint32_t ns[2] = {0, 0};         // S MMAs issued per group
-    uint32_t npv[2] = {0, 0};        // PV MMAs issued per group
+    uint32_t np[2] = {0, 0};         // P tiles consumed per group
     uint32_t k = 0;
     bool ok = true;
-    auto take = [&](uint32_t &slot) -> bool {   // the next KV tile of the sequence
+    auto take = [&](uint32_t &slot) -> bool {   // the next KV half tile of the sequence
         slot = q % NSLOT;
         const bool r = wait_bar<false>(smem_u32(&s.kv_full[slot]), (q / NSLOT) & 1u, c, SITE_STAGE_FULL, q);
         ++q;
         tc_fence_after();
         return r;
     };
-    auto issue_s = [&](int g, uint32_t k_tile) -> bool {
-        if (ns[g] > 0 && !wait_bar<false>(smem_u32(&s.s_free[g]), (ns[g] - 1) & 1u, c, SITE_ACC_EMPTY, ns[g])) return false;
+    auto issue_s = [&](int g, uint32_t kslot) {
+        const uint32_t qt = base + OFF_Q + static_cast<uint32_t>(g) * QTILE;
+        const uint32_t kt = base + OFF_KV + kslot * SLOT;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            umma_bf16_pair(tmem + static_cast<uint32_t>(g) * 128u, q_desc(qt, kk), k_desc(kt, kk), IDESC_S,
+                           static_cast<uint32_t>(kk != 0));
+        umma_commit_pair(smem_u32(&s.s_full[g]), 0x3);
+    };
+    auto issue_pv = [&](int g, uint32_t vslot, bool first) -> bool {
+        if (!wait_bar<true>(smem_u32(&s.p_full[g]), np[g] & 1u, c, SITE_ACC_FULL, np[g])) return false;
+        ++np[g];
+        if (first && k > 0 && !wait_bar<true>(smem_u32(&s.o_free[g]), (k - 1) & 1u, c, SITE_ACC_EMPTY, k)) return false;
         tc_fence_after();
-        mma_s(tmem + static_cast<uint32_t>(g) * 128u, base + OFF_Q + static_cast<uint32_t>(g) * TILE_BYTES, k_tile);
-        umma_commit(smem_u32(&s.s_full[g]));
-        ++ns[g];
+        const uint32_t vt = base + OFF_KV + vslot * SLOT;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+            umma_bf16_pair_ts(tmem + 256u + static_cast<uint32_t>(g) * 128u,
+                              tmem + static_cast<uint32_t>(g) * 128u + static_cast<uint32_t>(kk) * 8u, v_desc(vt, kk),
+                              IDESC_PV, static_cast<uint32_t>(!first || kk != 0));
         return true;
     };
-    auto issue_pv = [&](int g, uint32_t v_tile, bool first) -> bool {
-        if (!wait_bar<false>(smem_u32(&s.p_full[g]), npv[g] & 1u, c, SITE_ACC_FULL, npv[g])) return false;
-        if (first && k > 0 && !wait_bar<false>(smem_u32(&s.o_free[g]), (k - 1) & 1u, c, SITE_ACC_EMPTY, k)) return false;
-        tc_fence_after();
-        mma_pv(tmem + 256u + static_cast<uint32_t>(g) * 128u, base + OFF_P + static_cast<uint32_t>(g) * TILE_BYTES, v_tile,
-               !first);
-        umma_commit(smem_u32(&s.o_done[g]));
-        ++npv[g];
-        return true;
-    };
-    for (int u = cblock; u < p.num_units && ok; u += ncompute, ++k) {
+    for (int u = pair; u < p.num_units && ok; u += npairs, ++k) {
         if (!wait_bar<false>(smem_u32(&s.q_full), k & 1u, c, SITE_STAGE_FULL, u)) break;
         tc_fence_after();
         uint32_t ks, vs;
         if (!(ok = take(ks))) break;
-        if (!(ok = issue_s(0, base + OFF_KV + ks * TILE_BYTES))) break;
-        if (!(ok = issue_s(1, base + OFF_KV + ks * TILE_BYTES))) break;
-        umma_commit(smem_u32(&s.kv_empty[ks]));
-        if (n == 1) umma_commit(smem_u32(&s.q_empty));
+        issue_s(0, ks);
+        issue_s(1, ks);
+        umma_commit_pair(smem_u32(&s.kv_empty[ks]), 0x3);
+        if (n == 1) umma_commit_pair(smem_u32(&s.q_empty), 0x3);
         for (int j = 0; j < n && ok; ++j) {
             const bool more = j + 1 < n;
+            if (!(ok = take(vs))) break;
+            if (!(ok = issue_pv(0, vs, j == 0))) break;
+            if (!more) umma_commit_pair(smem_u32(&s.o_done[0]), 0x3);
             if (more) {
                 if (!(ok = take(ks))) break;
-                if (!(ok = issue_s(0, base + OFF_KV + ks * TILE_BYTES))) break;
+                issue_s(0, ks);
             }
-            if (!(ok = take(vs))) break;
-            if (!(ok = issue_pv(0, base + OFF_KV + vs * TILE_BYTES, j == 0))) break;
+            if (!(ok = issue_pv(1, vs, j == 0))) break;
+            if (!more) umma_commit_pair(smem_u32(&s.o_done[1]), 0x3);
+            umma_commit_pair(smem_u32(&s.kv_empty[vs]), 0x3);
             if (more) {
-                if (!(ok = issue_s(1, base + OFF_KV + ks * TILE_BYTES))) break;
-                umma_commit(smem_u32(&s.kv_empty[ks]));
-                if (j + 2 == n) umma_commit(smem_u32(&s.q_empty));   // the unit's last S MMAs are issued
+                issue_s(1, ks);
+                umma_commit_pair(smem_u32(&s.kv_empty[ks]), 0x3);
+                if (j + 2 == n) umma_commit_pair(smem_u32(&s.q_empty), 0x3);   // the unit's last S MMAs are issued
             }
-            if (!(ok = issue_pv(1, base + OFF_KV + vs * TILE_BYTES, j == 0))) break;
-            umma_commit(smem_u32(&s.kv_empty[vs]));
         }
     }
     // every MMA issued must complete before TMEM is released
-    umma_commit(smem_u32(&s.drain));
+    umma_commit_pair(smem_u32(&s.drain), 0x1);
     wait_bar<false>(smem_u32(&s.drain), 0, c, SITE_DRAIN, 0);
 }
 
@@ -489,24 +491,31 @@ __device__ __forceinline__ void softmax_pass(uint32_t t_s, int valid, float cl, 
     rowsum = s0 + s1;
 }
 
-// Softmax group g (warps 2-5: g = 0, query tile A; warps 6-9: g = 1, tile B).  The running
-// maximum m is only raised when a tile's maximum exceeds it by more than 8 (in the log2 domain);
-// otherwise the probabilities are formed against the stale maximum (at most 2^8), which needs no
-// first pass for the tile maximum.  A unit's first tile takes one (m = -inf), and a row whose
-// tile maximum does exceed m + 8 forms the tile again against its new maximum, after O and l are
-// scaled down by 2^(m_old - m_new).
-__device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *smem, uint32_t tmem, int cblock,
-                            int ncompute, int g, int warp, int lane) {
+// Softmax group g of a CTA (warps 2-5: g = 0, query tile A; warps 6-9: g = 1, tile B): one query
+// row per thread (its TMEM lane).  The running maximum m is only raised when a tile's maximum
+// exceeds it by more than 8 (in the log2 domain); otherwise the probabilities are formed against
+// the stale maximum (at most 2^8), which needs no first pass for the tile maximum.  A unit's first
+// tile takes one (m = -inf), and a row whose tile maximum does exceed m + 8 forms its tile again
+// against the new maximum, after O and l are scaled down by 2^(m_old - m_new).  P goes back into the
+// first 64 TMEM columns of S as packed bf16 pairs, where the P V MMA reads it.
+__device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint32_t tmem, int pair, int npairs,
+                            uint32_t crank, int g, int warp, int lane) {
     const int quarter = warp & 3;                 // the TMEM lane quarter this warp may access
-    const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
+    const int row = quarter * 32 + lane;          // query row in the CTA tile = TMEM lane
     const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lanes + static_cast<uint32_t>(g) * 128u;
     const uint32_t t_o = tmem + lanes + 256u + static_cast<uint32_t>(g) * 128u;
-    const uint32_t p_tile = smem_u32(smem + OFF_P + static_cast<uint32_t>(g) * TILE_BYTES);
+    const uint32_t p_full0 = mapa_shared(smem_u32(&s.p_full[g]), 0);
+    const uint32_t o_free0 = mapa_shared(smem_u32(&s.o_free[g]), 0);
+    auto arrive_even = [&](uint32_t local_bar, uint32_t even_bar) {   // on the even CTA's barrier
+        if (crank == 0) mbar_arrive(local_bar);
+        else mbar_arrive_cluster(even_bar);
+    };
     const int n = p.P * p.nt;
     const float cl = p.scale_log2;
     uint32_t gt = 0;       // KV tiles processed by this group (all units)
-    for (int u = cblock; u < p.num_units; u += ncompute) {
+    uint32_t k = 0;
+    for (int u = pair; u < p.num_units; u += npairs, ++k) {
         const Unit x = unit_of(p, u);
         float m = -INFINITY, l = 0.0f;
         for (int j = 0; j < n; ++j, ++gt) {
@@ -548,42 +557,28 @@ __device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t
                     m = mt;
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s.s_free[g]));
-            if (j > 0) {
-                // the previous P V has finished reading P and writing O
-                if (!wait_bar<false>(smem_u32(&s.o_done[g]), (gt - 1) & 1u, c, SITE_ACC_FULL, gt)) return;
-                tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+            // every MMA before S(j), the previous P V included, has completed: O may be rescaled
+            if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll 1
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t ov[16];
-                        tmem_ld16(t_o + static_cast<uint32_t>(cc * 16), ov);
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t ov[16];
+                    tmem_ld16(t_o + static_cast<uint32_t>(cc * 16), ov);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st16(t_o + static_cast<uint32_t>(cc * 16), ov);
-                    }
+                    for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st16(t_o + static_cast<uint32_t>(cc * 16), ov);
                 }
             }
             l = l * alpha + rowsum;
-            // P into the K-major swizzled layout: 16-byte chunk (row, g8) of box g8 / 8 sits at
-            // row * 128 + ((g8 % 8) ^ (row % 8)) * 16
-#pragma unroll
-            for (int g8 = 0; g8 < 16; ++g8) {
-                const uint32_t addr = p_tile + static_cast<uint32_t>(g8 >> 3) * BOX_BYTES + static_cast<uint32_t>(row) * 128u +
-                                      (static_cast<uint32_t>((g8 & 7) ^ (row & 7)) << 4);
-                st_shared_u4(addr, pk[4 * g8], pk[4 * g8 + 1], pk[4 * g8 + 2], pk[4 * g8 + 3]);
-            }
-            fence_proxy_async_smem();   // the generic-proxy stores of P before the tensor core reads them
+            tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(t_s + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s.p_full[g]));
+            if (lane == 0) arrive_even(smem_u32(&s.p_full[g]), p_full0);
         }
         // epilogue: O / l and the logsumexp of the unit's query rows
-        if (!wait_bar<false>(smem_u32(&s.o_done[g]), (gt - 1) & 1u, c, SITE_ACC_FULL, gt)) return;
+        if (!wait_bar<false>(smem_u32(&s.o_done[g]), k & 1u, c, SITE_ACC_FULL, k)) return;
         tc_fence_after();
-        const int qrow = x.qp * 2 * BQ + g * BQ + row;
+        const int qrow = x.qp * 4 * BQ + g * 2 * BQ + static_cast<int>(crank) * BQ + row;
         const bool store = qrow < p.S;
         const size_t obase = (static_cast<size_t>(x.h) * p.S + (store ? qrow : 0)) * D;
 #pragma unroll 1
@@ -609,7 +604,7 @@ __device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t
         if (store && p.lse[x.r]) p.lse[x.r][static_cast<size_t>(x.h) * p.S + qrow] = (m + log2f(l)) * 0.69314718055994531f;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s.o_free[g]));
+        if (lane == 0) arrive_even(smem_u32(&s.o_free[g]), o_free0);
     }
 }
 
@@ -629,37 +624,61 @@ __device__ void finish_call(const MkAttnParams &p, uint32_t epoch) {
     }
 }
 
+// Run by the even CTA's thread 0 between two cluster barriers at exit: every load either producer
+// issued has landed.  Both producers issue the same sequence, so load i of the KV ring uses
+// kv_full[i % NSLOT] in phase (i / NSLOT) & 1 and only the last NSLOT can be outstanding; a load
+// armed by one producer only (the other stopped after a failed wait) gets the missing arrival here.
+__device__ void drain_loads(Ctl &s, const Ctx &c) {
+    const uint32_t nl = s.kv_issued, np = s.peer_kv_issued;
+    const uint32_t n = nl > np ? nl : np;
+    for (uint32_t i = n > NSLOT ? n - NSLOT : 0; i < n; ++i) {
+        const uint32_t bar = smem_u32(&s.kv_full[i % NSLOT]);
+        if (i >= nl) mbar_arrive(bar);
+        if (i >= np) mbar_arrive(bar);
+        wait_bar<false>(bar, (i / NSLOT) & 1u, c, SITE_DRAIN, i);
+    }
+    const uint32_t ql = s.q_issued, qp = s.peer_q_issued;
+    const uint32_t qn = ql > qp ? ql : qp;
+    if (qn > 0) {
+        const uint32_t bar = smem_u32(&s.q_full);
+        if (ql < qn) mbar_arrive(bar);
+        if (qp < qn) mbar_arrive(bar);
+        wait_bar<false>(bar, (qn - 1) & 1u, c, SITE_DRAIN, qn);
+    }
+}
+
 __global__ void __launch_bounds__(MK_ATTN_THREADS, 1) mk_attn_kernel(const __grid_constant__ MkAttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Ctl &s = *reinterpret_cast<Ctl *>(smem + DATA_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_ctarank();
+    const int npairs_all = static_cast<int>(gridDim.x) >> 1;
     const int ncompute = p.mode == MK_ATTN_COPY_ONLY ? 0
-                         : p.mode == MK_ATTN_COMPUTE_ONLY ? static_cast<int>(gridDim.x)
-                                                          : static_cast<int>(gridDim.x) - p.copy_ctas;
-    const bool compute = static_cast<int>(blockIdx.x) < ncompute;
+                         : p.mode == MK_ATTN_COMPUTE_ONLY ? npairs_all
+                                                          : npairs_all - (p.copy_ctas >> 1);   // compute pairs
+    const int pair = static_cast<int>(blockIdx.x) >> 1;
+    const bool compute = pair < ncompute;
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&s.q_full), 1);
+        mbar_init(smem_u32(&s.q_full), 2);
         mbar_init(smem_u32(&s.q_empty), 1);
         for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(smem_u32(&s.kv_full[i]), 1);
+            mbar_init(smem_u32(&s.kv_full[i]), 2);
             mbar_init(smem_u32(&s.kv_empty[i]), 1);
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(smem_u32(&s.s_full[g]), 1);
-            mbar_init(smem_u32(&s.s_free[g]), 4);
-            mbar_init(smem_u32(&s.p_full[g]), 4);
+            mbar_init(smem_u32(&s.p_full[g]), 8);
             mbar_init(smem_u32(&s.o_done[g]), 1);
-            mbar_init(smem_u32(&s.o_free[g]), 4);
+            mbar_init(smem_u32(&s.o_free[g]), 8);
         }
         mbar_init(smem_u32(&s.drain), 1);
         for (int w = 0; w < COPY_WARPS; ++w)
             for (int b = 0; b < COPY_BUFS; ++b) mbar_init(smem_u32(&s.cbar[w][b]), 1);
         fence_mbar_init();
         s.abort = 0;
-        s.kv_issued = 0;
-        s.q_issued = 0;
+        s.kv_issued = s.q_issued = s.peer_kv_issued = s.peer_q_issued = 0;
         uint32_t e = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
         if (e == 0u) e = 1u;
         s.epoch = e;
@@ -669,14 +688,17 @@ __global__ void __launch_bounds__(MK_ATTN_THREADS, 1) mk_attn_kernel(const __gri
             prefetch_tmap(&p.tmQ[r]);
             prefetch_tmap(&p.tmK[r]);
             prefetch_tmap(&p.tmV[r]);
-            if (p.use_ring) prefetch_tmap(&p.tmR[r]);
+            if (p.use_ring) {
+                prefetch_tmap(&p.tmRK[r]);
+                prefetch_tmap(&p.tmRV[r]);
+            }
         }
     if (compute && warp == 1) {
-        tmem_alloc(smem_u32(&s.tmem_base), 512);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(&s.tmem_base), 512);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t epoch = s.epoch;
     const Ctx c{p.hdr, &s.abort, p.timeout_ns, 4 * p.timeout_ns};
@@ -684,11 +706,11 @@ __global__ void __launch_bounds__(MK_ATTN_THREADS, 1) mk_attn_kernel(const __gri
     if (compute) {
         const uint32_t tmem = s.tmem_base;
         if (warp == 0) {
-            if (lane == 0) run_producer(p, c, s, smem, blockIdx.x, ncompute, epoch);
+            if (lane == 0) run_producer(p, c, s, smem, pair, ncompute, crank, epoch);
         } else if (warp == 1) {
-            if (lane == 0) run_mma(p, c, s, smem, tmem, blockIdx.x, ncompute);
+            if (lane == 0 && crank == 0) run_mma(p, c, s, smem, tmem, pair, ncompute);
         } else if (warp < 10) {
-            run_softmax(p, c, s, smem, tmem, blockIdx.x, ncompute, warp < 6 ? 0 : 1, warp, lane);
+            run_softmax(p, c, s, tmem, pair, ncompute, crank, warp < 6 ? 0 : 1, warp, lane);
         } else if (p.mode == MK_ATTN_FUSED) {
             run_copy_warp(p, c, lane, epoch);
         }
@@ -696,10 +718,16 @@ __global__ void __launch_bounds__(MK_ATTN_THREADS, 1) mk_attn_kernel(const __gri
         run_copies(p, c, s, smem, warp, epoch);
     }
     __syncwarp();
+    if (threadIdx.x == 0 && crank == 1) {
+        st_cluster_u32(mapa_shared(smem_u32(&s.peer_kv_issued), 0), s.kv_issued);
+        st_cluster_u32(mapa_shared(smem_u32(&s.peer_q_issued), 0), s.q_issued);
+    }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
+    if (compute && threadIdx.x == 0 && crank == 0) drain_loads(s, c);
+    cluster_sync();
     tc_fence_after();
-    if (compute && warp == 1) tmem_dealloc(s.tmem_base, 512);
+    if (compute && warp == 1) tmem_dealloc_pair(s.tmem_base, 512);
     if (threadIdx.x == 0) finish_call(p, epoch);
 }
 
@@ -723,15 +751,31 @@ cudaError_t mk_attn_max_ctas(int *ctas) {
     e = cudaFuncSetAttribute(mk::attn::mk_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
+    int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mk::attn::mk_attn_kernel, MK_ATTN_THREADS,
-                                                      mk_attn_smem_bytes());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    cfg.blockDim = dim3(MK_ATTN_THREADS);
+    cfg.dynamicSmemBytes = mk_attn_smem_bytes();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, mk::attn::mk_attn_kernel, &cfg);
     if (e != cudaSuccess) return e;
-    *ctas = per_sm * sms;
+    *ctas = 2 * clusters;
     if (dev >= 0 && dev < 64) cached[dev] = *ctas + 1;
     return cudaSuccess;
 }
+
+// Whether this process's runtime accepted a cooperative launch of the clustered kernel (-1
+// unknown, 0 no, 1 yes); without it co-residency rests on the occupancy check made before every
+// launch, and the bounded waits turn a starved grid into an error.
+static int g_attn_coop = -1;
 
 cudaError_t mk_launch_attention(const MkAttnParams &p, int num_ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -739,14 +783,25 @@ cudaError_t mk_launch_attention(const MkAttnParams &p, int num_ctas, cudaStream_
     cfg.blockDim = dim3(MK_ATTN_THREADS);
     cfg.dynamicSmemBytes = mk_attn_smem_bytes();
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    int n = 0;
-    if (p.cooperative) {
-        attr[n].id = cudaLaunchAttributeCooperative;   // every block co-resident, or no launch
-        attr[n].val.cooperative = 1;
-        ++n;
-    }
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = n;
+    if (p.cooperative && g_attn_coop != 0) {
+        attr[1].id = cudaLaunchAttributeCooperative;   // every block co-resident, or no launch
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, mk::attn::mk_attn_kernel, p);
+        if (e == cudaSuccess) {
+            g_attn_coop = 1;
+            return e;
+        }
+        if (g_attn_coop == 1) return e;
+        (void)cudaGetLastError();   // configuration error, not sticky: retry without it
+        g_attn_coop = 0;
+    }
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, mk::attn::mk_attn_kernel, p);
 }

@@ -108,9 +108,10 @@ enum MkAttnMode {
 
 struct MkAttnParams {
     CUtensorMap tmQ[MK_MAX_P];   // Q_r: dims {d, S, H}, box {64, 128, 1}, 128-byte swizzle
-    CUtensorMap tmK[MK_MAX_P];   // K_r: same
-    CUtensorMap tmV[MK_MAX_P];   // V_r: same
-    CUtensorMap tmR[MK_MAX_P];   // ring buffer of rank r: dims {d, S, (P-1)*2*H}, box {64, 128, 1}
+    CUtensorMap tmK[MK_MAX_P];   // K_r: dims {d, S, H}, box {64, 64, 1} (half of a KV tile's rows)
+    CUtensorMap tmV[MK_MAX_P];   // V_r: dims {d, S, H}, box {64, 128, 1}
+    CUtensorMap tmRK[MK_MAX_P];  // ring buffer of rank r: dims {d, S, (P-1)*2*H}, box {64, 64, 1} (K planes)
+    CUtensorMap tmRV[MK_MAX_P];  // the same buffer, box {64, 128, 1} (V planes)
     const void *k[MK_MAX_P];     // K_r, V_r and the ring buffers as plain pointers (bulk copies)
     const void *v[MK_MAX_P];
     void *ring[MK_MAX_P];
@@ -120,7 +121,7 @@ struct MkAttnParams {
     uint32_t *flags;             // [P][P-1][H][nt] readiness of forwarded KV tiles (epoch-valued)
     uint64_t timeout_ns;
     float scale_log2;            // softmax scale * log2(e)
-    int32_t P, H, S, nt, nq;     // nt: 128-row KV tiles per slice; nq: 256-row query units per slice
+    int32_t P, H, S, nt, nq;     // nt: 128-row KV tiles per slice; nq: 512-row query units per slice
     int32_t num_units, num_copies;
     int32_t mode, copy_ctas, use_ring, out_bf16, cooperative;
 };
@@ -140,7 +141,7 @@ cudaError_t mk_max_persistent_ctas(int bn, bool pair, int *ctas);
 cudaError_t mk_launch_persistent(const MkParams &p, int bn, bool pair, int num_ctas, cudaStream_t s);
 cudaError_t mk_launch_reduce(const MkParams &p, int bn, int num_ctas, cudaStream_t s);
 
-// Implemented in mk_attention.cu.
+// Implemented in mk_attention.cu (SM pairs: clusters of two blocks).
 size_t mk_attn_smem_bytes();
 cudaError_t mk_attn_max_ctas(int *ctas);
 cudaError_t mk_launch_attention(const MkAttnParams &p, int num_ctas, cudaStream_t s);

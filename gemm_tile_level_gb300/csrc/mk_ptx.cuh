@@ -495,6 +495,30 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
                  : "memory");
 }
 
+// 3-D tiled TMA load into this CTA's shared memory whose completion is counted on an mbarrier of
+// either CTA of the pair (`bar_cluster` is a shared::cluster address), with an L2 policy.
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar_cluster, int32_t x,
+                                                      int32_t y, int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(tmap), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// D (+)= A * B over the pair with A in tensor memory: each CTA supplies its M/2 rows of A from its
+// own TMEM at `a_tmem` (row = lane, K = 16 bf16 as 8 columns of packed pairs) and its half of B
+// (N/2 columns) from shared memory; issued by one thread of the even CTA.
+__device__ __forceinline__ void umma_bf16_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 2^x with the hardware approximation (subnormal results flush to zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

@@ -205,7 +205,7 @@ ATTN_WORKLOADS = {
                                          normal(1.0)),
     "ring_p8_h32_s4096_d128": AttnWorkload("ring_p8_h32_s4096_d128", 8, 32, 4096, 128, normal(1.0), normal(1.0),
                                            normal(1.0)),
-    # the same sequence with 4 heads: a case small enough for a full profiler capture
-    "ring_p8_h4_s4096_d128": AttnWorkload("ring_p8_h4_s4096_d128", 8, 4, 4096, 128, normal(1.0), normal(1.0),
+    # the same sequence with 8 heads: a case small enough for a full profiler capture
+    "ring_p8_h8_s4096_d128": AttnWorkload("ring_p8_h8_s4096_d128", 8, 8, 4096, 128, normal(1.0), normal(1.0),
                                           normal(1.0)),
 }
