@@ -287,15 +287,16 @@ __device__ void run_copy_warp(const MkAttnParams &p, const Ctx &c, int lane, uin
 // 16-column K step.  This CTA's 64 rows of a K tile (B, K-major): two 64-column boxes of 64 rows.
 // This CTA's 64 columns of a V tile (B, MN-major: K = KV rows, N = d): one box of 128 rows, 16 rows
 // = 2 KiB per K step.
-__device__ __forceinline__ uint64_t q_desc(uint32_t tile, int kk) {
-    return sw128_desc(tile + static_cast<uint32_t>(kk >> 2) * QBOX + static_cast<uint32_t>(kk & 3) * 32u, 16, 1024);
-}
-__device__ __forceinline__ uint64_t k_desc(uint32_t slot, int kk) {
-    return sw128_desc(slot + static_cast<uint32_t>(kk >> 2) * KBOX + static_cast<uint32_t>(kk & 3) * 32u, 16, 1024);
-}
-__device__ __forceinline__ uint64_t v_desc(uint32_t slot, int kk) {
-    return sw128_desc(slot + static_cast<uint32_t>(kk) * 2048u, SLOT, 1024);
-}
+// A descriptor's start address is its low 14-bit field in 16-byte units; every operand here lies
+// below 256 KiB of shared memory, so a K step adds its byte offset / 16 to a base descriptor with no
+// carry into the other fields.  (Building each descriptor from scratch cost the single issuing
+// thread about 85 cycles per MMA, more than an M = 256, N = 128, K = 16 MMA takes.)
+__device__ __forceinline__ constexpr uint64_t q_step(int kk) { return ((kk >> 2) * QBOX + (kk & 3) * 32u) >> 4; }
+__device__ __forceinline__ constexpr uint64_t k_step(int kk) { return ((kk >> 2) * KBOX + (kk & 3) * 32u) >> 4; }
+__device__ __forceinline__ constexpr uint64_t v_step(int kk) { return (kk * 2048u) >> 4; }
+__device__ __forceinline__ uint64_t q_desc0(uint32_t tile) { return sw128_desc(tile, 16, 1024); }
+__device__ __forceinline__ uint64_t k_desc0(uint32_t slot) { return sw128_desc(slot, 16, 1024); }
+__device__ __forceinline__ uint64_t v_desc0(uint32_t slot) { return sw128_desc(slot, SLOT, 1024); }
 
 // Producer (warp 0 of each CTA, one thread): this CTA's rows of Q for each unit, then its halves of
 // the KV tiles in the order K_0, V_0, K_1, V_1, ..., counted on the even CTA's barriers.
@@ -371,13 +372,13 @@ __device__ void run_mma(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *sm
         tc_fence_after();
         return r;
     };
+    const uint64_t qd[2] = {q_desc0(base + OFF_Q), q_desc0(base + OFF_Q + QTILE)};
     auto issue_s = [&](int g, uint32_t kslot) {
-        const uint32_t qt = base + OFF_Q + static_cast<uint32_t>(g) * QTILE;
-        const uint32_t kt = base + OFF_KV + kslot * SLOT;
+        const uint64_t kd = k_desc0(base + OFF_KV + kslot * SLOT);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(g) * 128u;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16_pair(tmem + static_cast<uint32_t>(g) * 128u, q_desc(qt, kk), k_desc(kt, kk), IDESC_S,
-                           static_cast<uint32_t>(kk != 0));
+            umma_bf16_pair(d_tmem, qd[g] + q_step(kk), kd + k_step(kk), IDESC_S, static_cast<uint32_t>(kk != 0));
         umma_commit_pair(smem_u32(&s.s_full[g]), 0x3);
     };
     auto issue_pv = [&](int g, uint32_t vslot, bool first) -> bool {
@@ -385,12 +386,19 @@ __device__ void run_mma(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t *sm
         ++np[g];
         if (first && k > 0 && !wait_bar<true>(smem_u32(&s.o_free[g]), (k - 1) & 1u, c, SITE_ACC_EMPTY, k)) return false;
         tc_fence_after();
-        const uint32_t vt = base + OFF_KV + vslot * SLOT;
+        const uint64_t vd = v_desc0(base + OFF_KV + vslot * SLOT);
+        const uint32_t d_tmem = tmem + 256u + static_cast<uint32_t>(g) * 128u;
+        const uint32_t a_tmem = tmem + static_cast<uint32_t>(g) * 128u;
+        if (first) {
+            umma_bf16_pair_ts(d_tmem, a_tmem, vd, IDESC_PV, 0u);
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-            umma_bf16_pair_ts(tmem + 256u + static_cast<uint32_t>(g) * 128u,
-                              tmem + static_cast<uint32_t>(g) * 128u + static_cast<uint32_t>(kk) * 8u, v_desc(vt, kk),
-                              IDESC_PV, static_cast<uint32_t>(!first || kk != 0));
+            for (int kk = 1; kk < BKV / 16; ++kk)
+                umma_bf16_pair_ts(d_tmem, a_tmem + static_cast<uint32_t>(kk) * 8u, vd + v_step(kk), IDESC_PV, 1u);
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk)
+                umma_bf16_pair_ts(d_tmem, a_tmem + static_cast<uint32_t>(kk) * 8u, vd + v_step(kk), IDESC_PV, 1u);
+        }
         return true;
     };
     for (int u = pair; u < p.num_units && ok; u += npairs, ++k) {
