@@ -641,6 +641,7 @@ mk_status run_ring_attention(int P, int64_t H, int64_t S, int64_t d, const void 
     p.hdr = reinterpret_cast<MkWsHeader *>(wsb);
     p.flags = reinterpret_cast<uint32_t *>(wsb + MK_WS_HEADER_BYTES);
     p.timeout_ns = o.wait_timeout_ns ? o.wait_timeout_ns : kDefaultTimeoutNs;
+    p.skip_copy = o.debug_skip_unit;
     const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / sqrt(static_cast<double>(d));
     p.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
     p.P = P;

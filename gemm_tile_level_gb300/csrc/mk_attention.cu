@@ -85,6 +85,8 @@ struct Ctl {
     uint32_t peer_kv_issued, peer_q_issued;    // even CTA: the odd CTA's counts, stored there at exit
 };
 
+static_assert(DATA_BYTES + sizeof(Ctl) + 1024 <= 227 * 1024, "shared memory of one block (227 KiB at most)");
+
 // A unit: head h, rank r, 512 query rows (qp): tile A is rows [0, 256) of it, tile B [256, 512);
 // CTA c of the pair holds rows [128 c, 128 c + 128) of each.
 struct Unit {
@@ -232,6 +234,7 @@ __device__ void run_copies(const MkAttnParams &p, const Ctx &c, Ctl &s, uint8_t 
         if (global_abort(c)) break;
         const int item = claim_copy(p);
         if (item >= p.num_copies) break;
+        if (item == p.skip_copy) continue;   // fault injection: this tile is never forwarded
         copy_tile(p, c, item, stage, bars, seq, epoch);
     }
     bulk_wait_all();
@@ -250,6 +253,7 @@ __device__ void run_copy_warp(const MkAttnParams &p, const Ctx &c, int lane, uin
         stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
         item = __shfl_sync(0xFFFFFFFFu, item, 0);
         if (stop || item >= p.num_copies) break;
+        if (item == p.skip_copy) continue;   // fault injection: this tile is never forwarded
         const CopyItem x = copy_item(p, item);
         if (x.s >= 2) {
             int ok = 1;

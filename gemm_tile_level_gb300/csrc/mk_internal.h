@@ -120,6 +120,7 @@ struct MkAttnParams {
     MkWsHeader *hdr;
     uint32_t *flags;             // [P][P-1][H][nt] readiness of forwarded KV tiles (epoch-valued)
     uint64_t timeout_ns;
+    int64_t skip_copy;           // fault injection: the forwarded KV tile never copied (-1 = off)
     float scale_log2;            // softmax scale * log2(e)
     int32_t P, H, S, nt, nq;     // nt: 128-row KV tiles per slice; nq: 512-row query units per slice
     int32_t num_units, num_copies;

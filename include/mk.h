@@ -280,6 +280,9 @@ mk_status mk_allgather_gemm(int P, int64_t M, int64_t N, int64_t K, const void *
  * which comm_sms blocks (0 = chosen from the shape) forward the KV tiles while the
  * others compute; MK_SPLIT_UNFUSED forwards every step's KV in one kernel and attends
  * in a second.  Other split modes and the GEMM flags are MK_ERR_INVALID_ARG.
+ * opts.debug_skip_unit (fault injection for tests): the forwarded KV tile with this index in
+ * ring order (head, then step, then receiving rank, then 128-row tile) is never forwarded, so the
+ * compute's bounded wait for it runs out (MK_ERR_TIMEOUT from mk_status_check).
  * Arithmetic: scores Q K^T in fp32 from bf16 operands, probabilities as bf16 for P V,
  * fp32 accumulation, an online softmax over the KV tiles in ring order.
  * Workspace: mk_ring_attention_workspace_size(P, H, S, d) bytes, zeroed once (it holds

@@ -200,3 +200,22 @@ def test_full_size_workload_sampled():
             num += float(((got - o) ** 2).sum())
             den += float((o ** 2).sum())
     assert math.sqrt(num / den) <= 3e-3
+
+
+def test_a_withheld_tile_times_out_and_the_next_call_recovers():
+    """Fault injection on the host side: one forwarded KV tile is never copied, so the compute that
+    needs it waits out its (short) limit; the call reports MK_ERR_TIMEOUT through the workspace and
+    exits cleanly, and the next call on the same workspace is correct."""
+    wl = ig.AttnWorkload("t", 4, 2, 256, 128, ig.normal(1.0), ig.normal(1.0), ig.normal(1.0), seed=3)
+    Q, K, V = ig.make_attn_operands(wl)
+    Qd, Kd, Vd = upload(Q, K, V)
+    ws = api.ring_attention_workspace(4, 2, 256, 128)
+    want, _, _ = run(Qd, Kd, Vd, mk.MK_F32)
+    opts = api.make_opts(mk.MK_SPLIT_ADAPTIVE, timeout_ns=50_000_000, skip_unit=5)
+    _, _, _, st = api.ring_attention(Qd, Kd, Vd, mk.MK_F32, ws=ws, opts=opts)
+    mk.check(st)
+    assert mk.mk_status_check(ws) == mk.MK_ERR_TIMEOUT
+    assert mk.mk_status_check(ws) == mk.MK_OK   # read and cleared
+    got, _, _ = run(Qd, Kd, Vd, mk.MK_F32, ws=ws)
+    for r in range(4):
+        assert torch.equal(got[r], want[r])
