@@ -93,6 +93,7 @@ struct MkParams {
     int32_t b_nk;                // B_r given as N x K_r (K-major operand; one TMA box of B rows per stage)
     int32_t chain_owner;         // chained mode, short M: one SM pair computes all P ranks of a tile in
                                  // rank order and keeps the running sum in registers (BN = 128 only)
+    int32_t band_cols;           // rank-major bands cut into slices of this many tile columns (0 = whole width)
 };
 
 // Ring Attention (sequence parallelism): launch parameters of mk_attn_kernel.

@@ -135,6 +135,34 @@ __device__ __forceinline__ void unit_tile(const MkParams &p, int rows, int u, in
     t = b * per_band + (rem - r * bt);
 }
 
+// Compute unit u -> (tile row `row` of `rows`, tile column tn, rank r).  With p.band_cols > 0
+// (chained and accumulate modes, rank-major) each band of raster_group tile rows is further cut
+// into slices of band_cols tile columns, and the P ranks are computed slice by slice: a slice's
+// running sums stay in L2 through its P rank passes while B is read once per band and A once per
+// slice, instead of B once per (shorter) band.  Tiles run column by column inside a slice.
+// Otherwise the order of unit_tile and raster.
+__device__ __forceinline__ void unit_coords(const MkParams &p, int rows, int u, int &row, int &tn, int &r) {
+    if (p.band_cols <= 0 || !p.rank_major) {
+        int t;
+        unit_tile(p, rows, u, t, r);
+        raster(t, rows, p.tiles_n, p.raster_group, row, tn);
+        return;
+    }
+    const int G = p.raster_group, W = p.band_cols;
+    const int per_band = p.P * G * p.tiles_n;
+    const int b = u / per_band;
+    const int rem = u - b * per_band;
+    const int gsize = min(G, rows - b * G);
+    const int per_slice = p.P * gsize * W;
+    const int c = rem / per_slice;
+    const int rem2 = rem - c * per_slice;
+    const int wsize = min(W, p.tiles_n - c * W);
+    r = rem2 / (gsize * wsize);
+    const int l = rem2 - r * (gsize * wsize);
+    row = b * G + l % gsize;
+    tn = c * W + l / gsize;
+}
+
 // One past the largest compute unit index that tile t consumes (its rank P-1 unit).
 __device__ __forceinline__ uint32_t tile_units_end(const MkParams &p, int rows, uint32_t t) {
     if (!p.rank_major) return (t + 1) * static_cast<uint32_t>(p.P);
@@ -1091,9 +1119,8 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
         if (it.x != ITEM_COMPUTE) continue;
         if (ahead_mode) ahead = atomicAdd(&c.hdr->compute_next, 1u);   // consumed at the next claim
         const int u = it.y;
-        int t, r, tm, tn;
-        unit_tile(p, p.tiles_m, u, t, r);
-        raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+        int r, tm, tn;
+        unit_coords(p, p.tiles_m, u, tm, tn, r);
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
         for (int kb = 0; kb < p.num_kb; ++kb) {
             if (!wait_bar<false>(smem_u32(&s.empty[stage]), phase ^ 1u, c, SITE_STAGE_EMPTY, u)) {
@@ -1211,9 +1238,8 @@ __device__ void run1_epilogue(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
         if (it.x == ITEM_END) break;
         if (it.x == ITEM_COMPUTE) {
             const int u = it.y;
-            int t, r, tm, tn;
-            unit_tile(p, p.tiles_m, u, t, r);
-            raster(t, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+            int r, tm, tn;
+            unit_coords(p, p.tiles_m, u, tm, tn, r);
             const int lt = tm * p.tiles_n + tn;
             ok = true;
             if (lane == 0) ok = wait_bar<false>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
@@ -1371,14 +1397,13 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         const bool owner = BN == 128 && p.chain_owner;
         const int nranks = owner ? p.P : 1;
         for (int rr = 0; rr < nranks && !stop; ++rr) {
-            int pt, r, sm, tn;
+            int r, sm, tn;
             if (owner) {
-                pt = u;
                 r = rr;
+                raster(u, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
             } else {
-                unit_tile(p, p.pair_tiles_m, u, pt, r);
+                unit_coords(p, p.pair_tiles_m, u, sm, tn, r);
             }
-            raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
             const int tm = 2 * sm + static_cast<int>(crank);
             const CUtensorMap *amap = &p.tmA[r];
             int ay = tm * MK_BM;
@@ -1615,9 +1640,8 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             if (!owner_tile<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0)) break;
         } else if (it.x == ITEM_COMPUTE) {
             const int u = it.y;
-            int pt, r, sm, tn;
-            unit_tile(p, p.pair_tiles_m, u, pt, r);
-            raster(pt, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+            int r, sm, tn;
+            unit_coords(p, p.pair_tiles_m, u, sm, tn, r);
             const int tm = 2 * sm + static_cast<int>(crank);
             const bool exists = tm < p.tiles_m;
             const int lt = tm * p.tiles_n + tn;
