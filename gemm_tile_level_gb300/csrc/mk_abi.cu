@@ -35,6 +35,13 @@ constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up t
 #define MK_CHAIN_OWNER_MAX_ROWS 256
 #endif
 constexpr int64_t kChainedOwnerMaxRows = MK_CHAIN_OWNER_MAX_ROWS; // chained mode: tile owners up to this M
+// Chained mode on SM pairs: ranks per compute unit.  Two ranks of a tile computed back to back
+// into the two TMEM accumulators fold into the running sum with one L2 read and one L2 write of
+// it, where one rank per unit takes two of each.
+#ifndef MK_CHAIN_RANKS
+#define MK_CHAIN_RANKS 2
+#endif
+constexpr int32_t kChainRanks = MK_CHAIN_RANKS;
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
 constexpr int64_t kAgBandRows = 4;             // AllGather + GEMM: 256-row tile rows per rank-major band
 // Pause between an epilogue's 32-column store chunks: an eighth of one unit's MMA time at about
@@ -372,6 +379,11 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.epi_pace_ns = epilogue_pace_ns(o, Kr);
     p.partial_bf16 = (o.flags & MK_FLAG_BF16_PARTIALS) ? 1 : 0;
     p.chain_owner = chain_owner ? 1 : 0;
+    // two ranks per unit in the chained mode on SM pairs, unless a unit is withheld (the fault
+    // injection counts one-rank units)
+    p.chain_ranks = (o.split_mode == MK_SPLIT_CHAINED && pair && !chain_owner && o.debug_skip_unit < 0) ? kChainRanks : 1;
+    if (p.chain_ranks > 1)
+        p.num_pair_units = static_cast<int32_t>(g.num_pair_tiles * ((P + p.chain_ranks - 1) / p.chain_ranks));
     const int esize = p.partial_bf16 ? 2 : 4;
     p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P,
                                       esize);

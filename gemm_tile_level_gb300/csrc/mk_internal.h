@@ -94,6 +94,7 @@ struct MkParams {
     int32_t chain_owner;         // chained mode, short M: one SM pair computes all P ranks of a tile in
                                  // rank order and keeps the running sum in registers (BN = 128 only)
     int32_t band_cols;           // rank-major bands cut into slices of this many tile columns (0 = whole width)
+    int32_t chain_ranks;         // chained mode on SM pairs: ranks per compute unit (1, or 2 folded per running-sum pass)
 };
 
 // Ring Attention (sequence parallelism): launch parameters of mk_attn_kernel.

@@ -115,6 +115,12 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, i
     tn = local / gsize;
 }
 
+// Rank entries per tile in the unit order: P, or the P ranks taken chain_ranks at a time (chained
+// mode on SM pairs computes ranks 2i and 2i+1 of a tile in one unit, see chain_two).
+__device__ __forceinline__ int rank_groups(const MkParams &p) {
+    return p.chain_ranks > 1 ? (p.P + p.chain_ranks - 1) / p.chain_ranks : p.P;
+}
+
 // Compute unit u -> (tile t in raster order, rank r).  Tile-major order visits the P ranks of a
 // tile back to back.  Rank-major order cuts the tile rows into bands of G rows (G = raster_group)
 // and computes a band for rank 0, then the same band for rank 1, and so on: while one rank's band
@@ -122,22 +128,24 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, i
 // instead of all P ranks' operands competing for L2 at once.  `rows` is tiles_m, or pair_tiles_m
 // for SM-pair tiles.
 __device__ __forceinline__ void unit_tile(const MkParams &p, int rows, int u, int &t, int &r) {
+    const int P = rank_groups(p);
     if (!p.rank_major) {
-        t = u / p.P;
-        r = u - t * p.P;
+        t = u / P;
+        r = u - t * P;
         return;
     }
     const int per_band = p.raster_group * p.tiles_n;
-    const int b = u / (per_band * p.P);
-    const int rem = u - b * per_band * p.P;
+    const int b = u / (per_band * P);
+    const int rem = u - b * per_band * P;
     const int bt = min(p.raster_group, rows - b * p.raster_group) * p.tiles_n;   // tiles in band b
     r = rem / bt;
     t = b * per_band + (rem - r * bt);
 }
 
-// Compute unit u -> (tile row `row` of `rows`, tile column tn, rank r).  With p.band_cols > 0
-// (chained and accumulate modes, rank-major) each band of raster_group tile rows is further cut
-// into slices of band_cols tile columns, and the P ranks are computed slice by slice: a slice's
+// Compute unit u -> (tile row `row` of `rows`, tile column tn, rank entry r: the rank, or the
+// rank group with p.chain_ranks > 1).  With p.band_cols > 0 (chained and accumulate modes,
+// rank-major) each band of raster_group tile rows is further cut into slices of band_cols tile
+// columns, and the P ranks are computed slice by slice: a slice's
 // running sums stay in L2 through its P rank passes while B is read once per band and A once per
 // slice, instead of B once per (shorter) band.  Tiles run column by column inside a slice.
 // Otherwise the order of unit_tile and raster.
@@ -148,12 +156,12 @@ __device__ __forceinline__ void unit_coords(const MkParams &p, int rows, int u, 
         raster(t, rows, p.tiles_n, p.raster_group, row, tn);
         return;
     }
-    const int G = p.raster_group, W = p.band_cols;
-    const int per_band = p.P * G * p.tiles_n;
+    const int G = p.raster_group, W = p.band_cols, P = rank_groups(p);
+    const int per_band = P * G * p.tiles_n;
     const int b = u / per_band;
     const int rem = u - b * per_band;
     const int gsize = min(G, rows - b * G);
-    const int per_slice = p.P * gsize * W;
+    const int per_slice = P * gsize * W;
     const int c = rem / per_slice;
     const int rem2 = rem - c * per_slice;
     const int wsize = min(W, p.tiles_n - c * W);
@@ -161,6 +169,19 @@ __device__ __forceinline__ void unit_coords(const MkParams &p, int rows, int u, 
     const int l = rem2 - r * (gsize * wsize);
     row = b * G + l % gsize;
     tn = c * W + l / gsize;
+}
+
+// SM-pair compute unit u -> (pair tile row sm, tile column tn, ranks r0 .. r0 + nr - 1).
+__device__ __forceinline__ void unit_span(const MkParams &p, int u, int &sm, int &tn, int &r0, int &nr) {
+    int e;
+    unit_coords(p, p.pair_tiles_m, u, sm, tn, e);
+    if (p.chain_ranks > 1) {
+        r0 = e * p.chain_ranks;
+        nr = min(p.chain_ranks, p.P - r0);
+    } else {
+        r0 = e;
+        nr = 1;
+    }
 }
 
 // One past the largest compute unit index that tile t consumes (its rank P-1 unit).
@@ -695,10 +716,9 @@ __device__ void finish_accumulate(const MkParams &p, const Ctx &c, int tm, int t
 // makes, in the same order, so the result is the same bit for bit; no reduce role is needed and
 // a partial tile is read back only as the running sum, which the rank-major bands keep in L2.
 // False if the wait for the predecessor gave up (the grid is aborting).
-template <int BN>
-__device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc, int r, int tm, int tn, int warp,
-                              int lane, int etid, uint32_t epoch) {
-    const int lt = tm * p.tiles_n + tn;
+// Collective over the epilogue group: wait until rank r-1 has released the running sum of tile
+// lt (nothing to wait for at r = 0).  False if the wait gave up (the grid is aborting).
+__device__ bool wait_predecessor(const MkParams &p, const Ctx &c, int lt, int r, int lane, int etid, uint32_t epoch) {
     bool ok = true;
     if (r > 0 && etid < 32) {
         // lane 0 acquires the predecessor's flag (one flag: no need for the whole warp)
@@ -722,8 +742,14 @@ __device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc
         }
         ok = __shfl_sync(0xFFFFFFFFu, stop, 0) == 0;
     }
-    ok = bar_and(1, MK_EPI_THREADS, ok);   // orders every thread's loads of S after the acquire
-    if (!ok) return false;
+    return bar_and(1, MK_EPI_THREADS, ok);   // orders every thread's loads of S after the acquire
+}
+
+template <int BN>
+__device__ bool chain_partial(const MkParams &p, const Ctx &c, uint32_t tmem_acc, int r, int tm, int tn, int warp,
+                              int lane, int etid, uint32_t epoch) {
+    const int lt = tm * p.tiles_n + tn;
+    if (!wait_predecessor(p, c, lt, r, lane, etid, epoch)) return false;
     const int lq = warp & 3;
     const int half = (warp - MK_EPI_WARP0) >> 2;
     const int row = lq * 32 + lane;
@@ -1395,15 +1421,13 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
         // tile owners exist only with 128-column tiles: the 256-column kernel keeps one unit per item
         const bool owner = BN == 128 && p.chain_owner;
-        const int nranks = owner ? p.P : 1;
+        int sm, tn, r0 = 0, nranks = p.P;
+        if (owner)
+            raster(u, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
+        else
+            unit_span(p, u, sm, tn, r0, nranks);
         for (int rr = 0; rr < nranks && !stop; ++rr) {
-            int r, sm, tn;
-            if (owner) {
-                r = rr;
-                raster(u, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
-            } else {
-                unit_coords(p, p.pair_tiles_m, u, sm, tn, r);
-            }
+            const int r = r0 + rr;
             const int tm = 2 * sm + static_cast<int>(crank);
             const CUtensorMap *amap = &p.tmA[r];
             int ay = tm * MK_BM;
@@ -1473,9 +1497,15 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
         }
         if (it.x == ITEM_END) break;
         if (it.x != ITEM_COMPUTE) continue;
-        // one unit, or a tile owner's P units (one per rank, each in its own accumulator; tile
-        // owners exist only with 128-column tiles)
-        const int nranks = (BN == 128 && p.chain_owner) ? p.P : 1;
+        // one unit's ranks (one, or two with chain_ranks = 2), or a tile owner's P ranks, each in
+        // the next accumulator (tile owners exist only with 128-column tiles)
+        int nranks = 1;
+        if (BN == 128 && p.chain_owner) {
+            nranks = p.P;
+        } else if (p.chain_ranks > 1) {
+            int sm, tn, r0;
+            unit_span(p, it.y, sm, tn, r0, nranks);
+        }
         bool ok = true;
         for (int rr = 0; rr < nranks && ok; ++rr) {
             if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) {
@@ -1609,6 +1639,162 @@ __device__ bool owner_tile(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, cons
     }
 }
 
+// Chained mode on SM pairs with two ranks per unit: ranks r0 and r0 + 1 of a tile land in two
+// accumulators one after the other.  While the MMAs of the second run, the epilogue adds the
+// running sum S_{r0-1} (read once from L2, after rank r0-1's flag) to the first accumulator in
+// place.  Once the second is complete it adds the first to it in place and releases the first,
+// so that the next unit's MMAs can start, then stores the second (the new running sum, or the
+// output after rank P-1) and releases it.  The additions are (S_{r0-1} + p_r0) + p_{r0+1}, the
+// reduce role's in its order, so the bits are the same, and the running sum crosses L2 once per
+// two ranks.  A unit with one rank (the last of an odd P) folds like chain_partial.  False if a
+// wait gave up (the grid is aborting).
+template <int BN>
+__device__ bool chain_two(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base, int u,
+                          uint32_t crank, int warp, int lane, int etid, int &acc, uint32_t &aphase, uint32_t tempty0,
+                          uint32_t epoch) {
+    int sm, tn, r0, nr;
+    unit_span(p, u, sm, tn, r0, nr);
+    const int tm = 2 * sm + static_cast<int>(crank);
+    const bool exists = tm < p.tiles_m;
+    const int lt = tm * p.tiles_n + tn;
+    const bool last = r0 + nr == p.P;
+    const bool kz = p.num_kb == 0;   // K_r = 0: the MMAs never wrote the accumulators, every p_r is 0
+    const int lq = warp & 3;
+    const int half = (warp - MK_EPI_WARP0) >> 2;
+    const int row = lq * 32 + lane;
+    const int grow = tm * MK_BM + row;
+    const uint32_t lanes = static_cast<uint32_t>(lq * 32) << 16;
+    auto wait_acc = [&]() -> bool {   // the accumulator `acc` is complete
+        bool ok = true;
+        if (lane == 0) ok = wait_bar<false>(smem_u32(&s.tfull[acc]), aphase, c, SITE_ACC_FULL, u);
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!bar_and(1, MK_EPI_THREADS, ok)) return false;
+        tc_fence_after();
+        return true;
+    };
+    auto release_acc = [&]() {   // hand `acc` back to the MMA warp and move to the next one
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (crank == 0) mbar_arrive(smem_u32(&s.tempty[acc]));
+            else mbar_arrive_remote(tempty0 + 8u * acc);
+        }
+        if (++acc == ACC) {
+            acc = 0;
+            aphase ^= 1u;
+        }
+    };
+    auto acc_ld = [&](uint32_t taddr, bool zero, uint32_t (&v)[16]) {
+        if (zero) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = 0u;
+        } else {
+            tmem_ld16(taddr, v);
+        }
+    };
+    if (!wait_acc()) return false;
+    bool folded = true;
+    if (nr == 1) {
+        if (exists)
+            folded = chain_partial<BN>(p, c, tmem_base + static_cast<uint32_t>(acc * BN), r0, tm, tn, warp, lane, etid,
+                                       epoch);
+        release_acc();
+    } else {
+        float *S = partial_tile<BN>(p, 0, lt);
+        const uint32_t ta = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
+        // S_{r0-1} + p_r0 into the first accumulator (at r0 = 0, p_0 starts the sum as it is)
+        if (exists && r0 > 0) {
+            folded = wait_predecessor(p, c, lt, r0, lane, etid, epoch);
+            if (folded) {
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {   // 16 of the thread's BN/2 columns at a time
+                    const int col0 = half * (BN / 2) + cc * 16;
+                    const float *base = S + (static_cast<size_t>(col0 >> 3) * MK_BM + row) * 8;
+                    float sv[2][8];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) ld_cg_f8(base + q * MK_BM * 8, sv[q]);
+                    uint32_t v[16];
+                    acc_ld(ta + static_cast<uint32_t>(col0), kz, v);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)   // fp32 addition commutes bit for bit
+                            v[8 * q + j] = __float_as_uint(sv[q][j] + __uint_as_float(v[8 * q + j]));
+                    tmem_st16(ta + static_cast<uint32_t>(col0), v);
+                }
+            }
+        }
+        const int first = acc;
+        if (++acc == ACC) {
+            acc = 0;
+            aphase ^= 1u;
+        }
+        if (!wait_acc()) return false;
+        const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
+        // (S_{r0-1} + p_r0) + p_{r0+1} into the second accumulator; then the first is free
+        if (exists && folded) {
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int col0 = half * (BN / 2) + cc * 16;
+                uint32_t va[16], vb[16];
+                acc_ld(ta + static_cast<uint32_t>(col0), kz && r0 == 0, va);
+                acc_ld(tb + static_cast<uint32_t>(col0), kz, vb);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) vb[q] = __float_as_uint(__uint_as_float(va[q]) + __uint_as_float(vb[q]));
+                tmem_st16(tb + static_cast<uint32_t>(col0), vb);
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (crank == 0) mbar_arrive(smem_u32(&s.tempty[first]));
+            else mbar_arrive_remote(tempty0 + 8u * first);
+        }
+        // the second accumulator out: the next running sum, or the output
+        if (exists && folded) {
+            const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 64; ++cc) {
+                const int col0 = half * (BN / 2) + cc * 32;
+                uint32_t v[32];
+                tmem_ld32(tb + static_cast<uint32_t>(col0), v);
+                if (last) {
+                    if (grow < p.M) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int gcol = tn * BN + col0 + 8 * q;
+                            if (gcol < p.N)
+                                store_out8(p, grow, gcol,
+                                           make_float4(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1]),
+                                                       __uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                           make_float4(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]),
+                                                       __uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                        }
+                    }
+                } else {
+                    float *base = S + (static_cast<size_t>(col0 >> 3) * MK_BM + row) * 8;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float x[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(v[8 * q + j]);
+                        st_f8_hint(base + q * MK_BM * 8, x, pol);
+                    }
+                }
+                epilogue_pace(p);
+            }
+        }
+        release_acc();
+    }
+    bar_sync(1, MK_EPI_THREADS);   // every store of the running sum (or of the output) has been issued
+    if (etid == 0 && folded) {
+        if (exists) st_release_gpu(p.flags + static_cast<size_t>(lt) * p.P + (r0 + nr - 1), epoch);
+        atomicAdd(&c.hdr->units_done, 1u);
+        if (exists && last) atomicAdd(&c.hdr->tiles_done, 1u);
+    }
+    return true;
+}
+
 template <int BN>
 __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_t *stages, const Ctx &c,
                               uint32_t tmem_base, uint32_t epoch, uint32_t crank) {
@@ -1638,6 +1824,8 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (it.x == ITEM_END) break;
         if (BN == 128 && it.x == ITEM_COMPUTE && p.chain_owner) {
             if (!owner_tile<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0)) break;
+        } else if (it.x == ITEM_COMPUTE && p.chain_ranks > 1) {
+            if (!chain_two<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0, epoch)) break;
         } else if (it.x == ITEM_COMPUTE) {
             const int u = it.y;
             int r, sm, tn;

@@ -2,7 +2,9 @@
 into the running sum of ranks 0..r-1 after rank r-1's release, and rank P-1 writes the output.
 On a short M (M <= 256, the default tile kind and order) one SM pair instead owns each tile,
 computes its P ranks in turn and keeps the running sum in TMEM; a tile-kind or unit-order flag
-selects the rank-ordered chain there too, so both paths are run below.
+selects the rank-ordered chain there too, so both paths are run below.  On SM pairs above one
+band a compute unit covers two ranks of a tile (their sum crosses L2 once); odd P, P = 1 and
+P = 2 exercise its one-rank and first-pair cases.
 
 These are the reduce role's fp32 additions in the reduce role's order, so on random inputs the
 result must equal the adaptive, static and unfused results bit for bit, besides matching the
@@ -38,6 +40,9 @@ SHAPES = [
     (16, 64, 256, 64),
     (7, 384, 768, 136),
     (8, 1100, 1032, 200),
+    (5, 1100, 520, 72),    # SM pairs, odd P: the last unit folds one rank
+    (1, 640, 264, 64),     # SM pairs, one rank: straight to the output
+    (2, 768, 136, 40),     # SM pairs, P = 2: one two-rank unit per tile, ragged N
 ]
 
 
