@@ -27,7 +27,7 @@ def workspace(op: int, P: int, M: int, N: int, K_per_rank: int, device="cuda") -
 
 
 def make_opts(split_mode=mk.MK_SPLIT_ADAPTIVE, comm_sms=0, timeout_ns=0, trace=None, num_ctas=0,
-              flags=0, skip_unit=-1, raster_group=0, reduce_split=0) -> mk.mk_opts:
+              flags=0, skip_unit=-1, raster_group=0, reduce_split=0, chain_ranks=0) -> mk.mk_opts:
     o = mk.mk_opts_default()
     o.split_mode = split_mode
     o.comm_sms = comm_sms
@@ -41,6 +41,7 @@ def make_opts(split_mode=mk.MK_SPLIT_ADAPTIVE, comm_sms=0, timeout_ns=0, trace=N
     o.debug_skip_unit = skip_unit
     o.raster_group = raster_group
     o.reduce_split = reduce_split
+    o.chain_ranks = chain_ranks
     return o
 
 

@@ -35,13 +35,6 @@ constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up t
 #define MK_CHAIN_OWNER_MAX_ROWS 256
 #endif
 constexpr int64_t kChainedOwnerMaxRows = MK_CHAIN_OWNER_MAX_ROWS; // chained mode: tile owners up to this M
-// Chained mode on SM pairs: ranks per compute unit.  Two ranks of a tile computed back to back
-// into the two TMEM accumulators fold into the running sum with one L2 read and one L2 write of
-// it, where one rank per unit takes two of each.
-#ifndef MK_CHAIN_RANKS
-#define MK_CHAIN_RANKS 2
-#endif
-constexpr int32_t kChainRanks = MK_CHAIN_RANKS;
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
 constexpr int64_t kAgBandRows = 4;             // AllGather + GEMM: 256-row tile rows per rank-major band
 // Pause between an epilogue's 32-column store chunks: an eighth of one unit's MMA time at about
@@ -214,6 +207,8 @@ mk_status check_opts(const mk_opts *o) {
     if (o->raster_group < 0) return fail(MK_ERR_INVALID_ARG, "raster_group < 0");
     if (o->reduce_split < 0 || o->reduce_split > 64)
         return fail(MK_ERR_INVALID_ARG, "reduce_split %d outside [0, 64]", o->reduce_split);
+    if (o->chain_ranks < 0 || o->chain_ranks > MK_MAX_P)
+        return fail(MK_ERR_INVALID_ARG, "chain_ranks %d outside [0, %d]", o->chain_ranks, MK_MAX_P);
     if (o->trace_bytes && !o->trace) return fail(MK_ERR_INVALID_ARG, "trace_bytes without trace buffer");
     if (o->trace && !aligned16(o->trace)) return fail(MK_ERR_ALIGNMENT, "trace buffer not 16-byte aligned");
     if ((o->flags & MK_FLAG_BF16_PARTIALS) &&
@@ -379,9 +374,16 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     p.epi_pace_ns = epilogue_pace_ns(o, Kr);
     p.partial_bf16 = (o.flags & MK_FLAG_BF16_PARTIALS) ? 1 : 0;
     p.chain_owner = chain_owner ? 1 : 0;
-    // two ranks per unit in the chained mode on SM pairs, unless a unit is withheld (the fault
-    // injection counts one-rank units)
-    p.chain_ranks = (o.split_mode == MK_SPLIT_CHAINED && pair && !chain_owner && o.debug_skip_unit < 0) ? kChainRanks : 1;
+    // Chained mode on SM pairs: consecutive ranks of a tile in one unit, computed back to back
+    // into the two TMEM accumulators in turn, fold into the running sum there; it crosses L2
+    // once per unit, and with all P ranks in one unit (the default) never.  Measured at P = 8
+    // (ms per call, 2 / 4 / 8 ranks per unit): 16384 x 8192, K_r = 1024: 1.536 / 1.497 / 1.411;
+    // 8192 x 8192, K_r = 1024: 0.791 / 0.766 / 0.752; 2048 x 4096, K_r = 512: 0.092 / 0.090 / 0.084;
+    // 8192 x 8192, K_r = 3584: 2.241 / 2.218 / 2.231; 1024 x 8192, K_r = 1024: 0.120 / 0.124 / 0.122.
+    // A withheld unit (the fault injection counts one-rank units) keeps one rank per unit.
+    p.chain_ranks = (o.split_mode == MK_SPLIT_CHAINED && pair && !chain_owner && o.debug_skip_unit < 0)
+                        ? (o.chain_ranks > 0 && o.chain_ranks < P ? o.chain_ranks : P)
+                        : 1;
     if (p.chain_ranks > 1)
         p.num_pair_units = static_cast<int32_t>(g.num_pair_tiles * ((P + p.chain_ranks - 1) / p.chain_ranks));
     const int esize = p.partial_bf16 ? 2 : 4;
@@ -757,6 +759,7 @@ void mk_opts_default(mk_opts *o) {
     o->debug_skip_unit = -1;
     o->raster_group = 0;
     o->reduce_split = 0;
+    o->chain_ranks = 0;
 }
 
 size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank) {

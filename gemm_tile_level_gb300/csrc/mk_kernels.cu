@@ -116,7 +116,7 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int G, i
 }
 
 // Rank entries per tile in the unit order: P, or the P ranks taken chain_ranks at a time (chained
-// mode on SM pairs computes ranks 2i and 2i+1 of a tile in one unit, see chain_two).
+// mode on SM pairs computes several consecutive ranks of a tile in one unit, see chain_span).
 __device__ __forceinline__ int rank_groups(const MkParams &p) {
     return p.chain_ranks > 1 ? (p.P + p.chain_ranks - 1) / p.chain_ranks : p.P;
 }
@@ -1639,19 +1639,19 @@ __device__ bool owner_tile(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, cons
     }
 }
 
-// Chained mode on SM pairs with two ranks per unit: ranks r0 and r0 + 1 of a tile land in two
-// accumulators one after the other.  While the MMAs of the second run, the epilogue adds the
+// Chained mode on SM pairs with several ranks per unit: ranks r0 .. r0 + nr - 1 of a tile land in
+// the two TMEM accumulators in turn.  While the second rank's MMAs run, the epilogue adds the
 // running sum S_{r0-1} (read once from L2, after rank r0-1's flag) to the first accumulator in
-// place.  Once the second is complete it adds the first to it in place and releases the first,
-// so that the next unit's MMAs can start, then stores the second (the new running sum, or the
-// output after rank P-1) and releases it.  The additions are (S_{r0-1} + p_r0) + p_{r0+1}, the
-// reduce role's in its order, so the bits are the same, and the running sum crosses L2 once per
-// two ranks.  A unit with one rank (the last of an odd P) folds like chain_partial.  False if a
-// wait gave up (the grid is aborting).
+// place.  Each later accumulator, once complete, gets the sum so far added to it in place, and the
+// accumulator that held the sum goes back to the MMA warp for the next rank.  The last sum is
+// stored (the running sum for rank r0 + nr, or the output after rank P-1).  The additions are
+// ((S_{r0-1} + p_r0) + p_{r0+1}) + ..., the reduce role's in its order, so the bits are the same,
+// and the running sum crosses L2 once per nr ranks.  A unit with one rank folds like
+// chain_partial.  False if a wait gave up (the grid is aborting).
 template <int BN>
-__device__ bool chain_two(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base, int u,
-                          uint32_t crank, int warp, int lane, int etid, int &acc, uint32_t &aphase, uint32_t tempty0,
-                          uint32_t epoch) {
+__device__ bool chain_span(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const Ctx &c, uint32_t tmem_base, int u,
+                           uint32_t crank, int warp, int lane, int etid, int &acc, uint32_t &aphase, uint32_t tempty0,
+                           uint32_t epoch) {
     int sm, tn, r0, nr;
     unit_span(p, u, sm, tn, r0, nr);
     const int tm = 2 * sm + static_cast<int>(crank);
@@ -1672,13 +1672,15 @@ __device__ bool chain_two(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const
         tc_fence_after();
         return true;
     };
-    auto release_acc = [&]() {   // hand `acc` back to the MMA warp and move to the next one
+    auto release = [&](int a) {   // hand accumulator `a` back to the MMA warp
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-            if (crank == 0) mbar_arrive(smem_u32(&s.tempty[acc]));
-            else mbar_arrive_remote(tempty0 + 8u * acc);
+            if (crank == 0) mbar_arrive(smem_u32(&s.tempty[a]));
+            else mbar_arrive_remote(tempty0 + 8u * a);
         }
+    };
+    auto next_acc = [&]() {
         if (++acc == ACC) {
             acc = 0;
             aphase ^= 1u;
@@ -1698,14 +1700,15 @@ __device__ bool chain_two(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const
         if (exists)
             folded = chain_partial<BN>(p, c, tmem_base + static_cast<uint32_t>(acc * BN), r0, tm, tn, warp, lane, etid,
                                        epoch);
-        release_acc();
+        release(acc);
+        next_acc();
     } else {
         float *S = partial_tile<BN>(p, 0, lt);
-        const uint32_t ta = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
         // S_{r0-1} + p_r0 into the first accumulator (at r0 = 0, p_0 starts the sum as it is)
         if (exists && r0 > 0) {
             folded = wait_predecessor(p, c, lt, r0, lane, etid, epoch);
             if (folded) {
+                const uint32_t ta = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
 #pragma unroll 1
                 for (int cc = 0; cc < BN / 32; ++cc) {   // 16 of the thread's BN/2 columns at a time
                     const int col0 = half * (BN / 2) + cc * 16;
@@ -1724,34 +1727,33 @@ __device__ bool chain_two(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const
                 }
             }
         }
-        const int first = acc;
-        if (++acc == ACC) {
-            acc = 0;
-            aphase ^= 1u;
-        }
-        if (!wait_acc()) return false;
-        const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
-        // (S_{r0-1} + p_r0) + p_{r0+1} into the second accumulator; then the first is free
-        if (exists && folded) {
+        // the sum so far, in accumulator `acc`, into each later rank's accumulator
+        bool sum_zero = kz && r0 == 0;   // the sum so far is known to be +0 without a TMEM read
+        for (int i = 1; i < nr; ++i) {
+            const int prev = acc;
+            next_acc();
+            if (!wait_acc()) return false;
+            if (exists && folded) {
+                const uint32_t ta = tmem_base + static_cast<uint32_t>(prev * BN) + lanes;
+                const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                const int col0 = half * (BN / 2) + cc * 16;
-                uint32_t va[16], vb[16];
-                acc_ld(ta + static_cast<uint32_t>(col0), kz && r0 == 0, va);
-                acc_ld(tb + static_cast<uint32_t>(col0), kz, vb);
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    const int col0 = half * (BN / 2) + cc * 16;
+                    uint32_t va[16], vb[16];
+                    acc_ld(ta + static_cast<uint32_t>(col0), sum_zero, va);
+                    acc_ld(tb + static_cast<uint32_t>(col0), kz, vb);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) vb[q] = __float_as_uint(__uint_as_float(va[q]) + __uint_as_float(vb[q]));
-                tmem_st16(tb + static_cast<uint32_t>(col0), vb);
+                    for (int q = 0; q < 16; ++q)
+                        vb[q] = __float_as_uint(__uint_as_float(va[q]) + __uint_as_float(vb[q]));
+                    tmem_st16(tb + static_cast<uint32_t>(col0), vb);
+                }
             }
+            sum_zero = false;
+            release(prev);   // the next rank's MMAs may start in it
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            if (crank == 0) mbar_arrive(smem_u32(&s.tempty[first]));
-            else mbar_arrive_remote(tempty0 + 8u * first);
-        }
-        // the second accumulator out: the next running sum, or the output
+        // the last accumulator out: the next running sum, or the output
         if (exists && folded) {
+            const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
             const uint64_t pol = p.l2_hints ? policy_evict_last() : policy_evict_normal();
 #pragma unroll 1
             for (int cc = 0; cc < BN / 64; ++cc) {
@@ -1784,7 +1786,8 @@ __device__ bool chain_two(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, const
                 epilogue_pace(p);
             }
         }
-        release_acc();
+        release(acc);
+        next_acc();
     }
     bar_sync(1, MK_EPI_THREADS);   // every store of the running sum (or of the output) has been issued
     if (etid == 0 && folded) {
@@ -1825,7 +1828,7 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (BN == 128 && it.x == ITEM_COMPUTE && p.chain_owner) {
             if (!owner_tile<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0)) break;
         } else if (it.x == ITEM_COMPUTE && p.chain_ranks > 1) {
-            if (!chain_two<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0, epoch)) break;
+            if (!chain_span<BN>(p, s, c, tmem_base, it.y, crank, warp, lane, etid, acc, aphase, tempty0, epoch)) break;
         } else if (it.x == ITEM_COMPUTE) {
             const int u = it.y;
             int r, sm, tn;

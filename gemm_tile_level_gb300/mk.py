@@ -59,7 +59,8 @@ class mk_opts(ctypes.Structure):
                 ("wait_timeout_ns", ctypes.c_uint64), ("trace", ctypes.c_void_p),
                 ("trace_bytes", ctypes.c_uint64), ("num_ctas", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("debug_skip_unit", ctypes.c_int64),
-                ("raster_group", ctypes.c_int32), ("reduce_split", ctypes.c_int32)]
+                ("raster_group", ctypes.c_int32), ("reduce_split", ctypes.c_int32),
+                ("chain_ranks", ctypes.c_int32)]
 
 
 class mk_trace_record(ctypes.Structure):

@@ -79,12 +79,14 @@ typedef enum {
                                r-1's release, adds its partial tile to the running sum of ranks
                                0..r-1 and stores it (rank P-1 writes the output).  The same fp32
                                additions in the same order as the reduce role, so the same bits
-                               (AllReduce and ReduceScatter only).  For M <= 256 one SM pair
-                               instead computes all P ranks of a 256 x 128 tile in rank order
-                               and keeps the running sum in tensor memory (the same additions);
-                               for 256 < M <= 512 it uses one-SM tiles.  A tile-kind or
-                               unit-order flag, or debug_skip_unit, selects the rank-ordered
-                               chain at any M. */
+                               (AllReduce and ReduceScatter only).  On SM-pair tiles a compute
+                               unit covers chain_ranks consecutive ranks of a tile (all P by
+                               default), computed back to back with the running sum kept in
+                               tensor memory between them.  For M <= 256 one SM pair computes
+                               all P ranks of a 256 x 128 tile and keeps the running sum in
+                               tensor memory (the same additions); for 256 < M <= 512 it uses
+                               one-SM tiles.  A tile-kind or unit-order flag, or
+                               debug_skip_unit, selects the one-rank chain at any M. */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */
@@ -163,6 +165,14 @@ typedef enum {
  *                     tiles with P <= 8) are clamped to it.  Every element is
  *                     still summed over ranks 0..P-1 in order, so results do
  *                     not depend on it.  Ignored by AllGather + GEMM.
+ *   chain_ranks     : MK_SPLIT_CHAINED on SM-pair tiles above M = 256: ranks of a
+ *                     tile per compute unit.  The unit computes them back to back
+ *                     into the two tensor-memory accumulators in turn, adds the
+ *                     running sum read from the workspace to the first, each
+ *                     accumulator to the next in place, and stores the sum once;
+ *                     0 (or >= P) = all P ranks, so that the running sum never
+ *                     leaves tensor memory.  Results do not depend on it.  Ignored
+ *                     otherwise; 0 <= chain_ranks <= 16.
  */
 typedef struct {
     int32_t split_mode;
@@ -175,6 +185,7 @@ typedef struct {
     int64_t debug_skip_unit;
     int32_t raster_group;
     int32_t reduce_split;
+    int32_t chain_ranks;
 } mk_opts;
 
 /* One controller record written to mk_opts.trace (32 bytes). */

@@ -44,10 +44,11 @@ def test_struct_layout_matches_header(mk, tmp_path):
 #include <stddef.h>
 #include "mk.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(mk_opts), offsetof(mk_opts, comm_sms),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(mk_opts), offsetof(mk_opts, comm_sms),
          offsetof(mk_opts, wait_timeout_ns), offsetof(mk_opts, trace), offsetof(mk_opts, trace_bytes),
          offsetof(mk_opts, num_ctas), offsetof(mk_opts, flags), offsetof(mk_opts, debug_skip_unit),
-         sizeof(mk_trace_record), offsetof(mk_opts, raster_group), offsetof(mk_opts, reduce_split));
+         sizeof(mk_trace_record), offsetof(mk_opts, raster_group), offsetof(mk_opts, reduce_split),
+         offsetof(mk_opts, chain_ranks));
   return 0;
 }
 """)
@@ -57,7 +58,8 @@ int main(void) {
     o = mk.mk_opts
     want = [ctypes.sizeof(o), o.comm_sms.offset, o.wait_timeout_ns.offset, o.trace.offset,
             o.trace_bytes.offset, o.num_ctas.offset, o.flags.offset, o.debug_skip_unit.offset,
-            ctypes.sizeof(mk.mk_trace_record), o.raster_group.offset, o.reduce_split.offset]
+            ctypes.sizeof(mk.mk_trace_record), o.raster_group.offset, o.reduce_split.offset,
+            o.chain_ranks.offset]
     assert got == want
 
 
@@ -138,6 +140,10 @@ def test_argument_checks_return_before_any_launch(mk):
         o = mk.mk_opts_default()
         o.reduce_split = bad
         assert call_ar(mk, opts=o) == mk.MK_ERR_INVALID_ARG and "reduce_split" in mk.mk_last_error()
+    for bad in (-1, 17):
+        o = mk.mk_opts_default()
+        o.chain_ranks = bad
+        assert call_ar(mk, opts=o) == mk.MK_ERR_INVALID_ARG and "chain_ranks" in mk.mk_last_error()
     assert call_ar(mk, N=100) == mk.MK_ERR_UNSUPPORTED_SHAPE and "multiples of 8" in mk.mk_last_error()
     # bf16 partial tiles need a split that stores partial tiles
     for mode in (mk.MK_SPLIT_ACCUMULATE, mk.MK_SPLIT_CHAINED):

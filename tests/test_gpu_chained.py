@@ -3,8 +3,9 @@ into the running sum of ranks 0..r-1 after rank r-1's release, and rank P-1 writ
 On a short M (M <= 256, the default tile kind and order) one SM pair instead owns each tile,
 computes its P ranks in turn and keeps the running sum in TMEM; a tile-kind or unit-order flag
 selects the rank-ordered chain there too, so both paths are run below.  On SM pairs above one
-band a compute unit covers two ranks of a tile (their sum crosses L2 once); odd P, P = 1 and
-P = 2 exercise its one-rank and first-pair cases.
+band a compute unit covers chain_ranks consecutive ranks of a tile (all P by default) whose sum
+crosses the workspace once per unit; 1, 2 and 3 ranks per unit with odd P, P = 1 and P = 2 run
+its one-rank, first-unit and later-unit cases.
 
 These are the reduce role's fp32 additions in the reduce role's order, so on random inputs the
 result must equal the adaptive, static and unfused results bit for bit, besides matching the
@@ -58,6 +59,12 @@ def test_integer_bit_exact(P, M, N, Kr, out):
         for fl, band in ((0, 0), (mk.MK_FLAG_TILE_MAJOR, 0), (mk.MK_FLAG_RANK_MAJOR, 0), (0, 1)):
             C = gu.call_ar(Ad, Bd, code, opts=ch_opts(tiles, flags=fl, raster_group=band))
             gu.assert_bit_exact(gu.host_values(C), ref)
+    # SM pairs above one band: 1, 2 and 3 ranks per unit besides the default (all P): the running
+    # sum crosses the workspace between units, a unit may hold a single rank
+    for cr in (1, 2, 3):
+        for fl in (0, mk.MK_FLAG_TILE_MAJOR):
+            C = gu.call_ar(Ad, Bd, code, opts=ch_opts(flags=fl, chain_ranks=cr))
+            gu.assert_bit_exact(gu.host_values(C), ref)
 
 
 @pytest.mark.parametrize("P,M,N,Kr", SHAPES)
@@ -72,6 +79,8 @@ def test_random_same_bits_as_the_reduce_role(P, M, N, Kr):
             got = gu.call_ar(Ad, Bd, mk.MK_F32, opts=ch_opts(tiles, flags=order))
             gu.check_tolerance(gu.host_values(got), ref, out_bf16=False)
             assert torch.equal(got, want)
+    for cr in (1, 2, 3):
+        assert torch.equal(gu.call_ar(Ad, Bd, mk.MK_F32, opts=ch_opts(chain_ranks=cr)), want)
 
 
 @pytest.mark.parametrize("P,M,N", [(3, 200, 136), (8, 256, 8192), (2, 1024, 512)])
