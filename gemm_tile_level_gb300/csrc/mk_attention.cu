@@ -530,10 +530,9 @@ __device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint32_
     for (int u = pair; u < p.num_units; u += npairs, ++k) {
         const Unit x = unit_of(p, u);
         float m = -INFINITY, l = 0.0f;
-        for (int j = 0; j < n; ++j, ++gt) {
+        for (int j = 0, t = 0; j < n; ++j, ++gt, t = (t + 1 == p.nt) ? 0 : t + 1) {   // t = j mod nt
             if (!wait_bar<false>(smem_u32(&s.s_full[g]), gt & 1u, c, SITE_ACC_FULL, gt)) return;
             tc_fence_after();
-            const int t = j % p.nt;
             const int valid = min(BKV, p.S - t * BKV);
             float alpha = 1.0f;
             if (j == 0) {
@@ -581,8 +580,9 @@ __device__ void run_softmax(const MkAttnParams &p, const Ctx &c, Ctl &s, uint32_
                 }
             }
             l = l * alpha + rowsum;
-            tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(t_s + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tmem_st32_nowait(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32_nowait(t_s + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_even(smem_u32(&s.p_full[g]), p_full0);

@@ -1727,28 +1727,31 @@ __device__ bool chain_span(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, cons
                 }
             }
         }
-        // the sum so far, in accumulator `acc`, into each later rank's accumulator
-        bool sum_zero = kz && r0 == 0;   // the sum so far is known to be +0 without a TMEM read
+        // the sum so far, in accumulator `acc`, into each later rank's accumulator (with K_r = 0
+        // every p_r and so every sum is +0, and the accumulators hold nothing to read)
         for (int i = 1; i < nr; ++i) {
             const int prev = acc;
             next_acc();
             if (!wait_acc()) return false;
-            if (exists && folded) {
+            if (exists && folded && !kz) {
+                // the MMAs of the next rank wait for `prev`: the loads of both accumulators go
+                // out together and the stores are waited for once, at the end
                 const uint32_t ta = tmem_base + static_cast<uint32_t>(prev * BN) + lanes;
                 const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    const int col0 = half * (BN / 2) + cc * 16;
+                for (int cc = 0; cc < BN / 32; ++cc) {   // 16 of the thread's BN/2 columns at a time
+                    const uint32_t col0 = static_cast<uint32_t>(half * (BN / 2) + cc * 16);
                     uint32_t va[16], vb[16];
-                    acc_ld(ta + static_cast<uint32_t>(col0), sum_zero, va);
-                    acc_ld(tb + static_cast<uint32_t>(col0), kz, vb);
+                    tmem_ld16_nowait(ta + col0, va);
+                    tmem_ld16_nowait(tb + col0, vb);
+                    tmem_wait_ld16(va);
+                    tmem_wait_ld16(vb);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        vb[q] = __float_as_uint(__uint_as_float(va[q]) + __uint_as_float(vb[q]));
-                    tmem_st16(tb + static_cast<uint32_t>(col0), vb);
+                    for (int q = 0; q < 16; ++q) vb[q] = __float_as_uint(__uint_as_float(va[q]) + __uint_as_float(vb[q]));
+                    tmem_st16_nowait(tb + col0, vb);
                 }
+                tmem_wait_st();
             }
-            sum_zero = false;
             release(prev);   // the next rank's MMAs may start in it
         }
         // the last accumulator out: the next running sum, or the output
@@ -1759,7 +1762,12 @@ __device__ bool chain_span(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, cons
             for (int cc = 0; cc < BN / 64; ++cc) {
                 const int col0 = half * (BN / 2) + cc * 32;
                 uint32_t v[32];
-                tmem_ld32(tb + static_cast<uint32_t>(col0), v);
+                if (kz) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = 0u;
+                } else {
+                    tmem_ld32(tb + static_cast<uint32_t>(col0), v);
+                }
                 if (last) {
                     if (grow < p.M) {
 #pragma unroll
