@@ -522,7 +522,12 @@ def configs_leg(torch, api, mk, stream, peaks, steps: int, warmup: int):
             rec["bound"] = rf["bound"]
             rec["roofline_ms"] = rf["roofline_ms"]
             rec[split] = {"ms": ms, "us": ms * 1e3, "tflops": wl.flops / (ms * 1e-3) / 1e12,
-                          "roofline_frac": rf["frac"]}
+                          "roofline_frac": rf["frac"],
+                          "tensor_frac": wl.flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+        rec["roofline_note"] = ("roofline_ms = max(FLOPs / bf16 peak, algorithmic bytes / HBM peak), the "
+                                "algorithmic bytes counting every partial tile written and read once; the "
+                                "chained and accumulate splits move no partial tiles and may run below it "
+                                "(roofline_frac > 1); tensor_frac = FLOPs / bf16 peak / time")
         rec["chained_over_unfused"] = rec["chained"]["ms"] / rec["unfused"]["ms"]
         rec["adaptive_over_unfused"] = rec["adaptive"]["ms"] / rec["unfused"]["ms"]
         out[name] = rec

@@ -177,6 +177,34 @@ def test_one_dominant_key_returns_its_value_row_bit_exact():
     assert checked > 50
 
 
+def test_growing_scores_raise_the_maximum_inside_tiles():
+    """Scores that rise by more than 2^8 every 16 keys: every chunk of every tile raises a row's
+    running maximum, so the probabilities already formed (stored in TMEM or still in registers)
+    and their sum are rescaled; within tolerance of the oracle, and the in-place form agrees."""
+    P, H, S, d = 2, 2, 256, 128
+    rng = np.random.default_rng(11)
+    Q = [np.zeros((H, S, d)) for _ in range(P)]
+    K = [np.zeros((H, S, d)) for _ in range(P)]
+    V = [rng.standard_normal((H, S, d)) for _ in range(P)]
+    for r in range(P):
+        Q[r][:, :, 0] = 4.0
+        Q[r][:, :, 1] = rng.uniform(-1, 1, (H, S))
+        # s * scale * log2(e) rises by about 0.7 per key: more than 8 per 16-key chunk
+        K[r][:, :, 0] = np.arange(r * S, (r + 1) * S) * 1.4
+        K[r][:, :, 1] = rng.uniform(-1, 1, (H, S))
+    Qb = [oracle.round_bf16(x) for x in Q]
+    Kb = [oracle.round_bf16(x) for x in K]
+    Vb = [oracle.round_bf16(x) for x in V]
+    Qd, Kd, Vd = upload(Qb, Kb, Vb)
+    ref = oracle.ring_attention(Qb, Kb, Vb)
+    for split in ("fused", "unfused"):
+        O32, L32, _ = run(Qd, Kd, Vd, mk.MK_F32, split=split)
+        check_against_oracle(O32, L32, ref, out_bf16=False)
+    Oi, Li, _ = run(Qd, Kd, Vd, mk.MK_F32, ring=False)
+    for r in range(P):
+        assert torch.equal(Oi[r], O32[r]) and torch.equal(Li[r], L32[r])
+
+
 def test_full_size_workload_sampled():
     """The bench workload (8 ranks x 4096 tokens, 32 heads of 128): sampled query rows of every
     rank against the oracle, and the in-place and forwarded forms bit for bit."""
