@@ -50,7 +50,7 @@ struct MkWsHeader {
     uint32_t units_done;    // compute units whose partial tile is released
     uint32_t tiles_done;    // output tiles reduced and written
     uint32_t trace_count;   // controller records written
-    uint64_t compute_busy;  // SM cycles spent issuing compute units (sum over blocks)
+    uint64_t reserved0;     // (unused; keeps the fields below in place)
     uint64_t reduce_busy;   // SM cycles spent reducing ready tiles (sum over blocks)
     uint32_t err_site;      // which wait gave up (diagnostic)
     uint32_t err_index;     // the unit / tile it was waiting for (diagnostic)

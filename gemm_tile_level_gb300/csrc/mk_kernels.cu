@@ -902,7 +902,6 @@ __device__ void finish_call(const MkParams &p, uint32_t epoch) {
         h->units_done = 0;
         h->tiles_done = 0;
         h->target_nr = 0;
-        h->compute_busy = 0;
         h->reduce_busy = 0;
         // accumulate mode has no waits to run out: a tile whose P contributions did not all
         // arrive shows up here as a missing output tile
@@ -1201,7 +1200,6 @@ __device__ void run1_mma(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_
         if (it.x != ITEM_COMPUTE) continue;
         if (!wait_bar<false>(smem_u32(&s.tempty[acc]), aphase ^ 1u, c, SITE_ACC_EMPTY, it.y)) break;
         tc_fence_after();
-        const long long t0 = clock64();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -1233,8 +1231,6 @@ __device__ void run1_mma(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, uint8_
             acc = 0;
             aphase ^= 1u;
         }
-        atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
-                  static_cast<unsigned long long>(clock64() - t0));
     }
     // Every MMA issued by this thread must complete before TMEM is released.
     umma_commit(smem_u32(&s.drain));
@@ -1513,7 +1509,6 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
                 break;
             }
             tc_fence_after();
-            const long long t0 = clock64();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
             for (int kb = 0; kb < p.num_kb; ++kb) {
                 if (!wait_bar<false>(smem_u32(&s.full[stage]), phase, c, SITE_STAGE_FULL, it.y)) {
@@ -1543,8 +1538,6 @@ __device__ void run2_mma(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, uint8_
                 acc = 0;
                 aphase ^= 1u;
             }
-            atomicAdd(reinterpret_cast<unsigned long long *>(&c.hdr->compute_busy),
-                      static_cast<unsigned long long>(clock64() - t0));
         }
         if (!ok) break;
     }
