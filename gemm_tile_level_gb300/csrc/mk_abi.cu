@@ -386,6 +386,18 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
                         : 1;
     if (p.chain_ranks > 1)
         p.num_pair_units = static_cast<int32_t>(g.num_pair_tiles * ((P + p.chain_ranks - 1) / p.chain_ranks));
+    if (p.chain_ranks == P && P > 1 && p.rank_major && o.raster_group <= 0) {
+        // Whole-tile units run every rank of a tile: the tiles in flight (one per SM pair) share
+        // operands rank by rank, so they are kept to a block of about sqrt(pairs) tile rows by
+        // pairs / rows columns.  Measured at P = 8, M = N = 8192, K_r = 3584: 8 x 10 runs 2.197 ms,
+        // 9 x 9 2.207, 8 rows x 17 columns (the running-sum slices) 2.215.
+        int32_t G = 1;
+        while ((G + 1) * (G + 1) <= role_units) ++G;
+        if (G > g.pair_tiles_m) G = static_cast<int32_t>(g.pair_tiles_m);
+        const int64_t W = (role_units + G - 1) / G;
+        p.raster_group = G;
+        p.band_cols = W < g.tiles_n ? static_cast<int32_t>(W) : 0;
+    }
     const int esize = p.partial_bf16 ? 2 : 4;
     p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P,
                                       esize);
