@@ -109,7 +109,7 @@ def test_short_m_sweep_shape_both_paths_same_bits(M):
                        rms_ref=rms)
 
 
-@pytest.mark.parametrize("M", [512, 256])   # the rank-ordered chain; tile owners
+@pytest.mark.parametrize("M", [1024, 512, 256])   # SM-pair units of several ranks; the one-SM chain; tile owners
 def test_reducescatter_and_distinct_outputs(M):
     P, N, Kr = 4, 520, 96
     wl = ig.Workload("ch_rs", "reducescatter", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16", seed=3)
@@ -119,6 +119,9 @@ def test_reducescatter_and_distinct_outputs(M):
         for order in (0, mk.MK_FLAG_RANK_MAJOR):
             shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts(tiles, flags=order))
             gu.assert_bit_exact(np.concatenate([gu.host_values(s) for s in shards]), ref)
+    for cr in (1, 3):
+        shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts(chain_ranks=cr))
+        gu.assert_bit_exact(np.concatenate([gu.host_values(s) for s in shards]), ref)
     for order in (0, mk.MK_FLAG_RANK_MAJOR):
         Cs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
         gu.call_ar(Ad, Bd, mk.MK_BF16, C=Cs, opts=ch_opts(flags=order))
