@@ -154,6 +154,19 @@ def test_missing_unit_times_out_then_recovers(tiles):
     gu.assert_bit_exact(gu.host_values(C), oracle.allreduce(A, B))
 
 
+def test_full_size_every_element_against_the_oracle():
+    """The bench workload (P=8, M=N=8192, K_r=3584, random operands, bf16 output) in the default
+    (chained) form, compared with the fp64 oracle on every one of its 67 M elements (the oracle
+    takes about a minute on the GPU host's cores).  The role split, the unfused baseline and the
+    other forms give the same bits (test_full_size_same_bits_as_the_reduce_role), so this covers
+    them too."""
+    wl = ig.WORKLOADS["ar_mlp_down_p8_m8192_n8192_k3584"]
+    A, B, Ad, Bd = gu.upload(wl)
+    got = gu.host_values(gu.call_ar(Ad, Bd, mk.MK_BF16, opts=ch_opts()))
+    ref = oracle.allreduce(A, B)
+    gu.check_tolerance(got, ref, out_bf16=True)
+
+
 def test_reducescatter_full_size_same_bits_and_sampled():
     wl = ig.WORKLOADS["rs_p8_m16384_n8192_k1024"]
     A, B, Ad, Bd = gu.upload(wl)
