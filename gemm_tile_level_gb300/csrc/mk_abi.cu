@@ -433,9 +433,9 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
 }
 
 // AllGather + GEMM workspace: the header and one readiness flag per 128-row chunk of A (rounded
-// up to whole 256-row pair tiles).
-size_t ag_workspace_bytes(const Geometry &g) {
-    return MK_WS_HEADER_BYTES + align_up(static_cast<size_t>(2 * g.pair_tiles_m) * sizeof(uint32_t), MK_WS_ALIGN);
+// up to whole 256-row pair tiles) and receiving rank.
+size_t ag_workspace_bytes(const Geometry &g, int P) {
+    return MK_WS_HEADER_BYTES + align_up(static_cast<size_t>(P) * 2 * g.pair_tiles_m * sizeof(uint32_t), MK_WS_ALIGN);
 }
 
 // First split of AllGather + GEMM (roles are fixed for the call): SMs for the copies in proportion
@@ -498,7 +498,7 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
         }
     }
     if (reinterpret_cast<uintptr_t>(ws) % MK_WS_ALIGN) return fail(MK_ERR_ALIGNMENT, "workspace not 256-byte aligned");
-    const size_t need = ag_workspace_bytes(g);
+    const size_t need = ag_workspace_bytes(g, P);
     if (ws_bytes < need) return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, need);
 
     int resident = 0;
@@ -778,7 +778,7 @@ size_t mk_workspace_size(int op, int P, int64_t M, int64_t N, int64_t K_per_rank
     Geometry g;
     if (!make_geometry(P, M, N, K_per_rank, &g)) return 0;
     if (op == MK_OP_ALLREDUCE || op == MK_OP_REDUCESCATTER) return g.total;
-    if (op == MK_OP_ALLGATHER_GEMM) return ag_workspace_bytes(g);
+    if (op == MK_OP_ALLGATHER_GEMM) return ag_workspace_bytes(g, P);
     return 0;
 }
 

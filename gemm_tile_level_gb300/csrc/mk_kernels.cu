@@ -959,10 +959,28 @@ __device__ void init_barriers(SmemCtl<STAGES> &s, const MkParams &p, uint32_t fu
 }
 
 // ----------------------------------------------------------------- AllGather + GEMM helpers
-// Producer thread: acquire the flag of 128-row chunk `chunk` of the gathered A (bounded), then
-// order the acquire before the TMA (async-proxy) reads of that chunk.
-__device__ bool wait_chunk_ready(const MkParams &p, const Ctx &c, int chunk, uint32_t epoch) {
-    const uint32_t *f = p.flags + chunk;
+// Copy item i -> (destination rank r, 256-row pair row y): band by band (raster_group pair rows),
+// rank by rank inside a band, the order in which the rank-major compute reads the gathered rows,
+// so that rank r's copy of a band is complete as soon as its own share of copies is.  Each CTA of
+// the pair copies one 128-row chunk (2y + its rank in the pair) to rank r's gathered buffer.
+__device__ __forceinline__ void ag_item(const MkParams &p, int i, int &r, int &y) {
+    const int G = p.raster_group;
+    const int b = i / (G * p.P);
+    const int rem = i - b * G * p.P;
+    const int gsize = min(G, p.pair_tiles_m - b * G);
+    r = rem / gsize;
+    y = b * G + (rem - r * gsize);
+}
+
+// Readiness flag of 128-row chunk `chunk` in rank r's gathered copy of A.
+__device__ __forceinline__ uint32_t *ag_flag(const MkParams &p, int chunk, int r) {
+    return p.flags + static_cast<size_t>(r) * (2 * p.pair_tiles_m) + chunk;
+}
+
+// Producer thread: acquire the flag of 128-row chunk `chunk` of rank r's gathered A (bounded),
+// then order the acquire before the TMA (async-proxy) reads of that chunk.
+__device__ bool wait_chunk_ready(const MkParams &p, const Ctx &c, int chunk, int r, uint32_t epoch) {
+    const uint32_t *f = ag_flag(p, chunk, r);
     uint64_t t0 = 0;
     for (uint32_t polls = 0; ld_acquire_gpu(f) != epoch; ++polls) {
         if (t0 == 0) t0 = globaltimer();
@@ -1021,7 +1039,8 @@ __device__ __forceinline__ void store_output_tile(const MkParams &p, uint32_t tm
 // thread drives bulk copies through the block's TMA ring: global -> shared in pieces of up to
 // 48 KiB (two pieces ahead), shared -> global to the P destinations as bulk groups.  The
 // chunk's rows are contiguous in the gathered buffers and, within one shard, in the source.
-__device__ void do_copy_chunk(const MkParams &p, const Ctx &c, int chunk, int etid, uint32_t epoch, Staging &st) {
+__device__ void do_copy_chunk(const MkParams &p, const Ctx &c, int chunk, int dst, int etid, uint32_t epoch,
+                              Staging &st) {
     if (etid == 0 && chunk < p.tiles_m) {
         constexpr uint32_t PIECE = 48u * 1024u;
         const size_t row_bytes = static_cast<size_t>(p.Kr) * 2;
@@ -1064,8 +1083,7 @@ __device__ void do_copy_chunk(const MkParams &p, const Ctx &c, int chunk, int et
         while (have0) {
             const uint32_t b = (st.seq + k) & 3u;
             wait_bar<false>(smem_u32(&st.rfull[b]), ((st.seq + k) >> 2) & 1u, c, SITE_STAGE_FULL, k);
-            for (int r = 0; r < p.P; ++r)
-                bulk_store(static_cast<char *>(p.ag_dst[r]) + pc[0].dst_off, smem_u32(st.ring + b * PIECE), pc[0].bytes);
+            bulk_store(static_cast<char *>(p.ag_dst[dst]) + pc[0].dst_off, smem_u32(st.ring + b * PIECE), pc[0].bytes);
             bulk_commit();
             Piece next2;
             const bool have2 = have1 && piece_at(k + 2, next2);
@@ -1081,7 +1099,7 @@ __device__ void do_copy_chunk(const MkParams &p, const Ctx &c, int chunk, int et
         }
         bulk_wait_all();
         fence_proxy_async_global();
-        st_release_gpu(p.flags + chunk, epoch);
+        st_release_gpu(ag_flag(p, chunk, dst), epoch);
         st.seq += k;
     }
     bar_sync(1, MK_EPI_THREADS);
@@ -1368,7 +1386,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     const bool ag = p.op == MK_IOP_AG;
     // tile owners (chained mode, short M) claim whole tiles and load the tile's P ranks in turn
     const ClaimGeom g{static_cast<uint32_t>((BN == 128 && p.chain_owner) ? p.num_pair_tiles : p.num_pair_units),
-                      static_cast<uint32_t>(ag ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), blockIdx.x >> 1,
+                      static_cast<uint32_t>(ag ? p.P * p.pair_tiles_m : p.num_pair_tiles * p.red_split), blockIdx.x >> 1,
                       gridDim.x >> 1, 2u, ag ? 1u : static_cast<uint32_t>(p.red_split), p.pair_tiles_m};
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);      // even CTA's full barriers
     const uint32_t wempty0 = mapa_shared(smem_u32(&s.wempty[0]), 0);
@@ -1430,7 +1448,7 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             if (p.op == MK_IOP_AG) {
                 if (p.ag_gather) {
                     // a failed wait has raised the abort: the loads still go ahead so the pipeline drains
-                    if (p.ag_wait && tm < p.tiles_m) (void)wait_chunk_ready(p, c, tm, s.epoch);
+                    if (p.ag_wait && tm < p.tiles_m) (void)wait_chunk_ready(p, c, tm, r, s.epoch);
                 } else {
                     const int sh = min(p.P - 1, tm * MK_BM / p.rows_per_shard);   // rows_per_shard % 128 == 0
                     amap = &p.tmA[sh];
@@ -1880,7 +1898,9 @@ __device__ void run2_epilogue(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
             }
         } else {
             if (p.op == MK_IOP_AG) {
-                do_copy_chunk(p, c, 2 * it.y + static_cast<int>(crank), etid, epoch, st);
+                int dst, y;
+                ag_item(p, it.y, dst, y);
+                do_copy_chunk(p, c, 2 * y + static_cast<int>(crank), dst, etid, epoch, st);
             } else {
                 int sm, tn;
                 raster(it.y / p.red_split, p.pair_tiles_m, p.tiles_n, p.raster_group, sm, tn);
@@ -1946,7 +1966,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_pair_kernel(const __grid_con
     } else if (lane == 0 && blockIdx.x == 0 &&
                (p.mode == MK_MODE_ADAPTIVE || (p.mode == MK_MODE_STATIC && p.trace))) {
         run_controller(p, c, p.num_pair_units,
-                       2 * (p.op == MK_IOP_AG ? p.pair_tiles_m : p.num_pair_tiles * p.red_split), 2,
+                       2 * (p.op == MK_IOP_AG ? p.P * p.pair_tiles_m : p.num_pair_tiles * p.red_split), 2,
                        gridDim.x >> 1, 2);
     }
     __syncwarp();

@@ -252,9 +252,11 @@ mk_status mk_gemm_reducescatter(int P, int64_t M, int64_t N, int64_t K_per_rank,
  *                   nothing is moved and the compute role reads the shards in
  *                   place (requires M/P to be a multiple of 128)
  *   C[r]          : M x N, out_dtype
- * Communication-role blocks copy 128-row chunks into every gathered buffer
- * and release one readiness flag per chunk; compute-role blocks acquire the
- * flag of the rows they load.  The split of SMs between the roles is fixed
+ * Communication-role blocks copy 128-row chunks into the gathered buffers,
+ * one (chunk, receiving rank) at a time in the order the compute reads them
+ * (band by band, rank by rank), and release one readiness flag per chunk and
+ * rank; compute-role blocks acquire the flag of the rows they load from their
+ * rank's buffer.  The split of SMs between the roles is fixed
  * for the call (comm_sms, or derived from the shape in adaptive mode);
  * MK_SPLIT_UNFUSED gathers in one kernel and multiplies in a second.
  * Workspace: mk_workspace_size(MK_OP_ALLGATHER_GEMM, P, M, N, K).
