@@ -473,6 +473,13 @@ def gpu_arm(args, wl, ranks):
                "sample": f"rows 0..{rows - 1} of {wl.M}, all N={wl.N}, all P={wl.P} ranks, "
                          f"K_r={wl.Kr}; {secs:.1f} s fp64"}
     clk = clocks.summary()
+    if roof["bound"] == "tensor":
+        # the same launch against the sustained peak (cuBLAS back to back under the power cap), the
+        # reference for a long run like the 200 timed steps here; and the SM cycles per launch at
+        # the median clock sampled during them
+        roof["frac_of_sustained_peak"] = achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        if clk.get("sm_mhz"):
+            roof["sm_cycles_per_launch"] = kernel_ms * 1e-3 * clk["sm_mhz"] * 1e6
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ranks.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
