@@ -143,6 +143,8 @@ bool make_geometry(int P, int64_t M, int64_t N, int64_t Kr, Geometry *g, int bn 
 // the fewest operand bytes (W = the whole width is the plain banded order).  At P = 8, M = N = 8192,
 // K_r = 3584: 8 pair rows x 17 tile columns per pass, 6 x 470 MB of operand reads instead of
 // 9 x 470 MB with 4-row full-width bands; at M = 16384, K_r = 1024: 1.6 GB instead of 2.4 GB.
+// (Chained units that cover all P ranks of a tile keep no running sums in L2; their tile order is
+// set after this, see run_rowparallel.)
 void choose_band_slices(bool pair, int P, int64_t M, int64_t N, int64_t Kr, int64_t rows, const Geometry &g,
                         int32_t *band_rows, int32_t *band_cols) {
     const double tile_bytes = static_cast<double>(pair ? 2 * MK_BM : MK_BM) * g.bn * 4.0;

@@ -26,11 +26,15 @@
 //   warp 10  : the split controller (block 0, adaptive mode)
 //
 // Two more ways to form the sum use the compute blocks alone (no reduce role):
-//   chained    : the epilogue of (tile, r) acquires flag[tile][r-1], adds its accumulator to the
-//                running sum of ranks 0..r-1 and stores it (rank P-1 writes the output): the
-//                reduce role's additions in its order, so the same bits.  On a short M one SM
-//                pair owns each 256 x 128 tile instead, computes its P ranks in turn and keeps
-//                the running sum in TMEM (owner_tile);
+//   chained    : the reduce role's additions in its order, so the same bits, made where the
+//                partials are produced.  On SM pairs a compute unit covers chain_ranks
+//                consecutive ranks of a tile (all P by default), computed back to back into the
+//                two TMEM accumulators; the epilogue adds the sum so far into each new
+//                accumulator in place and writes the output after rank P-1 (chain_span).  With
+//                fewer ranks per unit, or one-SM tiles, the unit of (tile, r) acquires
+//                flag[tile][r-1] and adds to the running sum stored in the workspace
+//                (chain_partial).  On a short M one SM pair owns each 256 x 128 tile and keeps
+//                the running sum in TMEM next to the accumulators (owner_tile);
 //   accumulate : the epilogue adds its accumulator into one fp32 tile with L2 reductions, and
 //                the last of the P contributions writes the output (no fixed order).
 //
@@ -1433,7 +1437,8 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
         if (ahead_mode) ahead = atomicAdd(&c.hdr->compute_next, 1u);   // consumed at the next claim
         const int u = it.y;
         if (!wait_epilogue_done(&s.epi_done, ring_free_at, c)) break;
-        // tile owners exist only with 128-column tiles: the 256-column kernel keeps one unit per item
+        // a unit's ranks (chained mode: chain_ranks of them; otherwise one), or a tile owner's P
+        // ranks (tile owners exist only with 128-column tiles)
         const bool owner = BN == 128 && p.chain_owner;
         int sm, tn, r0 = 0, nranks = p.P;
         if (owner)
