@@ -43,7 +43,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "gemm_tile_level_gb300", "csrc", f)
-                  for f in ("mk_kernels.cu", "mk_ptx.cuh", "mk_internal.h")]
+                  for f in ("mk_kernels.cu", "mk_ptx.cuh", "mk_device.cuh", "mk_internal.h", "mk_abi.cu")]
 
 
 def workload_by_name(name: str) -> ig.Workload:
@@ -73,11 +73,17 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: comments and layout whitespace are left out, so that only
+    a change to what compiles makes a committed DRAM capture stale."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
