@@ -30,12 +30,13 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr double kRasterL2Budget = 32e6;   // tile-major: bytes of A rows (all ranks) resident per band
 constexpr double kBandL2Budget = 24e6;     // rank-major: bytes of one rank's A rows resident per band
 constexpr int64_t kRankMajorMinRows = 1024;  // default compute order: rank-major from this M on
-constexpr int64_t kChainedOneSmMaxRows = 512; // chained mode: one-SM tiles up to this M
+constexpr int64_t kChainedOneSmMaxRows = 256; // chained mode: one-SM tiles up to this M (unless tile owners)
 #ifndef MK_CHAIN_OWNER_MAX_ROWS
 #define MK_CHAIN_OWNER_MAX_ROWS 256
 #endif
 constexpr int64_t kChainedOwnerMaxRows = MK_CHAIN_OWNER_MAX_ROWS; // chained mode: tile owners up to this M
 constexpr double kAccumulatorL2Budget = 36e6; // accumulate mode: bytes of one band's fp32 accumulators
+constexpr double kOperandHintBytes = 64e6;     // A rows of a band beyond which operand loads take no L2 hints
 constexpr int64_t kAgBandRows = 4;             // AllGather + GEMM: 256-row tile rows per rank-major band
 // Pause between an epilogue's 32-column store chunks: an eighth of one unit's MMA time at about
 // 0.33 us per 64-deep k-block, at most 1 us (4 chunks per warp then take at most half a unit).
@@ -254,17 +255,16 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
     if (ws_bytes < g.total)
         return fail(MK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, g.total);
 
-    // Chained mode on a short M (one band of at most two 256-row tile rows) folds the ranks of a
-    // tile while several of them are still in flight; one-SM tiles give each rank pass twice
-    // the tiles, so that fewer folds wait on a predecessor (measured: 2-3 % faster at M <= 512).
-    //
-    // With a single 256-row band (M <= 256) every rank of a tile is in flight at once, the P folds
-    // of a tile follow one another through L2 and their latency sets the call time.  There one SM
-    // pair owns each 256 x 128 tile instead: it computes the tile's P ranks one after the other
-    // and its epilogue keeps the running sum in TMEM (the same additions in the same order), so no
-    // fold waits on another block (measured at P=8, N=8192, K_r=1024: 56 us against 60 us for the
-    // chain; at M = 512 and up the chain is faster, 81 against 100 us).  A caller that fixes the
-    // tile kind or the unit order, or withholds a unit, gets the rank-ordered chain.
+    // Chained mode on a short M.  With a single 256-row band (M <= 256) one SM pair owns each
+    // 256 x 128 tile: it computes the tile's P ranks one after the other and its epilogue keeps
+    // the running sum in TMEM (the same additions in the same order), so no fold waits on another
+    // block.  Measured at P = 8, N = 8192, K_r = 1024, M = 256 (us per call): tile owners 56.4,
+    // SM-pair units of all 8 / 4 / 2 ranks of a 256 x 256 tile 64.1 / 62.2 / 60.2 (32 tiles
+    // leave most pairs idle), the one-rank chain on one-SM tiles 60.  From M = 512 on the SM-pair
+    // units of all P ranks take over: 66.6 us at M = 512 against 85.3 for the one-SM chain and
+    // 100 for tile owners.  A caller that fixes the tile kind or the unit order at M <= 256 gets
+    // the one-rank chain on one-SM tiles; a withheld unit (fault injection) gives one-rank units
+    // at any M.
     const bool chain_owner = o.split_mode == MK_SPLIT_CHAINED && M <= kChainedOwnerMaxRows && o.debug_skip_unit < 0 &&
                              (o.flags & (MK_FLAG_SINGLE_SM_TILES | MK_FLAG_RANK_MAJOR | MK_FLAG_TILE_MAJOR)) == 0;
     const bool chained_short = o.split_mode == MK_SPLIT_CHAINED && M <= kChainedOneSmMaxRows && !chain_owner;
@@ -399,6 +399,18 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
         const int64_t W = (role_units + G - 1) / G;
         p.raster_group = G;
         p.band_cols = W < g.tiles_n ? static_cast<int32_t>(W) : 0;
+    }
+    // Operand loads: A rows evict_last and B columns evict_first keep a band's A rows in L2 while
+    // B streams past them.  A unit of several ranks reads the band's A rows of all its ranks;
+    // where those exceed kOperandHintBytes they cannot stay in L2 until the band's next tiles, the
+    // tiles in flight share B as much as A, and both are read with the normal policy.  Measured
+    // with units of all 8 ranks (8-row bands): K_r = 3584, M = N = 8192 (117 MB of band A rows):
+    // 3.98 against 5.1-5.3 GB of DRAM reads per call and 1.9 % faster (eight interleaved pairs
+    // of runs); K_r = 1024, M = 4096 (34 MB): 0.41 against 0.50 GB and 0.7 % slower without hints.
+    {
+        const double band_a = static_cast<double>(p.raster_group) * (pair ? 2 * MK_BM : MK_BM) * Kr * 2.0 *
+                               p.chain_ranks;
+        p.op_hints = p.l2_hints && !(p.chain_ranks > 1 && band_a > kOperandHintBytes);
     }
     const int esize = p.partial_bf16 ? 2 : 4;
     p.red_split = choose_reduce_split(o.reduce_split, pair ? g.num_pair_tiles : g.num_tiles, role_units, g.bn, P,
@@ -576,6 +588,7 @@ mk_status run_allgather(int P, int64_t M, int64_t N, int64_t K, const void *cons
     p.ctrl_tail_ns = 0;   // unused: AllGather + GEMM fixes the roles for the call
     p.red_split = 1;
     p.l2_hints = (o.flags & MK_FLAG_NO_L2_HINTS) ? 0 : 1;
+    p.op_hints = p.l2_hints;
     p.cooperative = (o.flags & MK_FLAG_NO_COOPERATIVE) ? 0 : 1;
     p.ag_gather = gather;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

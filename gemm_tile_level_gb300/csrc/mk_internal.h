@@ -77,7 +77,8 @@ struct MkParams {
     int32_t op, out_bf16, num_out, rows_per_shard;
     int32_t mode, static_nr, init_nr, raster_group;
     int32_t discard;
-    int32_t l2_hints;            // TMA loads: A rows evict_last, B columns evict_first
+    int32_t l2_hints;            // L2 eviction priorities on partial tiles, running sums and outputs
+    int32_t op_hints;            // TMA operand loads: A rows evict_last, B columns evict_first (else normal)
     int32_t cooperative;         // launch attribute (host side only)
     // AllGather + GEMM: A_shard[s] ((M/P) x K) copied in 128-row chunks into every A_gathered[r]
     // (M x K); the compute role waits on the chunk flags (ag_wait) before loading A rows.

@@ -1137,8 +1137,8 @@ __device__ void run1_producer(const MkParams &p, SmemCtl<Cfg1<BN>::STAGES> &s, u
     uint32_t phase = 0, wphase = 0;
     bool exhausted = false, stop = false;
     // A rows are reused by every column of the raster group: keep them; B columns stream.
-    const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
-    const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
+    const uint64_t pol_a = p.op_hints ? policy_evict_last() : policy_evict_normal();
+    const uint64_t pol_b = p.op_hints ? policy_evict_first() : policy_evict_normal();
     uint32_t pushed = 0, ring_free_at = 0;   // ring free once the epilogue has finished ring_free_at items
     bool last_reduce = false;
     uint32_t target = 0;                     // adaptive split: target_nr as last read
@@ -1399,8 +1399,8 @@ __device__ void run2_producer(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, u
     int stage = 0, wq = 0;
     uint32_t phase = 0, wphase = 0;
     bool exhausted = false, stop = false;
-    const uint64_t pol_a = p.l2_hints ? policy_evict_last() : policy_evict_normal();
-    const uint64_t pol_b = p.l2_hints ? policy_evict_first() : policy_evict_normal();
+    const uint64_t pol_a = p.op_hints ? policy_evict_last() : policy_evict_normal();
+    const uint64_t pol_b = p.op_hints ? policy_evict_first() : policy_evict_normal();
     uint32_t pushed = 0, ring_free_at = 0;
     bool last_reduce = false;
     uint32_t target = 0;   // adaptive split: target_nr as last read (see claim_work)

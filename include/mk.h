@@ -84,9 +84,9 @@ typedef enum {
                                default), computed back to back with the running sum kept in
                                tensor memory between them.  For M <= 256 one SM pair computes
                                all P ranks of a 256 x 128 tile and keeps the running sum in
-                               tensor memory (the same additions); for 256 < M <= 512 it uses
-                               one-SM tiles.  A tile-kind or unit-order flag, or
-                               debug_skip_unit, selects the one-rank chain at any M. */
+                               tensor memory (the same additions).  MK_FLAG_SINGLE_SM_TILES,
+                               or a unit-order flag at M <= 256, selects the one-rank chain on
+                               one-SM tiles; debug_skip_unit selects one-rank units at any M. */
 } mk_split_mode;
 
 /* Bits of mk_opts.flags */

@@ -96,20 +96,24 @@ def test_zero_k_gives_zeros(P, M, N):
 
 @pytest.mark.parametrize("M", [256, 512])
 def test_short_m_sweep_shape_both_paths_same_bits(M):
-    """The sweep's short shapes (P=8, N=8192, K_r=1024): tile owners and the rank-ordered chain
-    against the unfused baseline, bit for bit, and against the oracle on sampled elements."""
+    """The sweep's short shapes (P=8, N=8192, K_r=1024): tile owners (M = 256), SM-pair units of
+    several ranks (M = 512) and the one-rank chain on one-SM tiles against the unfused baseline,
+    bit for bit, and against the oracle on sampled elements."""
     wl = ig.sweep_workload(M)
     A, B, Ad, Bd = gu.upload(wl)
     want = gu.call_ar(Ad, Bd, mk.MK_BF16, opts=api.make_opts(mk.MK_SPLIT_UNFUSED))
     for fl in (0, mk.MK_FLAG_RANK_MAJOR, mk.MK_FLAG_SINGLE_SM_TILES):
         assert torch.equal(gu.call_ar(Ad, Bd, mk.MK_BF16, opts=ch_opts(flags=fl)), want)
+    if M > 256:   # SM-pair units of all 8 ranks by default; of 3 ranks (a short last group) and 2
+        for cr in (2, 3):
+            assert torch.equal(gu.call_ar(Ad, Bd, mk.MK_BF16, opts=ch_opts(chain_ranks=cr)), want)
     rows, cols = gu.sample_indices(wl.M, wl.N, 1024)
     rms = float(np.sqrt(np.mean(oracle.allreduce_rows(A, B, 0, 2) ** 2)))
     gu.check_tolerance(gu.host_values(want)[rows, cols], oracle.allreduce_at(A, B, rows, cols), out_bf16=True,
                        rms_ref=rms)
 
 
-@pytest.mark.parametrize("M", [1024, 512, 256])   # SM-pair units of several ranks; the one-SM chain; tile owners
+@pytest.mark.parametrize("M", [1024, 512, 256])   # SM-pair units of several ranks (1024, 512); tile owners (256)
 def test_reducescatter_and_distinct_outputs(M):
     P, N, Kr = 4, 520, 96
     wl = ig.Workload("ch_rs", "reducescatter", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "bf16", seed=3)
