@@ -326,6 +326,7 @@ class Problem:
             self.op = mk.MK_OP_ALLREDUCE
         self.ws = api.workspace(self.op, wl.P, wl.M, wl.N, wl.Kr)
         self.mk = mk
+        torch.cuda.synchronize()   # uploads and the zeroed workspace land before calls on other streams
 
     def call(self, opts, stream):
         mk, wl = self.mk, self.wl
@@ -334,6 +335,14 @@ class Problem:
                                             self.out_code, self.ws, opts=opts, stream=stream)
         return mk.mk_gemm_allreduce(wl.P, wl.M, wl.N, wl.Kr, self.Ad, self.Bd, [self.C] * wl.P,
                                     self.out_code, self.ws, opts=opts, stream=stream)
+
+
+def clear_workspace(torch, ws):
+    """Zero a workspace between calls issued on another stream: the calls before it have finished
+    and the zeros have landed before any call after it starts."""
+    torch.cuda.synchronize()
+    ws.zero_()
+    torch.cuda.synchronize()
 
 
 def time_launches(torch, prob, opts, steps, warmup, stream):
@@ -366,7 +375,7 @@ def gpu_arm(args, wl, ranks):
         prob = Problem(wl, torch, api, mk)
         opts = split_opts(api, mk, args.split, args.comm_sms)
         if args.split == "accumulate":
-            prob.ws.zero_()
+            clear_workspace(torch, prob.ws)
         for _ in range(args.warmup):
             mk.check(prob.call(opts, stream))
         mk.check(mk.mk_status_check(prob.ws, stream))
@@ -409,7 +418,7 @@ def gpu_arm(args, wl, ranks):
         # ---------------- the accumulate variant (no reduce role) on the same inputs (context)
         accumulate = None
         if args.split != "accumulate" and not args.no_baseline:
-            prob.ws.zero_()   # the other modes leave partial tiles where its accumulators go
+            clear_workspace(torch, prob.ws)   # the other modes leave partial tiles where its accumulators go
             n = max(3, min(args.steps, 20))
             tot, _ = time_launches(torch, prob, split_opts(api, mk, "accumulate", 0), n, 2, stream)
             accumulate = {"value": wl.flops / (tot / n * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -512,6 +521,42 @@ CONFIG_WORKLOADS = ("ar_p2_m128_n128_k256", "ar_p8_m2048_n4096_k512", "rs_p8_m16
                     "ar_sweep_p8_m256_n8192_k1024", "ar_sweep_p8_m4096_n8192_k1024")
 CONFIG_SPLITS = ("chained", "adaptive", "unfused", "accumulate")
 AG_SHAPE = (8, 8192, 3584, 4096)
+L2_BYTES = 129 << 20          # GB300 L2
+FLUSH_BELOW = 2 * L2_BYTES    # configurations whose operands take less are timed call by call with L2 flushed
+
+
+def time_config(torch, prob, opts, steps, warmup, stream, flush):
+    """Device time per call of one configuration (ms).  With `flush` (a device buffer larger than
+    L2): each call alone between two events, the buffer rewritten before it so that the call finds
+    none of its operands in L2.  Without: the calls back to back between one pair of events, queued
+    behind a short device sleep so that the host's issue rate does not set the time."""
+    for _ in range(warmup):
+        prob.mk.check(prob.call(opts, stream))
+    prob.mk.check(prob.mk.mk_status_check(prob.ws, stream))
+    torch.cuda.synchronize()
+    if flush is not None:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in ev:
+                flush.add_(1)
+                e0.record(stream)
+                prob.mk.check(prob.call(opts, stream))
+                e1.record(stream)
+        torch.cuda.synchronize()
+        prob.mk.check(prob.mk.mk_status_check(prob.ws, stream))
+        return sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sleep = getattr(torch.cuda, "_sleep", None)
+    with torch.cuda.stream(stream):
+        if sleep is not None:
+            sleep(int(2e6))   # about 1 ms: the host queues the calls meanwhile
+        e0.record(stream)
+        for _ in range(steps):
+            prob.mk.check(prob.call(opts, stream))
+        e1.record(stream)
+    torch.cuda.synchronize()
+    prob.mk.check(prob.mk.mk_status_check(prob.ws, stream))
+    return e0.elapsed_time(e1) / steps
 
 
 def configs_leg(torch, api, mk, stream, peaks, steps: int, warmup: int):
@@ -520,17 +565,23 @@ def configs_leg(torch, api, mk, stream, peaks, steps: int, warmup: int):
     role split, the unfused two-kernel baseline and the accumulate variant), then AllGather + GEMM
     fused against unfused.  About 20 calls per point."""
     out = {}
+    flush = torch.zeros(FLUSH_BELOW // 4, dtype=torch.float32, device="cuda")
     for name in CONFIG_WORKLOADS:
         wl = workload_by_name(name)
         prob = Problem(wl, torch, api, mk)
         nbytes = algorithmic_bytes(wl, 4)
+        operand_bytes = wl.P * (wl.M + wl.N) * wl.Kr * 2
+        small = operand_bytes < FLUSH_BELOW
         rec = {"op": wl.op, "P": wl.P, "M": wl.M, "N": wl.N, "K_per_rank": wl.Kr, "out_dtype": wl.out_dtype,
-               "flops": wl.flops, "algorithmic_bytes": nbytes, "steps": steps}
+               "flops": wl.flops, "algorithmic_bytes": nbytes, "steps": steps,
+               "l2": ("operands %.1f MB: L2 flushed (%d MB written) before every timed call, each call timed "
+                      "alone" % (operand_bytes / 1e6, FLUSH_BELOW >> 20)) if small else
+                     ("operands %.0f MB > 2 x 129 MB L2, no flush; calls back to back" % (operand_bytes / 1e6))}
         for split in CONFIG_SPLITS:
             if split == "accumulate":
-                prob.ws.zero_()   # the other modes leave partial tiles where its accumulators go
-            tot, _ = time_launches(torch, prob, split_opts(api, mk, split, 0), steps, warmup, stream)
-            ms = tot / steps
+                clear_workspace(torch, prob.ws)   # the other modes leave partial tiles where its accumulators go
+            ms = time_config(torch, prob, split_opts(api, mk, split, 0), steps, warmup, stream,
+                             flush if small else None)
             rf = roofline_of(wl.flops, nbytes, ms, peaks)
             rec["bound"] = rf["bound"]
             rec["roofline_ms"] = rf["roofline_ms"]
@@ -546,6 +597,7 @@ def configs_leg(torch, api, mk, stream, peaks, steps: int, warmup: int):
         out[name] = rec
         del prob
         torch.cuda.empty_cache()
+    del flush
     P, M, N, K = AG_SHAPE
     ag = AgProblem(torch, api, mk, P, M, N, K)
     rec = {"op": "allgather_gemm", "P": P, "M": M, "N": N, "K": K, "out_dtype": "bf16", "flops": ag.flops,
@@ -710,6 +762,7 @@ class AgProblem:
         self.C = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
         self.G = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
         self.ws = api.workspace(mk.MK_OP_ALLGATHER_GEMM, P, M, N, K)
+        torch.cuda.synchronize()   # uploads and the zeroed workspace land before calls on other streams
 
     def call(self, mode, stream):
         o = self.api.make_opts(mode, flags=_EXTRA_FLAGS & ~(BF16_PARTIALS_FLAG | B_NK_FLAG))
@@ -746,6 +799,7 @@ class RingProblem:
         self.L = [torch.empty((H, S), dtype=torch.float32, device="cuda") for _ in range(P)]
         self.R = [torch.empty((P - 1, 2, H, S, d), dtype=torch.bfloat16, device="cuda") for _ in range(P)] if P > 1 else None
         self.ws = api.ring_attention_workspace(P, H, S, d)
+        torch.cuda.synchronize()   # uploads and the zeroed workspace land before calls on other streams
         # Q, K, V read, the KV forwarded P-1 times (read and written), O and lse written
         self.nbytes = 3 * P * H * S * d * 2 + 2 * (P - 1) * P * H * S * d * 2 * 2 + P * H * S * (d * 2 + 4)
 
@@ -905,7 +959,7 @@ def sweep(args):
             lo, step = (1, args.sweep_stride) if _EXTRA_FLAGS & 2 else (2, max(2, args.sweep_stride))
             static = {nr: ms(split_opts(api, mk, "static", nr)) for nr in range(lo, S - 1, step)}
             unf = ms(split_opts(api, mk, "unfused", 0))
-            prob.ws.zero_()
+            clear_workspace(torch, prob.ws)
             acc = ms(split_opts(api, mk, "accumulate", 0))
             chn = ms(split_opts(api, mk, "chained", 0))
             best_nr = min(static, key=static.get)
