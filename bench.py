@@ -444,6 +444,11 @@ def gpu_arm(args, wl, ranks):
                        "note": "MK_SPLIT_CHAINED: each rank's epilogue adds its tile to the running sum of the ranks "
                                "before it, in rank order (the reduce role's additions, same bits)"}
 
+        # ---------------- cuBLAS through torch on the same operands (context: not the method)
+        library = None
+        if not args.no_baseline and ranks.world == 1:
+            library = library_leg(torch, prob, max(3, min(args.steps, 20)), stream, ms_per_step)
+
         # ---------------- the controller's trace of one adaptive call (Figure 7a of the method)
         if args.trace:
             trace_leg(torch, api, mk, prob, stream, args.trace, "adaptive")
@@ -505,8 +510,49 @@ def gpu_arm(args, wl, ranks):
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "unfused_baseline": unfused, "adaptive_split": adaptive, "accumulate_variant": accumulate,
-            "chained_variant": chained, "configs": configs}
+            "chained_variant": chained, "library_context": library, "configs": configs}
     print(json.dumps(line), flush=True)
+
+
+def library_leg(torch, prob, steps, stream, mk_ms):
+    """cuBLAS (torch.matmul / torch.bmm) on the same operands, as context only: one GEMM over the
+    concatenated K (A_cat = [A_0 | ... | A_{P-1}], B_cat = [B_0; ...; B_{P-1}]), the cost of the
+    product with no reduction between ranks at all; and the P rank GEMMs as one batched GEMM with
+    bf16 outputs, then their sum (an unfused form from library kernels, with bf16 partial tiles, so
+    other numerics)."""
+    wl = prob.wl
+    b_kn = [b.t() for b in prob.Bd] if _EXTRA_FLAGS & B_NK_FLAG else prob.Bd
+    with torch.cuda.stream(stream):
+        A_cat = torch.cat(prob.Ad, dim=1)
+        B_cat = torch.cat(b_kn, dim=0)
+        A_st = torch.stack(prob.Ad)
+        B_st = torch.stack(b_kn)
+    torch.cuda.synchronize()
+
+    def per_call(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    gemm_ms = per_call(lambda: torch.matmul(A_cat, B_cat))
+    bmm_ms = per_call(lambda: torch.bmm(A_st, B_st).sum(dim=0))
+    del A_cat, B_cat, A_st, B_st
+    torch.cuda.empty_cache()
+    tf = lambda ms: wl.flops / (ms * 1e-3) / 1e12
+    return {"cublas_gemm_concatenated_k": {"ms": gemm_ms, "tflops": tf(gemm_ms),
+                                           "note": "one bf16 GEMM M x (P*K_r) x N, fp32 accumulation, bf16 out: "
+                                                   "no reduction between ranks (context, not the method)"},
+            "cublas_bmm_then_sum": {"ms": bmm_ms, "tflops": tf(bmm_ms),
+                                    "note": "torch.bmm over the P ranks (bf16 partial tiles), then sum over ranks"},
+            "value_over_cublas_gemm": gemm_ms / mk_ms, "steps": steps}
 
 
 def roofline_of(flops: float, nbytes: float, ms: float, peaks: dict) -> dict:

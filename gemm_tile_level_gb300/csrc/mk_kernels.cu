@@ -1750,21 +1750,29 @@ __device__ bool chain_span(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, cons
             next_acc();
             if (!wait_acc()) return false;
             if (exists && folded && !kz) {
-                // the MMAs of the next rank wait for `prev`: the loads of both accumulators go
-                // out together and the stores are waited for once, at the end
+                // the MMAs of the next rank wait for `prev`: the loads of 32 columns of both
+                // accumulators go out together (one wait per 32 columns) and the stores are
+                // waited for once, at the end
                 const uint32_t ta = tmem_base + static_cast<uint32_t>(prev * BN) + lanes;
                 const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {   // 16 of the thread's BN/2 columns at a time
+                for (int cc = 0; cc < BN / 32; cc += 2) {   // 32 of the thread's BN/2 columns at a time
                     const uint32_t col0 = static_cast<uint32_t>(half * (BN / 2) + cc * 16);
-                    uint32_t va[16], vb[16];
+                    uint32_t va[16], vb[16], vc[16], vd[16];
                     tmem_ld16_nowait(ta + col0, va);
                     tmem_ld16_nowait(tb + col0, vb);
+                    tmem_ld16_nowait(ta + col0 + 16, vc);
+                    tmem_ld16_nowait(tb + col0 + 16, vd);
                     tmem_wait_ld16(va);
                     tmem_wait_ld16(vb);
+                    tmem_wait_ld16(vc);
+                    tmem_wait_ld16(vd);
 #pragma unroll
                     for (int q = 0; q < 16; ++q) vb[q] = __float_as_uint(__uint_as_float(va[q]) + __uint_as_float(vb[q]));
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) vd[q] = __float_as_uint(__uint_as_float(vc[q]) + __uint_as_float(vd[q]));
                     tmem_st16_nowait(tb + col0, vb);
+                    tmem_st16_nowait(tb + col0 + 16, vd);
                 }
                 tmem_wait_st();
             }
