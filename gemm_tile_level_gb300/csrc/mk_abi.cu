@@ -428,7 +428,12 @@ mk_status run_rowparallel(int op, int P, int64_t M, int64_t N, int64_t Kr, const
 
     if (o.split_mode == MK_SPLIT_UNFUSED) {
         p.mode = MK_MODE_COMPUTE_ONLY;
+        // The reduce kernel deals its items out statically: half tiles (two items per tile) ran
+        // 0.6-1.4 % faster than whole tiles at P = 8, N = 8192, M = 4096 and 16384 (K_r = 1024)
+        // and M = 8192 (K_r = 3584), where whole tiles already give every block 13 or more.
         p.red_split = choose_reduce_split(o.reduce_split, g.num_tiles, S, g.bn, P, esize);
+        if (o.reduce_split <= 0 && p.red_split < 2)
+            p.red_split = choose_reduce_split(2, g.num_tiles, S, g.bn, P, esize);
         e = mk_launch_persistent(p, g.bn, pair, S, s);
         if (e != cudaSuccess) return fail_cuda(e, "launch of the per-rank GEMM kernel");
         e = mk_launch_reduce(p, g.bn, S, s);
