@@ -49,16 +49,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // ------------------------------------------------------------------ TMA
-// 2-D tiled bulk tensor copy global -> shared, completion counted on `bar` in bytes.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int32_t x,
-                                            int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
+// 2-D tiled bulk tensor copy global -> shared, completion counted on `bar` in bytes, with an L2
+// eviction-priority policy.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, uint32_t bar,
                                                  int32_t x, int32_t y, uint64_t policy) {
     asm volatile(
@@ -303,16 +295,7 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t cluster_addr, int32_t a, 
 }
 
 // TMA tile load into this CTA's shared memory whose completion is counted on an mbarrier of
-// either CTA of the pair (`bar_cluster` is a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster, int32_t x,
-                                                 int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(tmap), "r"(bar_cluster), "r"(x), "r"(y)
-        : "memory");
-}
-
+// either CTA of the pair (`bar_cluster` is a shared::cluster address), with an L2 policy.
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar_cluster,
                                                       int32_t x, int32_t y, uint64_t policy) {
     asm volatile(
@@ -460,17 +443,6 @@ __device__ __forceinline__ void st_u4(void *p, uint32_t a, uint32_t b, uint32_t 
 }
 
 // ------------------------------------------------------------------ attention helpers
-// 3-D tiled bulk tensor copy global -> shared (coordinates innermost first), completion counted
-// on `bar` in bytes, with an L2 eviction-priority policy.
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
-                                                 int32_t z, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
-        : "memory");
-}
-
 // 16 consecutive 32-bit columns of the warp's 32 TMEM lanes, without waiting: the registers hold
 // the values only after tmem_wait_ld16 on them.
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&v)[16]) {
@@ -552,26 +524,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 16-byte store to shared memory (32-bit shared address).
-__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-// Store 32 consecutive 32-bit columns into the warp's 32 TMEM lanes (one row per thread), then
-// wait until the stores are done.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
 }
 
 // Two fp32 -> packed bf16x2 with round-to-nearest-even; `lo` lands in bits 0..15.
