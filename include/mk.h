@@ -160,8 +160,10 @@ typedef enum {
  *                     column slices, each claimed as its own item, so that the
  *                     final reductions of a shape with few tiles spread over
  *                     the whole grid; 0 = the smallest power of two (at most
- *                     8) giving every block (SM pair) at least one item, and at
- *                     least 2 for the reduce kernel of MK_SPLIT_UNFUSED.
+ *                     8) giving every block (SM pair) at least one item, at least
+ *                     2 where whole tiles give a block (SM pair) fewer than eight
+ *                     items, and at least 2 for the reduce kernel of
+ *                     MK_SPLIT_UNFUSED.
  *                     Values above the tile's chunk count (16 for 256-column
  *                     tiles with P <= 8) are clamped to it.  Every element is
  *                     still summed over ranks 0..P-1 in order, so results do
