@@ -127,3 +127,17 @@ def test_benchmarked_shape_every_rank(split):
             assert torch.equal(G[r], cat_dev), f"gathered copy of rank {r} differs from the shards"
         del C, G, Ad, Bd, cat_dev
         torch.cuda.empty_cache()
+
+
+def test_benchmarked_shape_every_element():
+    """The bench's AllGather + GEMM shape (P=8, M=8192, K=4096, 3584 columns per rank) on random
+    inputs, fused: every element of every rank's output against the fp64 oracle (about 35 s of
+    the oracle on the GPU host's cores)."""
+    P, M, N, K = 8, 8192, 3584, 4096
+    A, B, Ad, Bd = make(P, M, N, K, ig.normal(1.0), ig.normal(1.0 / K), seed=0)
+    C, G = run(Ad, Bd, mk.MK_BF16)
+    got = [gu.host_values(c) for c in C]
+    del C, G, Ad, Bd
+    torch.cuda.empty_cache()
+    for r, ref in enumerate(oracle.allgather_gemm(A, B)):
+        gu.check_tolerance(got[r], ref, out_bf16=True)

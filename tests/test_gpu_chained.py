@@ -171,6 +171,19 @@ def test_full_size_every_element_against_the_oracle():
     gu.check_tolerance(got, ref, out_bf16=True)
 
 
+def test_reducescatter_full_size_every_element_against_the_oracle():
+    """The ReduceScatter workload (P=8, M=16384, N=8192, K_r=1024, eight 2048-row bf16 shards) in
+    the default (chained) form: the shards, concatenated, against the fp64 oracle on every one of
+    the 134 M elements (about 40 s of the oracle on the GPU host's cores)."""
+    wl = ig.WORKLOADS["rs_p8_m16384_n8192_k1024"]
+    A, B, Ad, Bd = gu.upload(wl)
+    shards = gu.call_rs(Ad, Bd, mk.MK_BF16, opts=ch_opts())
+    got = np.concatenate([gu.host_values(sh) for sh in shards])
+    del shards, Ad, Bd
+    torch.cuda.empty_cache()
+    gu.check_tolerance(got, oracle.allreduce(A, B), out_bf16=True)
+
+
 def test_reducescatter_full_size_same_bits_and_sampled():
     wl = ig.WORKLOADS["rs_p8_m16384_n8192_k1024"]
     A, B, Ad, Bd = gu.upload(wl)
