@@ -510,7 +510,10 @@ def gpu_arm(args, wl, ranks):
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "unfused_baseline": unfused, "adaptive_split": adaptive, "accumulate_variant": accumulate,
-            "chained_variant": chained, "library_context": library, "configs": configs}
+            "chained_variant": chained, "library_context": library,
+            "launch_ms": {"mean": kernel_ms, "median": statistics.median(per_launch), "min": min(per_launch),
+                          "max": max(per_launch), "launches": len(per_launch)},
+            "configs": configs}
     print(json.dumps(line), flush=True)
 
 
