@@ -82,6 +82,8 @@ SHAPES = [
     (4, 2, 384),     # one and a half query units per slice
     (2, 1, 64),
     (8, 2, 128),
+    (16, 1, 256),    # the most ranks: fifteen forwarding steps
+    (5, 2, 640),     # odd P, a unit and a quarter per slice, ragged last KV tile of 128
 ]
 
 
