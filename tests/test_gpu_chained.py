@@ -44,6 +44,7 @@ SHAPES = [
     (5, 1100, 520, 72),    # SM pairs, odd P: the last unit folds one rank
     (1, 640, 264, 64),     # SM pairs, one rank: straight to the output
     (2, 768, 136, 40),     # SM pairs, P = 2: one two-rank unit per tile, ragged N
+    (16, 640, 392, 48),    # SM pairs, the most ranks: sixteen folds per unit, ragged M and N
 ]
 
 
