@@ -46,6 +46,7 @@ SHAPES = [
     (4, 1024, 264, 200),
     (8, 2048, 512, 512),
     (1, 130, 8, 8),
+    (16, 2048, 264, 136),   # the most ranks, ragged N and K
 ]
 
 
