@@ -1725,21 +1725,30 @@ __device__ bool chain_span(const MkParams &p, SmemCtl<Cfg2<BN>::STAGES> &s, cons
             folded = wait_predecessor(p, c, lt, r0, lane, etid, epoch);
             if (folded) {
                 const uint32_t ta = tmem_base + static_cast<uint32_t>(acc * BN) + lanes;
+                // 32 of the thread's BN/2 columns at a time: the running sum's L2 loads for both
+                // 16-column halves go out before the first is used, one round trip per 32 columns
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {   // 16 of the thread's BN/2 columns at a time
-                    const int col0 = half * (BN / 2) + cc * 16;
-                    const float *base = S + (static_cast<size_t>(col0 >> 3) * MK_BM + row) * 8;
-                    float sv[2][8];
+                for (int cg = 0; cg < BN / 32; cg += 2) {
+                    float sv[4][8];
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) ld_cg_f8(base + q * MK_BM * 8, sv[q]);
-                    uint32_t v[16];
-                    acc_ld(ta + static_cast<uint32_t>(col0), kz, v);
+                    for (int k = 0; k < 2; ++k) {
+                        const int col0 = half * (BN / 2) + (cg + k) * 16;
+                        const float *base = S + (static_cast<size_t>(col0 >> 3) * MK_BM + row) * 8;
+                        ld_cg_f8(base, sv[2 * k]);
+                        ld_cg_f8(base + MK_BM * 8, sv[2 * k + 1]);
+                    }
 #pragma unroll
-                    for (int q = 0; q < 2; ++q)
+                    for (int k = 0; k < 2; ++k) {
+                        const int col0 = half * (BN / 2) + (cg + k) * 16;
+                        uint32_t v[16];
+                        acc_ld(ta + static_cast<uint32_t>(col0), kz, v);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)   // fp32 addition commutes bit for bit
-                            v[8 * q + j] = __float_as_uint(sv[q][j] + __uint_as_float(v[8 * q + j]));
-                    tmem_st16(ta + static_cast<uint32_t>(col0), v);
+                        for (int q = 0; q < 2; ++q)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)   // fp32 addition commutes bit for bit
+                                v[8 * q + j] = __float_as_uint(sv[2 * k + q][j] + __uint_as_float(v[8 * q + j]));
+                        tmem_st16(ta + static_cast<uint32_t>(col0), v);
+                    }
                 }
             }
         }
