@@ -206,11 +206,11 @@ def test_mid_workload_full_oracle_and_same_bits():
 
 
 @pytest.mark.parametrize("num_ctas", [4, 10, 34])
-@pytest.mark.parametrize("M", [256, 1024])   # tile owners; the rank-ordered chain
-def test_small_grids(num_ctas, M):
+@pytest.mark.parametrize("M,P", [(256, 4), (256, 8), (1024, 8)])   # tile owners; SM-pair units of all ranks
+def test_small_grids(num_ctas, M, P):
     """Few SM pairs, so that every pair claims many tiles (or units) one ahead of the one it
     computes: the result must not depend on the grid."""
-    P, N, Kr = 8, 1024, 128
+    N, Kr = 1024, 128
     wl = ig.Workload("ch_grid", "allreduce", P, M, N, Kr, ig.INTEGER_PM2, ig.INTEGER_PM2, "f32", seed=M + num_ctas)
     A, B, Ad, Bd = gu.upload(wl)
     ref = gu.rounded_reference(oracle.allreduce(A, B), False)
